@@ -1,0 +1,198 @@
+"""Pins of the oracle's attention, LM head, gather and storage decoding.
+
+Each check ties the oracle to something other than itself: a library routine
+computing a special case (torch CPU fp64 scaled_dot_product_attention, matmul,
+argmax), a hand-built value, or an equivalence the pages state (mlxcel PR #1212:
+prefix selection == trim_to, identity selection is a no-op, the tail form equals
+the absolute form, Int8 scale sidecars move with their tokens).
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from oracle import attention as oa
+from oracle import gather as og
+from oracle import lm_head as ol
+from oracle import storage as osd
+from oracle import tree as ot
+
+
+# ----------------------------------------------------------------------------- storage
+def test_storage_known_values():
+    assert list(osd.bf16([0x3F80, 0xC000, 0x3F81, 0x0000, 0x8000])) == [1.0, -2.0, 1.0078125, 0.0, -0.0]
+    assert list(osd.f16([0x3C00, 0xC000, 0x3C01, 0x0001])) == [1.0, -2.0, 1.0009765625, 2.0 ** -24]
+    v = osd.int8_scaled(np.array([[3, -127], [1, 0]], dtype=np.int8), np.array([0x3800, 0x4000], dtype=np.uint16))
+    assert v.tolist() == [[1.5, -63.5], [2.0, 0.0]]  # scales 0.5 and 2.0
+
+
+def test_q4_hand_built_group():
+    # byte 0x21 -> element 0 = 1 (low nibble), element 1 = 2 (high nibble)
+    assert osd.unpack_q4(np.array([[0x21, 0xF0]], dtype=np.uint8)).tolist() == [[1, 2, 0, 15]]
+    codes = np.arange(64) % 16
+    packed = (codes[0::2] | (codes[1::2] << 4)).astype(np.uint8)[None, :]
+    scale = np.array([[0x3F00]], dtype=np.uint16)  # 0.5
+    bias = np.array([[0xBF80]], dtype=np.uint16)   # -1.0
+    w = osd.q4_affine(packed, scale, bias)
+    assert w.shape == (1, 64)
+    assert np.array_equal(w[0], 0.5 * codes - 1.0)
+
+
+# ----------------------------------------------------------------------------- attention
+def torch_sdpa(q, k, v, allowed):
+    """torch CPU fp64 SDPA with a boolean mask; q [R, D], k/v [N, D], allowed [R, N]."""
+    t = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float64))[None, None]
+    out = torch.nn.functional.scaled_dot_product_attention(t(q), t(k), t(v), attn_mask=t(allowed).bool())
+    return out[0, 0].numpy()
+
+
+@pytest.mark.parametrize("S,T", [(0, 1), (5, 1), (17, 4), (64, 6)])
+def test_linear_tree_is_causal_sdpa(S, T):
+    rng = np.random.default_rng(S * 10 + T)
+    D = 16
+    q = rng.standard_normal((T, 1, D))
+    K = rng.standard_normal((1, S + T, D))
+    V = rng.standard_normal((1, S + T, D))
+    par = [-1] + list(range(T - 1))
+    out = oa.tree_verify_attention(q, K, V, par, S)
+    allowed = np.arange(S + T)[None, :] <= (np.arange(T)[:, None] + S)
+    ref = torch_sdpa(q[:, 0], K[0], V[0], allowed)
+    assert np.allclose(out[:, 0], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_tree_node_equals_causal_attention_over_its_root_path():
+    rng = np.random.default_rng(3)
+    par = [-1, 0, 0, 1, 1, 2, 2, 3, 5, 8]
+    T, S, D = len(par), 9, 8
+    q = rng.standard_normal((T, 1, D))
+    K = rng.standard_normal((1, S + T, D))
+    V = rng.standard_normal((1, S + T, D))
+    out = oa.tree_verify_attention(q, K, V, par, S)
+    for i in range(T):
+        path = sorted(ot.ancestors(par, i))
+        cols = list(range(S)) + [S + j for j in path]
+        # the node is the last element of its own root path: causal SDPA over that sequence
+        n = len(cols)
+        allowed = np.ones((1, n), dtype=bool)
+        ref = torch_sdpa(q[i, :, :], K[0, cols], V[0, cols], allowed)
+        assert np.allclose(out[i, 0], ref[0], rtol=1e-12, atol=1e-12)
+
+
+def test_dense_mask_form_equals_ancestor_form():
+    rng = np.random.default_rng(4)
+    par = [-1, 0, 0, 1, 1, 2, 2]
+    T, S, D = 7, 33, 8
+    K = rng.standard_normal((S + T, D))
+    V = rng.standard_normal((S + T, D))
+    m = ot.history_mask(par, S)
+    for i in range(T):
+        q = rng.standard_normal(D)
+        a = oa.attend_row(q, K, V, S, ot.ancestors(par, i))
+        b = oa.attend_dense_mask(q, K, V, m[i])
+        assert np.allclose(a, b, rtol=1e-12, atol=1e-12)
+
+
+def test_gqa_head_mapping_matches_repeat_interleave():
+    rng = np.random.default_rng(5)
+    T, HQ, HKV, S, D = 3, 6, 2, 10, 8
+    par = [-1, 0, 1]
+    q = rng.standard_normal((T, HQ, D))
+    K = rng.standard_normal((HKV, S + T, D))
+    V = rng.standard_normal((HKV, S + T, D))
+    out = oa.tree_verify_attention(q, K, V, par, S)
+    Kr = np.repeat(K, HQ // HKV, axis=0)  # query head h reads kv head h // G
+    Vr = np.repeat(V, HQ // HKV, axis=0)
+    allowed = np.arange(S + T)[None, :] <= (np.arange(T)[:, None] + S)
+    for h in range(HQ):
+        ref = torch_sdpa(q[:, h], Kr[h], Vr[h], allowed)
+        assert np.allclose(out[:, h], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_single_node_is_decode_attention():
+    rng = np.random.default_rng(6)
+    S, D = 50, 16
+    q = rng.standard_normal(D)
+    K = rng.standard_normal((S + 1, D))
+    V = rng.standard_normal((S + 1, D))
+    s = K @ q / math.sqrt(D)
+    p = np.exp(s - s.max())
+    ref = (p / p.sum()) @ V
+    assert np.allclose(oa.attend_row(q, K, V, S, {0}), ref, rtol=1e-13, atol=1e-13)
+
+
+# ----------------------------------------------------------------------------- LM head
+def test_argmax_matches_torch_fp64():
+    rng = np.random.default_rng(8)
+    W = rng.standard_normal((1000, 64))
+    h = rng.standard_normal((5, 64))
+    idx, top, gap = ol.argmax_gap(ol.logits(W, h))
+    lt = torch.from_numpy(h) @ torch.from_numpy(W).T
+    assert idx.tolist() == torch.argmax(lt, dim=1).tolist()
+    srt = torch.sort(lt, dim=1, descending=True).values
+    assert np.allclose(gap, (srt[:, 0] - srt[:, 1]).numpy(), rtol=0, atol=1e-12)
+
+
+def test_argmax_ties_go_to_lowest_index_and_streaming_agrees():
+    W = np.zeros((40000, 4))
+    W[[7, 20000, 39999], 0] = 2.0  # three-way tie
+    W[5, 0] = 1.5
+    h = np.array([[1.0, 0, 0, 0]])
+    idx, top, gap = ol.argmax_gap(ol.logits(W, h))
+    assert (idx[0], top[0], gap[0]) == (7, 2.0, 0.0)
+    a, t, g = ol.argmax_streamed(lambda r0, r1: W[r0:r1], h, W.shape[0])
+    assert (a[0], t[0], g[0]) == (7, 2.0, 0.0)
+    W[7, 0] = 1.0
+    a, t, g = ol.argmax_streamed(lambda r0, r1: W[r0:r1], h, W.shape[0])
+    assert (a[0], t[0], g[0]) == (20000, 2.0, 0.0)
+    rng = np.random.default_rng(9)
+    W2 = rng.standard_normal((50000, 8))
+    h2 = rng.standard_normal((3, 8))
+    a1 = ol.argmax_gap(ol.logits(W2, h2))
+    a2 = ol.argmax_streamed(lambda r0, r1: W2[r0:r1], h2, W2.shape[0])
+    assert np.array_equal(a1[0], a2[0])
+    assert np.allclose(a1[2], a2[2], rtol=0, atol=1e-12)
+
+
+# ----------------------------------------------------------------------------- gather
+def kv_fixture(n=12, D=8, seed=0):
+    rng = np.random.default_rng(seed)
+    codes = rng.integers(-127, 128, size=(n, D)).astype(np.int8)
+    # distinct per-token scales: a misplaced scale is caught, raw codes would not catch it
+    scales = (np.arange(n, dtype=np.float32) * 0.001 + 0.005).astype(np.float16).view(np.uint16)
+    return codes, scales
+
+
+def test_prefix_gather_equals_trim_to():
+    codes, scales = kv_fixture()
+    S = 5
+    for k in range(1, 8):
+        kept = list(range(k))
+        b, n = og.gather_within_tail(codes, S, kept)
+        assert n == S + k
+        assert np.array_equal(b[:n], og.trim_to(codes, n))
+        assert og.is_identity(kept)
+
+
+def test_identity_gather_is_a_no_op():
+    codes, scales = kv_fixture()
+    b, n = og.gather_within_tail(codes, 4, [0, 1, 2, 3, 4, 5, 6, 7])
+    assert n == 12 and np.array_equal(b, codes)
+
+
+def test_tail_form_equals_absolute_form_and_scales_move():
+    codes, scales = kv_fixture()
+    S, path = 4, [0, 2, 5, 7]
+    bc, n = og.gather_within_tail(codes, S, path)
+    bs, n2 = og.gather_within_tail(scales, S, path)
+    absolute = list(range(S)) + [S + p for p in path]
+    assert n == n2 == S + len(path)
+    assert np.array_equal(bc[:n], og.gather_positions(codes, absolute))
+    assert np.array_equal(bs[:n], og.gather_positions(scales, absolute))
+    # every kept token decodes against its own scale
+    vals = osd.int8_scaled(bc[:n], bs[:n])
+    ref = osd.int8_scaled(codes, scales)[absolute]
+    assert np.array_equal(vals, ref)
+    # rows past the new length keep their bytes (in-place tail rewrite)
+    assert np.array_equal(bc[n:], codes[n:])
+    assert not og.is_identity(path)
