@@ -1,0 +1,391 @@
+"""Benchmark of the tree-verify step: verified nodes/s and achieved HBM bandwidth.
+
+One step = one whole verify round on one batch of synthetic input: tree_mask -> tree_verify_attention over all
+16 layers -> lm_head_argmax -> tree_accept_walk -> kv_gather_positions, plus resetting kv_len to S + T (the
+round's tree block is considered appended; the gather advanced kv_len).  Default workload: a 3-node chain over a
+4096-token bf16 prefix at the 27B-like shape (16 layers, 24 q / 4 kv heads, D=256, hidden 5120, bf16 LM head
+248,320 x 5120); its inputs (2.81 GB per round) are larger than L2, so no flush is needed between steps.
+
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config I]
+Under torchrun every rank runs its own replica on its own GPU (the path has no exchange step); rank 0 prints
+one JSON line.  --impl reference times the fp64 CPU oracle on a bounded sample on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "tree-verify nodes/s per round and achieved HBM GB/s as fraction of GB300 peak"
+DEFAULT_CONFIG = 1
+
+# ncu dram bytes (read + write) per launch of the dominant kernel, with the source hash it was measured on
+# (a changed kernel source makes the number stale and it is reported as null).
+TRAFFIC = {}
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def src_hash(name):
+    p = os.path.join(ROOT, "tree_speculative_decoding_array_gb300", "csrc", name)
+    with open(p, "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+# ----------------------------------------------------------------------------- clocks
+REASON_BITS = {0x1: "gpu_idle", 0x2: "applications_clocks_setting", 0x4: "sw_power_cap", 0x8: "hw_slowdown",
+               0x10: "sync_boost", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+               0x80: "hw_power_brake_slowdown", 0x100: "display_clock_setting"}
+
+
+class ClockSampler:
+    def __init__(self, index: int):
+        self.index, self.proc, self.lines = index, None, []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index),
+                 "--query-gpu=clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 4:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                bits = int(parts[3], 16) if parts[3].startswith("0x") else int(parts[3])
+                for b, n in REASON_BITS.items():
+                    if bits & b:
+                        reasons.add(n)
+            except ValueError:
+                continue
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+
+    import tree_speculative_decoding_array_gb300 as tsv
+    from synth import configs
+    from synth.workload import Workload
+
+    tsv.load()
+    dev = f"cuda:{local_rank}"
+    torch.cuda.set_device(dev)
+    cfg = configs.CONFIGS[args.config]
+    round_id = args.round if args.round is not None else ({1: 2}.get(args.config, 0))
+    wl = Workload(cfg, device=dev, round_id=round_id)
+    vr = wl.vr
+    wl.save_tail()
+    moved = any(p != list(range(len(p))) for p in wl.round["paths"])
+    stream = torch.cuda.current_stream()
+    names = ["mask", "attn", "lm", "walk", "gather"]
+
+    def reset():
+        vr.kv_len.fill_(cfg.NKV)
+        if moved:
+            wl.restore_tail()
+
+    def step(evs=None):
+        reset()
+        for i, n in enumerate(names):
+            if evs is not None:
+                evs[i][0].record(stream)
+            vr.run(stages=(n,))
+            if evs is not None:
+                evs[i][1].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    ev = [[(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in names]
+          for _ in range(args.steps)]
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(torch.cuda.current_device()) as clk:
+        t0.record(stream)
+        for s in range(args.steps):
+            step(ev[s])
+        t1.record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    ms = t0.elapsed_time(t1)
+    per_kernel = {n: statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
+                  for i, n in enumerate(names)}
+    if world > 1:
+        t = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # correctness of the timed state: one more round, check it against the planted walk
+    step()
+    torch.cuda.synchronize()
+    got_len = vr.outs["path_len"].cpu().tolist()
+    want_len = [len(p) for p in wl.round["paths"]]
+    assert got_len == want_len, (got_len, want_len)
+
+    # e2e through the public API with host buffers: per step H2D of the round inputs, D2H of the results
+    e2e = run_e2e(args, wl, stream) if rank == 0 else None
+
+    # launches of our kernels per step
+    lm_groups = 0
+    left = cfg.rows
+    while left > 0:
+        g = 8 if left >= 8 else (4 if left >= 4 else left)
+        left -= g
+        lm_groups += 1
+    launches = 1 + (1 + (tsv.attention_workspace_size(vr.adesc) > 0)) + (lm_groups + 1) + 1 + 2
+    return dict(cfg=cfg, ms=ms, per_kernel=per_kernel, clocks=clk.summary(), e2e=e2e, launches=launches,
+                round_id=round_id)
+
+
+def run_e2e(args, wl, stream):
+    import torch
+
+    vr, cfg = wl.vr, wl.cfg
+    pin = lambda t: t.detach().cpu().pin_memory()
+    h_par, h_tok, h_hid = pin(vr.parents), pin(vr.tokens), pin(vr.hidden)
+    h_q = [pin(q) for q in vr.q]
+    outs = vr.outs
+    h_out = {k: torch.empty(outs[k].shape, dtype=outs[k].dtype).pin_memory() for k in ("path", "path_len", "emitted", "argmax")}
+    h2d = sum(t.numel() * t.element_size() for t in [h_par, h_tok, h_hid] + h_q)
+    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
+    moved = any(p != list(range(len(p))) for p in wl.round["paths"])
+
+    def e2e_step():
+        vr.kv_len.fill_(cfg.NKV)
+        if moved:
+            wl.restore_tail()
+        vr.parents.copy_(h_par, non_blocking=True)
+        vr.tokens.copy_(h_tok, non_blocking=True)
+        vr.hidden.copy_(h_hid, non_blocking=True)
+        for d, h in zip(vr.q, h_q):
+            d.copy_(h, non_blocking=True)
+        vr.run()
+        for k, h in h_out.items():
+            h.copy_(outs[k], non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 4)
+    t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0.record(stream)
+    for _ in range(n):
+        e2e_step()
+    t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1) / n
+    return {"value": cfg.rows / (ms * 1e-3), "unit": "nodes/s", "ms_per_step": ms, "steps": n,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+# ----------------------------------------------------------------------------- oracle on the host
+ORACLE_SAMPLE = r"""
+import json, os, sys, time
+sys.path.insert(0, {root!r})
+import numpy as np
+from oracle import attention as oa, lm_head as ol, storage as osd, tree as ot, gather as og
+from synth import configs, tensors, trees
+cfg = configs.CONFIGS[{cfg_idx}]
+r = trees.make_round(cfg, {round_id})
+par = r["parents"][0].tolist()
+# inputs for the sample (untimed): one (layer, kv head) unit of attention, a slice of the LM head
+K = osd.kv_values(cfg.kv_dtype, tensors.kv_rows(cfg, "k", 0, 0, 0, 0, cfg.NKV),
+                  tensors.kv_scales(cfg, "k", 0, 0, 0, 0, cfg.NKV) if cfg.kv_dtype == configs.I8 else None)
+V = osd.kv_values(cfg.kv_dtype, tensors.kv_rows(cfg, "v", 0, 0, 0, 0, cfg.NKV),
+                  tensors.kv_scales(cfg, "v", 0, 0, 0, 0, cfg.NKV) if cfg.kv_dtype == configs.I8 else None)
+G = cfg.G
+q = {{i: osd.bf16(tensors.q_rows(cfg, 0, 0, i, list(range(G)))) for i in range(cfg.T)}}
+vr = {vocab_rows}
+if cfg.w_dtype == configs.Q4:
+    s_, b_ = tensors.wq_scales_biases(cfg, np.arange(vr))
+    Wst = (tensors.wq_packed(cfg, np.arange(vr)), s_, b_)
+else:
+    Wst = tensors.w_rows(cfg, np.arange(vr))
+h = osd.bf16(r["hidden"][:cfg.T])
+def attn_unit():
+    for i in range(cfg.T):
+        vis = ot.ancestors(par, i)
+        for g in range(G):
+            oa.attend_row(q[i][g], K, V, cfg.S, vis)
+def lm_slice():
+    W = osd.q4_affine(*Wst) if cfg.w_dtype == configs.Q4 else (osd.bf16(Wst) if cfg.w_dtype == configs.BF16 else osd.f16(Wst))
+    return ol.argmax_gap(ol.logits(W, h))
+def timed(f, budget):
+    n, t0 = 0, time.perf_counter()
+    while True:
+        f(); n += 1
+        dt = time.perf_counter() - t0
+        if dt > budget: return dt / n, n
+t_mask = timed(lambda: [ot.ancestor_bits(par)], 0.5)[0]
+t_attn, n_attn = timed(attn_unit, {budget})
+t_lm, n_lm = timed(lm_slice, {budget})
+t_walk = timed(lambda: ot.accept_walk(r["targets"][0], r["tokens"][0], par), 0.5)[0]
+blk = tensors.kv_rows(cfg, "k", 0, 0, 0, cfg.S, cfg.NKV)
+t_gather = timed(lambda: og.gather_within_tail(blk, 0, r["paths"][0]), 0.5)[0]
+units = cfg.n_layers * cfg.B * cfg.HKV
+t_round = cfg.B * t_mask + units * t_attn + (cfg.V / vr) * cfg.B * t_lm + cfg.B * t_walk + 2 * units * t_gather
+print(json.dumps(dict(t_round=t_round, t_attn_unit=t_attn, t_lm_slice=t_lm, vocab_rows=vr, units=units,
+                      n_attn=n_attn, n_lm=n_lm)))
+"""
+
+
+def run_oracle(cfg_idx, round_id, budget=6.0, vocab_rows=16384):
+    code = ORACLE_SAMPLE.format(root=ROOT, cfg_idx=cfg_idx, round_id=round_id, vocab_rows=vocab_rows, budget=budget)
+    env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    t0 = time.perf_counter()
+    r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
+    wall = time.perf_counter() - t0
+    if r.returncode != 0:
+        raise RuntimeError(f"oracle sample failed:\n{r.stderr[-2000:]}")
+    res = json.loads(r.stdout.strip().splitlines()[-1])
+    from synth import configs
+
+    cfg = configs.CONFIGS[cfg_idx]
+    res["nodes_per_s"] = cfg.rows / res["t_round"]
+    res["wall_s"] = wall
+    res["sample"] = (f"one (layer, seq, kv head) attention unit over {cfg.NKV} keys (x{res['units']} units) and "
+                     f"{vocab_rows} of {cfg.V} LM-head rows for one sequence's {cfg.T} nodes (x{cfg.V / vocab_rows:.1f}"
+                     f" x{cfg.B} seqs), plus mask/walk/gather, single thread, extrapolated to one round")
+    return res
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--round", type=int, default=None)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    from synth import configs
+
+    cfg = configs.CONFIGS[args.config]
+    config = {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "layers": cfg.n_layers, "HQ": cfg.HQ, "HKV": cfg.HKV,
+              "D": cfg.D, "S": cfg.S, "H": cfg.H, "V": cfg.V, "kv": configs.DTYPE_NAMES[cfg.kv_dtype],
+              "lm_head": configs.DTYPE_NAMES[cfg.w_dtype], "topology": cfg.topology,
+              "l2": f"inputs larger than L2 ({cfg.algorithmic_bytes() / 1e9:.2f} GB read per round), no flush",
+              "parallelism": f"replicas x{args.gpus}"}
+    round_id = args.round if args.round is not None else ({1: 2}.get(args.config, 0))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        res = run_oracle(args.config, round_id)
+        v = res["nodes_per_s"] * 1
+        line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "nodes/s", "n_gpus": args.gpus,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": res["t_round"] * 1e3,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": config,
+                "cpu_baseline": {"value": v, "unit": "nodes/s", "cores": 1, "kind": "oracle", "sample": res["sample"]},
+                "e2e": {"value": v, "unit": "nodes/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line))
+        return
+
+    import torch
+
+    if world > 1:
+        torch.distributed.init_process_group("nccl")
+    r = run_ours(args, rank, world, local_rank)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    if rank != 0:
+        return
+    cfg = r["cfg"]
+    ms_step = r["ms"] / args.steps
+    nodes_per_s = world * cfg.rows * args.steps / (r["ms"] * 1e-3)
+    peak, peak_kind = peaks()
+    round_gbs = cfg.algorithmic_bytes() / (ms_step * 1e-3) / 1e9
+    # dominant kernel: the LM head when its bytes dominate, else attention
+    dom = "lm" if cfg.lm_bytes() >= cfg.kv_bytes() + cfg.kv_scale_bytes() else "attn"
+    dom_bytes = cfg.lm_bytes() if dom == "lm" else cfg.kv_bytes() + cfg.kv_scale_bytes()
+    dom_ms = r["per_kernel"][dom]
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    src = {"lm": "lm_head.cu", "attn": "attention.cu"}[dom]
+    tr = TRAFFIC.get((cfg.name, src))
+    traffic = tr["bytes"] if tr and tr["hash"] == src_hash(src) else None
+    line = {
+        "metric": METRIC, "value": nodes_per_s, "unit": "nodes/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded SplitMix64 inputs, planted argmax)",
+        "config": config,
+        "rounds_per_s": world * args.steps / (r["ms"] * 1e-3),
+        "hbm": {"algorithmic_bytes_per_round": cfg.algorithmic_bytes(), "achieved_gbs": round_gbs,
+                "frac_of_peak": round_gbs / peak, "peak_gbs": peak, "peak_kind": peak_kind},
+        "roofline": {"kernel": {"lm": "lm_head_argmax", "attn": "tree_verify_attention"}[dom], "bound": "hbm",
+                     "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+                     "traffic": traffic, "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
+                     "peak_kind": peak_kind},
+        "kernels_ms": r["per_kernel"],
+        "gpu_launches": r["launches"] * args.steps,
+        "clocks": r["clocks"],
+        "e2e": r["e2e"],
+    }
+    if not args.no_cpu_baseline:
+        try:
+            o = run_oracle(args.config, r["round_id"])
+            line["cpu_baseline"] = {"value": o["nodes_per_s"], "unit": "nodes/s", "cores": 1, "kind": "oracle",
+                                    "sample": o["sample"]}
+        except Exception as e:  # the baseline is reported, never required for our number
+            line["cpu_baseline"] = {"value": None, "unit": "nodes/s", "cores": 1, "kind": "oracle",
+                                    "sample": f"failed: {e}"[:300]}
+    print(json.dumps(line))
+
+
+if __name__ == "__main__":
+    main()

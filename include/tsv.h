@@ -1,0 +1,218 @@
+/*
+ * tsv.h - C ABI of the tree speculative-decoding verify step on GB300 (sm_103a).
+ *
+ * One verify round of tree speculative decoding, as five calls on one CUDA
+ * stream (mask -> attention for every layer -> LM head + argmax -> accept walk
+ * -> KV compaction).  The operations follow these pages:
+ *
+ *   [1204] mlxcel issue #1204, "perf(speculative): draft a tree instead of a
+ *          chain, so an MTP round emits more than 2.33 tokens"
+ *   [1212] mlxcel PR #1212, "feat(speculative): draft and verify a token tree,
+ *          behind a flag, default off" (its commit messages)
+ *   [1185] mlxcel issue #1185, "perf(speculative): cut the MTP drafter's
+ *          per-step cost, now the binding constraint on M5-class hardware"
+ *   [728]  Splash issue #728, "Experiment: qualify shared-prefix tree
+ *          verification and conservative admission"
+ *
+ * Conventions shared by every call
+ * --------------------------------
+ * Ownership: every array argument is caller-owned memory.  Unless a parameter
+ *   says "host", it is DEVICE memory of the current CUDA device.  The library
+ *   keeps no pointer after a call returns and allocates no device memory;
+ *   scratch comes from a caller-provided workspace whose size the matching
+ *   *_workspace_size() call returns.
+ * Streams: every call only enqueues work on `stream` (0 = legacy default
+ *   stream) and returns without synchronising.  Results are ready when the
+ *   stream reaches them.
+ * Host errors: a call returns TSV_OK when its work was enqueued.  Any other
+ *   status means nothing was enqueued; tsv_last_error() then names the reason
+ *   (a per-thread string, valid until the next call on the same thread).
+ *   TSV_EUNSUPPORTED is a refusal ([1212], gather_positions commit: a layout
+ *   the operation cannot serve refuses with a message, and the caller must
+ *   decline tree drafting rather than proceed).
+ * Device errors: topology or path errors that only the device can see are
+ *   written to `dev_status` (int32[4], device memory) and never trap: word 0
+ *   receives the first TSV_DEV_* code (atomic compare-and-swap from 0, so it
+ *   is sticky), words 1..2 the sequence and node/position where it was found.
+ *   The caller zeroes the words once and reads them whenever it chooses;
+ *   outputs of a sequence with an error are unspecified (but in bounds).
+ *   dev_status may be NULL, in which case device errors are dropped.
+ * Sizes: 1 <= T <= 64 (one 64-bit ancestor word per node; tsv_tree_mask also
+ *   accepts T == 0).  Layout shapes are row-major, innermost last.
+ */
+#ifndef TSV_H
+#define TSV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    TSV_OK = 0,
+    TSV_EINVAL = 1,       /* bad argument: null pointer, size out of range, misaligned buffer */
+    TSV_ETOPOLOGY = 2,    /* a host-visible topology error */
+    TSV_EUNSUPPORTED = 3, /* a format or shape this build refuses (the caller must decline) */
+    TSV_ECAPACITY = 4,    /* workspace too small, or a size above a compiled maximum */
+    TSV_ECUDA = 5         /* the CUDA runtime reported an error while enqueueing */
+} tsv_status;
+
+typedef enum {
+    TSV_F16 = 0,       /* IEEE binary16 */
+    TSV_BF16 = 1,      /* bfloat16 */
+    TSV_I8_SCALED = 2, /* int8 code x fp16 per-token scale (KV caches only) */
+    TSV_Q4_G64 = 3     /* 4-bit affine, groups of 64 input features (LM head only) */
+} tsv_dtype;
+
+/* Device status codes (dev_status word 0). */
+#define TSV_DEV_OK 0
+#define TSV_DEV_BAD_ROOT 1    /* parents[b][0] != -1 */
+#define TSV_DEV_BAD_PARENT 2  /* parents[b][i] outside [0, i) for i >= 1 */
+#define TSV_DEV_BAD_PATH 3    /* path not strictly increasing from 0, or path_len outside [1, T] */
+#define TSV_DEV_BAD_KV_LEN 4  /* kv_len[b] < T, or kv_len[b] > capacity */
+
+#define TSV_MAX_T 64
+#define TSV_MAX_LAYERS 64
+
+/* Reason for the last non-TSV_OK status returned on this thread ("" if none). */
+const char* tsv_last_error(void);
+
+/* ABI version of this library (major * 100 + minor). */
+int tsv_version(void);
+
+/*
+ * tsv_tree_mask - topology check, ancestor bitmask and depth of every node.
+ *   [1204] "What this needs" item 1: each node attends to its ancestors only,
+ *   rebuilt every round from the topology; [1204] "Increment 1": nodes in
+ *   topological order with parents[i] < i; [1212] history-mask commit: the
+ *   [n, offset + n] additive form, history columns attended in full; [1212]
+ *   verify commit: blocked entries are -1e9, never -inf.
+ *
+ *   parents    int32 [B, T]   parents[b][0] == -1, 0 <= parents[b][i] < i.
+ *   anc        uint64 [B, T]  out: bit j of anc[b][i] set iff node j is an
+ *                             ancestor of node i or i itself.
+ *   depth      int32 [B, T]   out: edges from the root (root = 0).
+ *   dense_mask float [B, T, mask_offset + T] or NULL; out: the additive mask
+ *                             (0 = attend, -1e9 = blocked) for a history of
+ *                             mask_offset positions.  Provided for parity
+ *                             checks; the attention call never reads it.
+ *   Device errors: TSV_DEV_BAD_ROOT / TSV_DEV_BAD_PARENT; that sequence's anc
+ *   and depth are then 0 / -1.
+ */
+tsv_status tsv_tree_mask(const int32_t* parents, int32_t B, int32_t T, uint64_t* anc, int32_t* depth,
+                         float* dense_mask, int32_t mask_offset, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * Tree-masked GQA attention of the verify block, for n_layers layers at once.
+ *   [1204] "What this needs" item 1 and "Increment 3"; [1212] history-mask and
+ *   verify_forward_with_mask commits; [728] "Earlier shader evidence" (split-KV
+ *   attention with fp32 partials and statistics, 16 nodes x 24 heads x D256).
+ *   For every layer l, sequence b, query head h and node i:
+ *     O[b,i,h,:] = sum_c p_c V[b, h/G, c, :],  p = softmax_c( Q[b,i,h,:] . K[b,h/G,c,:] / sqrt(D) )
+ *   over c in [0, S_b) and c = S_b + j for every j set in anc[b][i], where
+ *   S_b = kv_len[b] - T (the block was appended in topological order at
+ *   [S_b, S_b + T)).  G = HQ / HKV.  Int8: K = code * k_scale[c], V = code * v_scale[c].
+ *   Accumulation is fp32; O is rounded to bf16 once.
+ */
+typedef struct {
+    int32_t n_layers;   /* 1 .. TSV_MAX_LAYERS */
+    int32_t B, T, HQ, HKV, D; /* HQ % HKV == 0; D in {64, 128, 256} */
+    int64_t s_cap;      /* capacity of every cache buffer's sequence axis, in positions */
+    int32_t max_kv_len; /* host-known upper bound of every kv_len[b] (<= s_cap); sizes the grid */
+    int32_t kv_dtype;   /* TSV_F16, TSV_BF16 or TSV_I8_SCALED */
+    int32_t splits;     /* key-range splits per (layer, sequence, kv head); 0 = automatic */
+    int32_t reserved;
+    const void* q[TSV_MAX_LAYERS];       /* per layer: bf16 [B, T, HQ, D] */
+    const void* k[TSV_MAX_LAYERS];       /* per layer: [B, HKV, s_cap, D] in kv_dtype (int8 codes) */
+    const void* v[TSV_MAX_LAYERS];       /* per layer: as k */
+    const void* k_scale[TSV_MAX_LAYERS]; /* per layer: fp16 [B, HKV, s_cap] (Int8 only, else NULL) */
+    const void* v_scale[TSV_MAX_LAYERS]; /* per layer: as k_scale */
+    void* o[TSV_MAX_LAYERS];             /* per layer: bf16 [B, T, HQ, D], out */
+    const int32_t* kv_len;               /* int32 [B]: S_b + T */
+    const uint64_t* anc;                 /* uint64 [B, T] from tsv_tree_mask */
+} tsv_attn_desc;
+
+size_t tsv_attention_workspace_size(const tsv_attn_desc* d);
+
+/* Device errors: TSV_DEV_BAD_KV_LEN (that sequence's outputs are left unwritten). */
+tsv_status tsv_tree_verify_attention(const tsv_attn_desc* d, void* workspace, size_t ws_bytes,
+                                     int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * tsv_lm_head_argmax - LM-head projection fused with a greedy argmax; the
+ * logits are never written.  [1185] "Phase 2" item 2a (fused projection and
+ * argmax at temperature 0) and "Phase 3" (affine group-64 4-bit weights with
+ * scales and biases); [1204] "What this needs" item 2 (one target argmax per
+ * verified position).
+ *   hidden  bf16 [rows, H]
+ *   W       TSV_F16 / TSV_BF16: [V, H].  TSV_Q4_G64: uint8 [V, H/2], byte j of a
+ *           row holds element 2j in its low nibble and 2j+1 in its high nibble;
+ *           scales, biases: bf16 [V, H/64]; w = scale * q + bias, q in [0, 15].
+ *   argmax  int32 [rows], out: index of the largest logit, ties -> lowest index.
+ *   maxlogit float [rows] or NULL, out: that logit (fp32 accumulation).
+ *   H % 64 == 0 (H % 256 == 0 for TSV_F16/TSV_BF16), 1 <= V < 2^31, rows >= 1.
+ */
+size_t tsv_lm_head_workspace_size(int32_t rows, int32_t V);
+
+tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32_t H, int32_t V, int32_t w_dtype,
+                              const void* W, const void* scales, const void* biases, int32_t* argmax,
+                              float* maxlogit, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * tsv_tree_accept_walk - descend the tree along the target's argmaxes.
+ *   [1204] "What this needs" item 2 and "Increment 1" (the accepted set is a
+ *   path, never a subtree); [1212] first commit; [728] "What it does" (every
+ *   committed token is the target's selection at its path node).
+ *   From u = 0: take the lowest-index child c of u with tokens[c] == argmax[u],
+ *   append it, repeat; stop when no child matches.
+ *   argmax, tokens, parents  int32 [B, T]
+ *   path      int32 [B, T] out: accepted nodes from the root, -1 padded.
+ *   path_len  int32 [B]    out: accepted + 1.
+ *   emitted   int32 [B, T] out: argmax[path[j]] for j < path_len, -1 padded.
+ *   Device errors: TSV_DEV_BAD_ROOT / TSV_DEV_BAD_PARENT (that sequence gets
+ *   path = [0], path_len = 1).
+ */
+tsv_status tsv_tree_accept_walk(const int32_t* argmax, const int32_t* tokens, const int32_t* parents, int32_t B,
+                                int32_t T, int32_t* path, int32_t* path_len, int32_t* emitted, int32_t* dev_status,
+                                cudaStream_t stream);
+
+/*
+ * tsv_kv_gather_positions - compact the verify block of every cache to the
+ * accepted path, in place.  [1204] "The rollback constraint, which decides
+ * feasibility"; [1212] gather_positions commit (Int8 scale sidecars move with
+ * their tokens; a prefix selection equals trim_to; the identity selection
+ * short-circuits) and gather_within_tail commit (only [tail_start, tail_start
+ * + kept_len) is rewritten; cost scales with the block, not the context).
+ *   For every layer, sequence b and kv head, with S = kv_len[b] - T:
+ *     rows S + j <- rows S + path[b][j] for j < path_len[b] (K, V and, for
+ *     Int8, k_scale and v_scale); then kv_len[b] = S + path_len[b].
+ *   Rows below S and at or beyond the new kv_len are not written.  When
+ *   path[b][j] == j for every j, no cache byte is moved.
+ *   path: strictly increasing with path[b][0] == 0 (every root path of a
+ *   topological tree is), 1 <= path_len[b] <= T.
+ *   Device errors: TSV_DEV_BAD_PATH, TSV_DEV_BAD_KV_LEN (that sequence is left
+ *   untouched, kv_len included).
+ */
+typedef struct {
+    int32_t n_layers, B, HKV, D;
+    int64_t s_cap;
+    int32_t kv_dtype; /* TSV_F16, TSV_BF16 or TSV_I8_SCALED */
+    int32_t reserved;
+    void* k[TSV_MAX_LAYERS];       /* per layer: [B, HKV, s_cap, D] */
+    void* v[TSV_MAX_LAYERS];
+    void* k_scale[TSV_MAX_LAYERS]; /* per layer: fp16 [B, HKV, s_cap] (Int8 only) */
+    void* v_scale[TSV_MAX_LAYERS];
+} tsv_kv_desc;
+
+tsv_status tsv_kv_gather_positions(const tsv_kv_desc* kv, int32_t* kv_len, const int32_t* path,
+                                   const int32_t* path_len, int32_t T, int32_t* dev_status, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TSV_H */

@@ -1,0 +1,70 @@
+"""Device buffers of one synthetic verify round, ready for the tsv calls.
+
+Caches, Q and the LM head are filled on the device by ``synth.device``; the
+round's tree, tokens and planted hidden states come from ``synth.trees`` on the
+host and are uploaded.  ``kv_len`` starts at S + T (the block was appended).
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from . import device as sd
+from . import trees
+from .configs import I8, Config
+
+
+def bits_to_bf16(bits: np.ndarray, device) -> torch.Tensor:
+    return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
+
+
+class Workload:
+    """All device tensors of ``cfg`` (optionally a subset of layers, extra capacity)."""
+
+    def __init__(self, cfg: Config, device="cuda", round_id: int = 0, n_layers: int | None = None,
+                 s_cap: int | None = None, splits: int = 0):
+        from tree_speculative_decoding_array_gb300 import VerifyRound
+
+        self.cfg = cfg
+        self.device = device
+        L = n_layers or cfg.n_layers
+        self.s_cap = s_cap or cfg.NKV
+        self.caches = [sd.alloc_cache(cfg, l, self.s_cap, device) for l in range(L)]
+        self.q = [sd.alloc_q(cfg, l, device) for l in range(L)]
+        self.head = sd.alloc_head(cfg, device)
+        self.round = trees.make_round(cfg, round_id)
+        r = self.round
+        self.parents = torch.from_numpy(r["parents"]).to(device)
+        self.tokens = torch.from_numpy(r["tokens"]).to(device)
+        self.hidden = bits_to_bf16(r["hidden"], device)
+        self.kv_len = torch.full((cfg.B,), cfg.NKV, dtype=torch.int32, device=device)
+        i8 = cfg.kv_dtype == I8
+        self.vr = VerifyRound(
+            T=cfg.T, HQ=cfg.HQ, HKV=cfg.HKV, D=cfg.D, V=cfg.V, kv_dtype=cfg.kv_dtype, w_dtype=cfg.w_dtype,
+            max_kv_len=self.s_cap, parents=self.parents, tokens=self.tokens, q=self.q,
+            k=[c["k"] for c in self.caches], v=[c["v"] for c in self.caches], hidden=self.hidden,
+            W=self.head["W"], kv_len=self.kv_len,
+            k_scale=[c["ks"] for c in self.caches] if i8 else None,
+            v_scale=[c["vs"] for c in self.caches] if i8 else None,
+            w_scales=self.head["scales"], w_biases=self.head["biases"], splits=splits)
+        self._tail = None
+
+    def set_round(self, round_id: int):
+        """Load another round's tree, tokens and hidden states (same caches and head)."""
+        self.round = trees.make_round(self.cfg, round_id)
+        r = self.round
+        self.parents.copy_(torch.from_numpy(r["parents"]))
+        self.tokens.copy_(torch.from_numpy(r["tokens"]))
+        self.hidden.copy_(bits_to_bf16(r["hidden"], "cpu"))
+
+    def save_tail(self):
+        """Keep a copy of the verify block [S, S+T) of every cache (the gather rewrites it)."""
+        S, T = self.cfg.S, self.cfg.T
+        self._tail = [{k: (t[:, :, S:S + T].clone()) for k, t in c.items()} for c in self.caches]
+
+    def restore_tail(self):
+        S, T = self.cfg.S, self.cfg.T
+        for c, saved in zip(self.caches, self._tail):
+            for k, t in c.items():
+                t[:, :, S:S + T].copy_(saved[k])
+        self.kv_len.fill_(self.cfg.NKV)

@@ -1,0 +1,195 @@
+"""Comparisons of one GPU verify round against the fp64 oracle (test infrastructure).
+
+Inputs for the oracle are regenerated on the host from the seeded generator
+(``synth.tensors``); nothing the oracle sees comes from the GPU.  Tolerances:
+attention within 2e-2 max-abs and 1e-2 relative L2 (bf16 output); argmax
+exact (every node is planted with a top-1/top-2 gap of at least 1e-2);
+mask, walk, path and gathered cache bytes bit-exact.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+from oracle import attention as oa
+from oracle import gather as og
+from oracle import lm_head as ol
+from oracle import storage as osd
+from oracle import tree as ot
+from synth import configs, tensors
+
+ATT_MAX_ABS = 2e-2
+ATT_REL_L2 = 1e-2
+
+
+def u64(t: torch.Tensor) -> list[int]:
+    return [int(x) & ((1 << 64) - 1) for x in t.cpu().numpy().reshape(-1).tolist()]
+
+
+def bf16_tensor_to_f64(t: torch.Tensor) -> np.ndarray:
+    return osd.bf16(t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16))
+
+
+# ----------------------------------------------------------------------------- per-step oracles
+def oracle_mask(parents: np.ndarray):
+    B, T = parents.shape
+    anc = [ot.ancestor_bits(parents[b].tolist()) for b in range(B)]
+    depth = [[ot.depth(parents[b].tolist(), i) for i in range(T)] for b in range(B)]
+    return anc, depth
+
+
+def kv_values(cfg, layer, b, kvh):
+    """fp64 K and V of one (layer, sequence, kv head) over the logical S + T rows."""
+    out = []
+    for w in ("k", "v"):
+        store = tensors.kv_rows(cfg, w, layer, b, kvh, 0, cfg.NKV)
+        sc = tensors.kv_scales(cfg, w, layer, b, kvh, 0, cfg.NKV) if cfg.kv_dtype == configs.I8 else None
+        out.append(osd.kv_values(cfg.kv_dtype, store, sc))
+    return out
+
+
+def oracle_attention_rows(cfg, layer, b, kvh, nodes, parents_b):
+    """O rows for every (node in nodes, head of the kv group) -> dict[(i, h)] = fp64 [D]."""
+    K, V = kv_values(cfg, layer, b, kvh)
+    G = cfg.G
+    heads = [kvh * G + g for g in range(G)]
+    res = {}
+    for i in nodes:
+        q = osd.bf16(tensors.q_rows(cfg, layer, b, i, heads))
+        vis = ot.ancestors(parents_b, i)
+        for gi, h in enumerate(heads):
+            res[(i, h)] = oa.attend_row(q[gi], K, V, cfg.S, vis)
+    return res
+
+
+def head_rows_fn(cfg):
+    if cfg.w_dtype == configs.Q4:
+        def wr(r0, r1):
+            rows = np.arange(r0, r1)
+            s, b = tensors.wq_scales_biases(cfg, rows)
+            return osd.q4_affine(tensors.wq_packed(cfg, rows), s, b)
+        return wr
+    dec = osd.bf16 if cfg.w_dtype == configs.BF16 else osd.f16
+    return lambda r0, r1: dec(tensors.w_rows(cfg, np.arange(r0, r1)))
+
+
+def oracle_lm_full(cfg, hidden_bits):
+    h = osd.bf16(hidden_bits)
+    return ol.argmax_streamed(head_rows_fn(cfg), h, cfg.V)
+
+
+def oracle_logits_at(cfg, hidden_bits_row, vocab_rows):
+    wr = head_rows_fn(cfg)
+    W = np.concatenate([wr(int(v), int(v) + 1) for v in vocab_rows])
+    return W @ osd.bf16(hidden_bits_row)
+
+
+# ----------------------------------------------------------------------------- comparison of a round
+def attn_stats(gpu: np.ndarray, ref: np.ndarray):
+    err = np.abs(gpu - ref)
+    rel = float(np.linalg.norm(gpu - ref) / max(np.linalg.norm(ref), 1e-30))
+    return float(err.max()), rel
+
+
+def check_round(wl, out, layers=(0,), attn_rows="all", lm="auto", kv_heads=None, seqs=None, rng_seed=0):
+    """Compare every output of one round on ``wl`` (a synth.workload.Workload) with the oracle.
+
+    attn_rows: "all" (every node), or an int = number of nodes sampled per (layer, seq, kv head).
+    lm: "full" (oracle argmax over the whole vocabulary), "planted" (argmax == planted target, oracle logit of
+        it == maxlogit, sampled vocabulary rows below it), or "auto" (full when V <= 65536).
+    """
+    cfg = wl.cfg
+    r = wl.round
+    rng = np.random.default_rng(rng_seed)
+    parents = r["parents"]
+    B, T = parents.shape
+    rep = {"ok": True}
+
+    # a1 mask
+    anc, depth = oracle_mask(parents)
+    g_anc = u64(out["anc"])
+    g_depth = out["depth"].cpu().numpy().reshape(-1).tolist()
+    rep["mask_exact"] = g_anc == [a for row in anc for a in row] and g_depth == [d for row in depth for d in row]
+
+    # a2 attention (sampled (layer, seq, kv head) units; all or sampled nodes)
+    seqs = list(range(B)) if seqs is None else seqs
+    kv_heads = list(range(cfg.HKV)) if kv_heads is None else kv_heads
+    worst_abs, worst_rel = 0.0, 0.0
+    for layer in layers:
+        o = bf16_tensor_to_f64(out["o"][layer])
+        for b in seqs:
+            for kvh in kv_heads:
+                nodes = list(range(T)) if attn_rows == "all" else sorted(
+                    set(rng.choice(T, size=min(T, int(attn_rows)), replace=False).tolist()) | {T - 1})
+                ref = oracle_attention_rows(cfg, layer, b, kvh, nodes, parents[b].tolist())
+                g = np.stack([o[b, i, h] for (i, h) in ref])
+                e = np.stack(list(ref.values()))
+                a, rl = attn_stats(g, e)
+                worst_abs, worst_rel = max(worst_abs, a), max(worst_rel, rl)
+    rep["attn_max_abs"], rep["attn_rel_l2"] = worst_abs, worst_rel
+    rep["attn_ok"] = worst_abs <= ATT_MAX_ABS and worst_rel <= ATT_REL_L2
+
+    # a3 LM head
+    g_arg = out["argmax"].cpu().numpy().astype(np.int64)
+    g_max = out["maxlogit"].cpu().numpy().astype(np.float64)
+    targets = r["targets"].reshape(-1).astype(np.int64)
+    mode = lm if lm != "auto" else ("full" if cfg.V <= 65536 else "planted")
+    if mode == "full":
+        o_arg, o_top, o_gap = oracle_lm_full(cfg, r["hidden"])
+        rep["lm_gap_min"] = float(o_gap.min())
+        rep["lm_exact"] = bool(np.array_equal(g_arg, o_arg)) and bool(np.array_equal(o_arg, targets))
+        rep["lm_maxlogit_err"] = float(np.max(np.abs(g_max - o_top)))
+    else:
+        rep["lm_exact"] = bool(np.array_equal(g_arg, targets))
+        errs, below = [], True
+        sample_rows = rng.choice(B * T, size=min(B * T, 8), replace=False)
+        for row in sample_rows:
+            vs = np.unique(np.concatenate([[targets[row]], rng.integers(0, cfg.V, size=512)]))
+            lg = oracle_logits_at(cfg, r["hidden"][row], vs)
+            top = lg[np.searchsorted(vs, targets[row])]
+            errs.append(abs(top - g_max[row]))
+            below &= bool(np.all(lg[vs != targets[row]] < top - cfg.min_gap))
+        rep["lm_maxlogit_err"] = float(max(errs))
+        rep["lm_sampled_below"] = below
+    rep["lm_ok"] = rep["lm_exact"] and rep["lm_maxlogit_err"] <= 1e-3 * (1 + float(np.max(np.abs(g_max)))) \
+        and rep.get("lm_sampled_below", True)
+
+    # a4 walk (on the oracle's argmax == the planted targets)
+    g_path = out["path"].cpu().numpy()
+    g_len = out["path_len"].cpu().numpy()
+    g_em = out["emitted"].cpu().numpy()
+    walk_ok = True
+    for b in range(B):
+        path, em = ot.accept_walk(r["targets"][b], r["tokens"][b], parents[b])
+        walk_ok &= g_len[b] == len(path) and g_path[b, :len(path)].tolist() == path \
+            and bool(np.all(g_path[b, len(path):] == -1)) and g_em[b, :len(path)].tolist() == em \
+            and path == r["paths"][b]
+    rep["walk_exact"] = bool(walk_ok)
+
+    # a5 gather (the caches were compacted in place by the round)
+    kvl = wl.kv_len.cpu().numpy()
+    gather_ok = True
+    S = cfg.S
+    for layer in layers:
+        c = wl.caches[layer]
+        for b in seqs:
+            path = r["paths"][b]
+            gather_ok &= int(kvl[b]) == S + len(path)
+            for kvh in kv_heads:
+                for w, key in (("k", "k"), ("v", "v")):
+                    orig = tensors.kv_rows(cfg, w, layer, b, kvh, S, S + T)
+                    exp, _ = og.gather_within_tail(orig, 0, path)
+                    got = c[key][b, kvh, S:S + T].cpu()
+                    got = got.view(torch.int8).numpy() if cfg.kv_dtype == configs.I8 else \
+                        got.view(torch.int16).numpy().view(np.uint16)
+                    gather_ok &= np.array_equal(got, exp)
+                    if cfg.kv_dtype == configs.I8:
+                        so = tensors.kv_scales(cfg, w, layer, b, kvh, S, S + T)
+                        se, _ = og.gather_within_tail(so, 0, path)
+                        gs = c["ks" if w == "k" else "vs"][b, kvh, S:S + T].cpu().view(torch.int16).numpy().view(np.uint16)
+                        gather_ok &= np.array_equal(gs, se)
+    rep["gather_exact"] = bool(gather_ok)
+    rep["dev_status"] = out["status"].cpu().tolist()
+    rep["ok"] = bool(rep["mask_exact"] and rep["attn_ok"] and rep["lm_ok"] and rep["walk_exact"]
+                     and rep["gather_exact"] and rep["dev_status"][0] == 0)
+    return rep

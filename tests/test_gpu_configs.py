@@ -1,0 +1,142 @@
+"""GPU parity at the five workloads' full sizes, in the launch configuration the bench times.
+
+Every output is checked on the oracle's side from host-regenerated inputs: the mask, walk, path and gathered
+bytes bit-exactly; attention on sampled (layer, sequence, kv head, node) rows within 2e-2 max-abs / 1e-2
+relative L2; the argmax exactly (full-vocabulary oracle argmax for the chain and 16-node workloads, planted
+target plus sampled vocabulary rows for the larger ones).
+"""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+from synth import configs, device as sd
+from synth.workload import Workload
+
+from .parity import check_round
+
+pytestmark = pytest.mark.gpu
+
+
+def _free():
+    gc.collect()
+    torch.cuda.empty_cache()
+
+
+def _run(wl, round_id=0):
+    if round_id:
+        wl.set_round(round_id)
+    out = wl.vr.run()
+    torch.cuda.synchronize()
+    return out
+
+
+def test_device_fill_matches_host_generator(gpu_lib):
+    from synth import tensors
+    for idx in (0, 2):
+        cfg = configs.scaled(configs.CONFIGS[idx], n_layers=1, S=300, V=777)
+        c = sd.alloc_cache(cfg, 0, cfg.NKV + 5, "cuda")
+        for w in ("k", "v"):
+            host = tensors.kv_full(cfg, w, 0)
+            dev = c[w][:, :, :cfg.NKV].cpu()
+            dev = dev.numpy() if cfg.kv_dtype == configs.I8 else dev.view(torch.int16).numpy().view(np.uint16)
+            assert np.array_equal(dev, host)
+            assert torch.count_nonzero(c[w][:, :, cfg.NKV:]).item() == 0
+            if cfg.kv_dtype == configs.I8:
+                hs = tensors.kv_scales_full(cfg, w, 0)
+                ds = c["ks" if w == "k" else "vs"][:, :, :cfg.NKV].cpu().view(torch.int16).numpy().view(np.uint16)
+                assert np.array_equal(ds, hs)
+        q = sd.alloc_q(cfg, 0, "cuda").cpu().view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(q, tensors.q_full(cfg, 0))
+        hd = sd.alloc_head(cfg, "cuda")
+        if cfg.w_dtype == configs.Q4:
+            p, s, b = tensors.w_full(cfg)
+            assert np.array_equal(hd["W"].cpu().numpy(), p)
+            assert np.array_equal(hd["scales"].cpu().view(torch.int16).numpy().view(np.uint16), s)
+            assert np.array_equal(hd["biases"].cpu().view(torch.int16).numpy().view(np.uint16), b)
+        else:
+            assert np.array_equal(hd["W"].cpu().view(torch.int16).numpy().view(np.uint16), tensors.w_full(cfg))
+
+
+def test_tiny_every_round(gpu_lib):
+    cfg = configs.CONFIGS[0]
+    wl = Workload(cfg)
+    wl.save_tail()
+    for rid in range(6):
+        wl.restore_tail()
+        out = _run(wl, rid)
+        rep = check_round(wl, out, layers=[0], attn_rows="all")
+        assert rep["ok"], rep
+
+
+def test_tiny_splits_and_ragged_capacity(gpu_lib):
+    cfg = configs.CONFIGS[0]
+    for splits in (1, 2, 3):
+        wl = Workload(cfg, s_cap=cfg.NKV + 61, splits=splits)
+        out = _run(wl)
+        rep = check_round(wl, out, layers=[0], attn_rows="all")
+        assert rep["ok"], rep
+
+
+def test_chain3_bf16_every_accept_length(gpu_lib):
+    """Linear chain T=3: mask == causal, walk == chain walk, gather == trim_to (identity), all accept lengths."""
+    cfg = configs.CONFIGS[1]
+    wl = Workload(cfg)
+    wl.save_tail()
+    seen = set()
+    for rid in range(3):
+        wl.restore_tail()
+        out = _run(wl, rid)
+        rep = check_round(wl, out, layers=[0, 7, 15], attn_rows="all", kv_heads=[0, 3],
+                          lm="full" if rid == 0 else "planted")
+        assert rep["ok"], rep
+        seen.add(len(wl.round["paths"][0]) - 1)
+    assert seen == {0, 1, 2}
+    del wl
+    _free()
+
+
+def test_specinfer16_int8_q4(gpu_lib):
+    cfg = configs.CONFIGS[2]
+    wl = Workload(cfg)
+    wl.save_tail()
+    accepts = set()
+    for rid in range(4):
+        wl.restore_tail()
+        out = _run(wl, rid)
+        rep = check_round(wl, out, layers=[0, 15], attn_rows=4, kv_heads=[1, 2],
+                          lm="full" if rid == 0 else "planted", rng_seed=rid)
+        assert rep["ok"], rep
+        accepts.add(len(wl.round["paths"][0]) - 1)
+    assert len(accepts) >= 2
+    del wl
+    _free()
+
+
+def test_eagle32x8_f16(gpu_lib):
+    cfg = configs.CONFIGS[3]
+    wl = Workload(cfg)
+    out = _run(wl)
+    paths = wl.round["paths"]
+    assert sum(1 for p in paths if p != list(range(len(p)))) >= 4  # scattered gathers exercised
+    rep = check_round(wl, out, layers=[0, 15], attn_rows=3, kv_heads=[0], seqs=[0, 5], lm="planted")
+    assert rep["ok"], rep
+    del wl, out
+    _free()
+
+
+def test_eagle64x32_int8_q4_long_context(gpu_lib):
+    cfg = configs.CONFIGS[4]
+    free, total = torch.cuda.mem_get_info()
+    need = cfg.kv_bytes() + cfg.kv_scale_bytes() + cfg.lm_bytes() + (4 << 30)
+    if free < need:
+        pytest.skip(f"needs {need / 2**30:.0f} GiB free, have {free / 2**30:.0f}")
+    wl = Workload(cfg)
+    out = _run(wl)
+    paths = wl.round["paths"]
+    assert paths[0] == [0] and paths[1] == list(range(len(paths[1])))  # zero accept and identity gather
+    rep = check_round(wl, out, layers=[3], attn_rows=2, kv_heads=[2], seqs=[0, 1, 31], lm="planted")
+    assert rep["ok"], rep
+    del wl, out
+    _free()

@@ -1,0 +1,225 @@
+"""Torch-facing wrappers of the tsv C ABI (argument marshalling only).
+
+Every function checks shapes/dtypes/devices of its torch tensors, passes raw
+device pointers and the current CUDA stream to the library, and raises
+``TsvError`` on any status other than TSV_OK.  All computation happens in the
+library's CUDA kernels.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass, field
+
+import torch
+
+from . import _abi
+from ._abi import BF16, F16, I8_SCALED, MAX_LAYERS, Q4_G64, AttnDesc, KvDesc, check, load
+
+KV_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, I8_SCALED: torch.int8}
+
+
+def _p(t):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(stream):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return C.c_void_p(s.cuda_stream)
+
+
+def _cuda(t, name, dtype=None, shape=None):
+    if t is None:
+        return
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+
+
+# ----------------------------------------------------------------------------- a1 tree mask
+def tree_mask(parents, anc, depth, dense_mask=None, mask_offset=0, dev_status=None, stream=None):
+    """parents int32 [B,T] -> anc int64 [B,T] (uint64 bits), depth int32 [B,T], optional dense mask."""
+    lib = load()
+    B, T = parents.shape
+    _cuda(parents, "parents", torch.int32)
+    _cuda(anc, "anc", torch.int64, (B, T))
+    _cuda(depth, "depth", torch.int32, (B, T))
+    if dense_mask is not None:
+        _cuda(dense_mask, "dense_mask", torch.float32, (B, T, mask_offset + T))
+    check(lib.tsv_tree_mask(_p(parents), B, T, _p(anc), _p(depth), _p(dense_mask), int(mask_offset),
+                            _p(dev_status), _stream(stream)), "tree_mask")
+
+
+# ----------------------------------------------------------------------------- a2 attention
+def attn_desc(q, k, v, o, kv_len, anc, *, T, HQ, HKV, D, kv_dtype, max_kv_len, k_scale=None, v_scale=None,
+              splits=0) -> AttnDesc:
+    """Descriptor over per-layer lists: q/o bf16 [B,T,HQ,D]; k/v [B,HKV,s_cap,D]; scales fp16 [B,HKV,s_cap]."""
+    n = len(q)
+    if not (1 <= n <= MAX_LAYERS) or not (len(k) == len(v) == len(o) == n):
+        raise ValueError("per-layer lists must have the same length in [1, 64]")
+    B = q[0].shape[0]
+    s_cap = k[0].shape[2]
+    d = AttnDesc()
+    d.n_layers, d.B, d.T, d.HQ, d.HKV, d.D = n, B, T, HQ, HKV, D
+    d.s_cap, d.max_kv_len, d.kv_dtype, d.splits = s_cap, int(max_kv_len), kv_dtype, int(splits)
+    kvt = KV_TORCH_DTYPE[kv_dtype]
+    for l in range(n):
+        _cuda(q[l], "q", torch.bfloat16, (B, T, HQ, D))
+        _cuda(o[l], "o", torch.bfloat16, (B, T, HQ, D))
+        _cuda(k[l], "k", kvt, (B, HKV, s_cap, D))
+        _cuda(v[l], "v", kvt, (B, HKV, s_cap, D))
+        d.q[l], d.k[l], d.v[l], d.o[l] = q[l].data_ptr(), k[l].data_ptr(), v[l].data_ptr(), o[l].data_ptr()
+        if kv_dtype == I8_SCALED:
+            _cuda(k_scale[l], "k_scale", torch.float16, (B, HKV, s_cap))
+            _cuda(v_scale[l], "v_scale", torch.float16, (B, HKV, s_cap))
+            d.k_scale[l], d.v_scale[l] = k_scale[l].data_ptr(), v_scale[l].data_ptr()
+    _cuda(kv_len, "kv_len", torch.int32, (B,))
+    _cuda(anc, "anc", torch.int64, (B, T))
+    d.kv_len, d.anc = kv_len.data_ptr(), anc.data_ptr()
+    return d
+
+
+def attention_workspace_size(desc: AttnDesc) -> int:
+    return int(load().tsv_attention_workspace_size(C.byref(desc)))
+
+
+def tree_verify_attention(desc: AttnDesc, workspace=None, dev_status=None, stream=None):
+    lib = load()
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    check(lib.tsv_tree_verify_attention(C.byref(desc), _p(workspace), ws_bytes, _p(dev_status), _stream(stream)),
+          "tree_verify_attention")
+
+
+# ----------------------------------------------------------------------------- a3 LM head
+def lm_head_workspace_size(rows: int, V: int) -> int:
+    return int(load().tsv_lm_head_workspace_size(rows, V))
+
+
+def lm_head_argmax(hidden, W, argmax, *, w_dtype, V, scales=None, biases=None, maxlogit=None, workspace=None,
+                   stream=None):
+    """hidden bf16 [rows,H]; W fp16/bf16 [V,H] or uint8 [V,H/2] (+ bf16 scales/biases [V,H/64])."""
+    lib = load()
+    rows, H = hidden.shape
+    _cuda(hidden, "hidden", torch.bfloat16)
+    if w_dtype == Q4_G64:
+        _cuda(W, "W", torch.uint8, (V, H // 2))
+        _cuda(scales, "scales", torch.bfloat16, (V, H // 64))
+        _cuda(biases, "biases", torch.bfloat16, (V, H // 64))
+    else:
+        _cuda(W, "W", torch.bfloat16 if w_dtype == BF16 else torch.float16, (V, H))
+    _cuda(argmax, "argmax", torch.int32, (rows,))
+    if maxlogit is not None:
+        _cuda(maxlogit, "maxlogit", torch.float32, (rows,))
+    if workspace is None:
+        workspace = torch.empty(lm_head_workspace_size(rows, V), dtype=torch.uint8, device=hidden.device)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    check(lib.tsv_lm_head_argmax(_p(hidden), rows, H, V, w_dtype, _p(W), _p(scales), _p(biases), _p(argmax),
+                                 _p(maxlogit), _p(workspace), ws_bytes, _stream(stream)), "lm_head_argmax")
+
+
+# ----------------------------------------------------------------------------- a4 walk
+def tree_accept_walk(argmax, tokens, parents, path, path_len, emitted, dev_status=None, stream=None):
+    lib = load()
+    B, T = parents.shape
+    for t, n in ((argmax, "argmax"), (tokens, "tokens"), (parents, "parents"), (path, "path"), (emitted, "emitted")):
+        _cuda(t, n, torch.int32, (B, T))
+    _cuda(path_len, "path_len", torch.int32, (B,))
+    check(lib.tsv_tree_accept_walk(_p(argmax), _p(tokens), _p(parents), B, T, _p(path), _p(path_len), _p(emitted),
+                                   _p(dev_status), _stream(stream)), "tree_accept_walk")
+
+
+# ----------------------------------------------------------------------------- a5 gather
+def kv_desc(k, v, *, HKV, D, kv_dtype, k_scale=None, v_scale=None) -> KvDesc:
+    n = len(k)
+    B, _, s_cap, _ = k[0].shape
+    d = KvDesc()
+    d.n_layers, d.B, d.HKV, d.D, d.s_cap, d.kv_dtype = n, B, HKV, D, s_cap, kv_dtype
+    kvt = KV_TORCH_DTYPE[kv_dtype]
+    for l in range(n):
+        _cuda(k[l], "k", kvt, (B, HKV, s_cap, D))
+        _cuda(v[l], "v", kvt, (B, HKV, s_cap, D))
+        d.k[l], d.v[l] = k[l].data_ptr(), v[l].data_ptr()
+        if kv_dtype == I8_SCALED:
+            _cuda(k_scale[l], "k_scale", torch.float16, (B, HKV, s_cap))
+            _cuda(v_scale[l], "v_scale", torch.float16, (B, HKV, s_cap))
+            d.k_scale[l], d.v_scale[l] = k_scale[l].data_ptr(), v_scale[l].data_ptr()
+    return d
+
+
+def kv_gather_positions(desc: KvDesc, kv_len, path, path_len, T: int, dev_status=None, stream=None):
+    lib = load()
+    _cuda(kv_len, "kv_len", torch.int32, (desc.B,))
+    _cuda(path, "path", torch.int32, (desc.B, T))
+    _cuda(path_len, "path_len", torch.int32, (desc.B,))
+    check(lib.tsv_kv_gather_positions(C.byref(desc), _p(kv_len), _p(path), _p(path_len), T, _p(dev_status),
+                                      _stream(stream)), "kv_gather_positions")
+
+
+# ----------------------------------------------------------------------------- one verify round
+@dataclass
+class VerifyRound:
+    """Device buffers of one verify round and the five calls in order on one stream.
+
+    Caches (k, v[, k_scale, v_scale]) and the LM head are resident state; the
+    per-round inputs are parents, tokens, q (per layer), hidden and kv_len.
+    """
+    T: int
+    HQ: int
+    HKV: int
+    D: int
+    V: int
+    kv_dtype: int
+    w_dtype: int
+    max_kv_len: int
+    parents: torch.Tensor
+    tokens: torch.Tensor
+    q: list
+    k: list
+    v: list
+    hidden: torch.Tensor
+    W: torch.Tensor
+    kv_len: torch.Tensor
+    k_scale: list = None
+    v_scale: list = None
+    w_scales: torch.Tensor = None
+    w_biases: torch.Tensor = None
+    splits: int = 0
+    outs: dict = field(default_factory=dict)
+
+    def __post_init__(self):
+        dev = self.parents.device
+        B, T = self.parents.shape
+        z = lambda *s, dt=torch.int32: torch.zeros(*s, dtype=dt, device=dev)
+        n = len(self.q)
+        self.outs = dict(anc=z(B, T, dt=torch.int64), depth=z(B, T), argmax=z(B * T), maxlogit=z(B * T, dt=torch.float32),
+                         path=z(B, T), path_len=z(B), emitted=z(B, T), status=z(4),
+                         o=[torch.empty(B, T, self.HQ, self.D, dtype=torch.bfloat16, device=dev) for _ in range(n)])
+        self.adesc = attn_desc(self.q, self.k, self.v, self.outs["o"], self.kv_len, self.outs["anc"], T=T, HQ=self.HQ,
+                               HKV=self.HKV, D=self.D, kv_dtype=self.kv_dtype, max_kv_len=self.max_kv_len,
+                               k_scale=self.k_scale, v_scale=self.v_scale, splits=self.splits)
+        self.kdesc = kv_desc(self.k, self.v, HKV=self.HKV, D=self.D, kv_dtype=self.kv_dtype, k_scale=self.k_scale,
+                             v_scale=self.v_scale)
+        self.attn_ws = torch.empty(max(attention_workspace_size(self.adesc), 256), dtype=torch.uint8, device=dev)
+        self.lm_ws = torch.empty(max(lm_head_workspace_size(B * T, self.V), 256), dtype=torch.uint8, device=dev)
+
+    def run(self, stream=None, stages=("mask", "attn", "lm", "walk", "gather")):
+        o = self.outs
+        B, T = self.parents.shape
+        if "mask" in stages:
+            tree_mask(self.parents, o["anc"], o["depth"], dev_status=o["status"], stream=stream)
+        if "attn" in stages:
+            tree_verify_attention(self.adesc, self.attn_ws, dev_status=o["status"], stream=stream)
+        if "lm" in stages:
+            lm_head_argmax(self.hidden, self.W, o["argmax"], w_dtype=self.w_dtype, V=self.V, scales=self.w_scales,
+                           biases=self.w_biases, maxlogit=o["maxlogit"], workspace=self.lm_ws, stream=stream)
+        if "walk" in stages:
+            tree_accept_walk(o["argmax"].view(B, T), self.tokens, self.parents, o["path"], o["path_len"], o["emitted"],
+                             dev_status=o["status"], stream=stream)
+        if "gather" in stages:
+            kv_gather_positions(self.kdesc, self.kv_len, o["path"], o["path_len"], T, dev_status=o["status"],
+                                stream=stream)
+        return o

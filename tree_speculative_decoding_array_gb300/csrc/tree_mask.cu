@@ -1,0 +1,85 @@
+// tsv_tree_mask: topology check, per-node ancestor bitmask and depth.
+//
+// mlxcel issue #1204, "What this needs" item 1: a node attends to its
+// ancestors only, and the mask is rebuilt every round from the topology.
+// "Increment 1": nodes are in topological order, parents[i] < i.  The mask is
+// kept as one 64-bit word per node (bit j = node j is an ancestor or the node
+// itself) instead of a dense T x T tensor; the attention kernels test bits.
+// PR #1212's history-mask commit gives the dense [T, offset + T] additive form
+// (history columns attended in full) and its verify commit the -1e9 blocking
+// value; the dense form is written only on request, for parity checks.
+#include "common.cuh"
+
+namespace tsv {
+
+// One CTA of 64 threads per sequence; thread i owns node i.
+__global__ void __launch_bounds__(64) tree_mask_kernel(const int32_t* __restrict__ parents, int B, int T,
+                                                       uint64_t* __restrict__ anc, int32_t* __restrict__ depth,
+                                                       int32_t* status) {
+    __shared__ int par[TSV_MAX_T];
+    __shared__ int bad;
+    const int b = blockIdx.x;
+    const int i = threadIdx.x;
+    if (i == 0) bad = 0;
+    __syncthreads();
+    if (i < T) {
+        const int p = parents[(size_t)b * T + i];
+        par[i] = p;
+        const bool ok = (i == 0) ? (p == -1) : (p >= 0 && p < i);
+        if (!ok) {
+            atomicExch(&bad, 1);
+            dev_fail(status, i == 0 ? TSV_DEV_BAD_ROOT : TSV_DEV_BAD_PARENT, b, i);
+        }
+    }
+    __syncthreads();
+    if (i >= T) return;
+    uint64_t a = 0;
+    int d = -1;
+    if (!bad) {
+        // parents strictly decrease along the chase, so it ends within i steps
+        a = 1ull << i;
+        d = 0;
+        for (int u = par[i]; u >= 0; u = par[u]) {
+            a |= 1ull << u;
+            ++d;
+        }
+    }
+    anc[(size_t)b * T + i] = a;
+    depth[(size_t)b * T + i] = d;
+}
+
+// Dense additive mask [B, T, offset + T]: 0 for history columns and for
+// ancestor-or-self block columns, -1e9 elsewhere.
+__global__ void dense_mask_kernel(const uint64_t* __restrict__ anc, int B, int T, int offset,
+                                  float* __restrict__ mask) {
+    const int W = offset + T;
+    const size_t n = (size_t)B * T * W;
+    for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(e % W);
+        const size_t row = e / W;  // b * T + q
+        float v = 0.0f;
+        if (c >= offset) v = ((anc[row] >> (c - offset)) & 1ull) ? 0.0f : -1e9f;
+        mask[e] = v;
+    }
+}
+
+}  // namespace tsv
+
+extern "C" tsv_status tsv_tree_mask(const int32_t* parents, int32_t B, int32_t T, uint64_t* anc, int32_t* depth,
+                                    float* dense_mask, int32_t mask_offset, int32_t* dev_status,
+                                    cudaStream_t stream) {
+    using namespace tsv;
+    clear_error();
+    if (B < 0 || T < 0) return fail(TSV_EINVAL, "tree_mask: B=%d T=%d must be >= 0", B, T);
+    if (T > TSV_MAX_T) return fail(TSV_ECAPACITY, "tree_mask: T=%d exceeds the maximum of %d nodes", T, TSV_MAX_T);
+    if (B == 0 || T == 0) return TSV_OK;
+    if (!parents || !anc || !depth) return fail(TSV_EINVAL, "tree_mask: parents, anc and depth must be non-null");
+    if (dense_mask && mask_offset < 0) return fail(TSV_EINVAL, "tree_mask: mask_offset=%d < 0", mask_offset);
+    tree_mask_kernel<<<B, 64, 0, stream>>>(parents, B, T, anc, depth, dev_status);
+    tsv_status st = check_launch("tree_mask");
+    if (st != TSV_OK || !dense_mask) return st;
+    const size_t n = (size_t)B * T * (size_t)(mask_offset + T);
+    const int grid = (int)((n + 255) / 256 < (size_t)sm_count() * 8 ? (n + 255) / 256 : (size_t)sm_count() * 8);
+    dense_mask_kernel<<<grid, 256, 0, stream>>>(anc, B, T, mask_offset, dense_mask);
+    return check_launch("tree_mask(dense)");
+}
