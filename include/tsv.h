@@ -74,6 +74,7 @@ typedef enum {
 #define TSV_DEV_BAD_PARENT 2  /* parents[b][i] outside [0, i) for i >= 1 */
 #define TSV_DEV_BAD_PATH 3    /* path not strictly increasing from 0, or path_len outside [1, T] */
 #define TSV_DEV_BAD_KV_LEN 4  /* kv_len[b] < T, or kv_len[b] > capacity */
+#define TSV_DEV_TIMEOUT 5     /* a bounded wait inside a kernel expired (a library bug; outputs unspecified) */
 
 #define TSV_MAX_T 64
 #define TSV_MAX_LAYERS 64
@@ -125,7 +126,7 @@ typedef struct {
     int32_t max_kv_len; /* host-known upper bound of every kv_len[b] (<= s_cap); sizes the grid */
     int32_t kv_dtype;   /* TSV_F16, TSV_BF16 or TSV_I8_SCALED */
     int32_t splits;     /* key-range splits per (layer, sequence, kv head); 0 = automatic */
-    int32_t reserved;
+    int32_t path;       /* TSV_ATTN_AUTO, TSV_ATTN_SIMT or TSV_ATTN_TCGEN05 */
     const void* q[TSV_MAX_LAYERS];       /* per layer: bf16 [B, T, HQ, D] */
     const void* k[TSV_MAX_LAYERS];       /* per layer: [B, HKV, s_cap, D] in kv_dtype (int8 codes) */
     const void* v[TSV_MAX_LAYERS];       /* per layer: as k */
@@ -135,6 +136,15 @@ typedef struct {
     const int32_t* kv_len;               /* int32 [B]: S_b + T */
     const uint64_t* anc;                 /* uint64 [B, T] from tsv_tree_mask */
 } tsv_attn_desc;
+
+/* Kernel choice.  AUTO takes the tensor-core (tcgen05) kernel where it applies
+ * (D == 256 with an fp16 or bf16 cache) and the CUDA-core kernel elsewhere.
+ * On the tensor-core path Q is rounded to the cache's 16-bit type for the
+ * Q K^T product (exact for bf16; for fp16 caches |q| must lie in fp16 range)
+ * and the softmax weights P enter P V as 16-bit values. */
+#define TSV_ATTN_AUTO 0
+#define TSV_ATTN_SIMT 1
+#define TSV_ATTN_TCGEN05 2
 
 size_t tsv_attention_workspace_size(const tsv_attn_desc* d);
 

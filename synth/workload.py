@@ -22,7 +22,7 @@ class Workload:
     """All device tensors of ``cfg`` (optionally a subset of layers, extra capacity)."""
 
     def __init__(self, cfg: Config, device="cuda", round_id: int = 0, n_layers: int | None = None,
-                 s_cap: int | None = None, splits: int = 0):
+                 s_cap: int | None = None, splits: int = 0, attn_path: int = 0):
         from tree_speculative_decoding_array_gb300 import VerifyRound
 
         self.cfg = cfg
@@ -46,7 +46,7 @@ class Workload:
             W=self.head["W"], kv_len=self.kv_len,
             k_scale=[c["ks"] for c in self.caches] if i8 else None,
             v_scale=[c["vs"] for c in self.caches] if i8 else None,
-            w_scales=self.head["scales"], w_biases=self.head["biases"], splits=splits)
+            w_scales=self.head["scales"], w_biases=self.head["biases"], splits=splits, attn_path=attn_path)
         self._tail = None
 
     def set_round(self, round_id: int):

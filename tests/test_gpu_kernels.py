@@ -101,9 +101,9 @@ def make_attn_case(rng, *, B, T, HQ, HKV, D, S_list, kv_dtype, layers=1, cap_ext
     return s_cap, data, trees
 
 
-def run_attn_case(gpu_lib, rng, *, B, T, HQ, HKV, D, S_list, kv_dtype, splits, layers=1):
+def run_attn_case(gpu_lib, rng, *, B, T, HQ, HKV, D, S_list, kv_dtype, splits, layers=1, path=0, cap_extra=3):
     s_cap, data, trees = make_attn_case(rng, B=B, T=T, HQ=HQ, HKV=HKV, D=D, S_list=S_list, kv_dtype=kv_dtype,
-                                        layers=layers)
+                                        layers=layers, cap_extra=cap_extra)
     qs, ks_, vs_, kss, vss, os_ = [], [], [], [], [], []
     for (q, k, v, ksc, vsc) in data:
         qs.append(torch.from_numpy(q).to(torch.bfloat16).to(DEV))
@@ -122,7 +122,8 @@ def run_attn_case(gpu_lib, rng, *, B, T, HQ, HKV, D, S_list, kv_dtype, splits, l
     gpu_lib.tree_mask(par, anc, depth)
     kv_len = i32([S + T for S in S_list])
     desc = gpu_lib.attn_desc(qs, ks_, vs_, os_, kv_len, anc, T=T, HQ=HQ, HKV=HKV, D=D, kv_dtype=kv_dtype,
-                             max_kv_len=max(S_list) + T, k_scale=kss or None, v_scale=vss or None, splits=splits)
+                             max_kv_len=max(S_list) + T, k_scale=kss or None, v_scale=vss or None, splits=splits,
+                             path=path)
     ws = torch.empty(max(gpu_lib.attention_workspace_size(desc), 16), dtype=torch.uint8, device=DEV)
     st = status()
     gpu_lib.tree_verify_attention(desc, ws, dev_status=st)
@@ -161,6 +162,27 @@ def test_attention_small(gpu_lib, kv_dtype, T, S_list, splits):
     rng = np.random.default_rng(T * 31 + kv_dtype)
     run_attn_case(gpu_lib, rng, B=2, T=T, HQ=6, HKV=2, D=256 if T < 33 else 128, S_list=S_list, kv_dtype=kv_dtype,
                   splits=splits)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("kv_dtype", [0, 1, 2])
+@pytest.mark.parametrize("T,S_list,splits", [(1, [0, 63], 0), (3, [64, 4096], 0), (16, [65, 1000], 3),
+                                             (22, [127, 5], 1), (33, [500, 200], 0), (64, [64, 1337], 2)])
+def test_attention_both_kernels(gpu_lib, path, kv_dtype, T, S_list, splits):
+    """CUDA-core (path 1) and tcgen05 (path 2) kernels on the same inputs; 1 to 3 tiles of 128 rows, ragged tails."""
+    rng = np.random.default_rng(T * 7 + kv_dtype)
+    run_attn_case(gpu_lib, rng, B=2, T=T, HQ=24, HKV=4, D=256, S_list=S_list, kv_dtype=kv_dtype, splits=splits,
+                  path=path, cap_extra=70)
+
+
+def test_attention_tcgen05_refuses_what_it_cannot_do(gpu_lib):
+    B, T, HQ, HKV, D = 1, 2, 4, 2, 128
+    q = [torch.zeros(B, T, HQ, D, dtype=torch.bfloat16, device=DEV)]
+    k = [torch.zeros(B, HKV, 8, D, dtype=torch.float16, device=DEV)]
+    desc = gpu_lib.attn_desc(q, k, [k[0].clone()], [q[0].clone()], i32([4]), torch.ones(B, T, dtype=torch.int64,
+                             device=DEV), T=T, HQ=HQ, HKV=HKV, D=D, kv_dtype=0, max_kv_len=8, path=2)
+    with pytest.raises(gpu_lib.TsvError, match="TSV_EUNSUPPORTED"):
+        gpu_lib.tree_verify_attention(desc, torch.empty(1 << 20, dtype=torch.uint8, device=DEV))
 
 
 @pytest.mark.parametrize("D", [64, 128, 256])

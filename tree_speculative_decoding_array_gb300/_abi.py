@@ -13,7 +13,8 @@ LIB_PATH = os.path.join(_HERE, "libtsv.so")
 
 OK, EINVAL, ETOPOLOGY, EUNSUPPORTED, ECAPACITY, ECUDA = range(6)
 F16, BF16, I8_SCALED, Q4_G64 = range(4)
-DEV_OK, DEV_BAD_ROOT, DEV_BAD_PARENT, DEV_BAD_PATH, DEV_BAD_KV_LEN = range(5)
+DEV_OK, DEV_BAD_ROOT, DEV_BAD_PARENT, DEV_BAD_PATH, DEV_BAD_KV_LEN, DEV_TIMEOUT = range(6)
+ATTN_AUTO, ATTN_SIMT, ATTN_TCGEN05 = range(3)
 MAX_T = 64
 MAX_LAYERS = 64
 
@@ -27,7 +28,7 @@ _vp, _i32, _i64, _sz = C.c_void_p, C.c_int32, C.c_int64, C.c_size_t
 class AttnDesc(C.Structure):
     _fields_ = [
         ("n_layers", _i32), ("B", _i32), ("T", _i32), ("HQ", _i32), ("HKV", _i32), ("D", _i32),
-        ("s_cap", _i64), ("max_kv_len", _i32), ("kv_dtype", _i32), ("splits", _i32), ("reserved", _i32),
+        ("s_cap", _i64), ("max_kv_len", _i32), ("kv_dtype", _i32), ("splits", _i32), ("path", _i32),
         ("q", _vp * MAX_LAYERS), ("k", _vp * MAX_LAYERS), ("v", _vp * MAX_LAYERS),
         ("k_scale", _vp * MAX_LAYERS), ("v_scale", _vp * MAX_LAYERS), ("o", _vp * MAX_LAYERS),
         ("kv_len", _vp), ("anc", _vp),

@@ -56,7 +56,7 @@ def tree_mask(parents, anc, depth, dense_mask=None, mask_offset=0, dev_status=No
 
 # ----------------------------------------------------------------------------- a2 attention
 def attn_desc(q, k, v, o, kv_len, anc, *, T, HQ, HKV, D, kv_dtype, max_kv_len, k_scale=None, v_scale=None,
-              splits=0) -> AttnDesc:
+              splits=0, path=0) -> AttnDesc:
     """Descriptor over per-layer lists: q/o bf16 [B,T,HQ,D]; k/v [B,HKV,s_cap,D]; scales fp16 [B,HKV,s_cap]."""
     n = len(q)
     if not (1 <= n <= MAX_LAYERS) or not (len(k) == len(v) == len(o) == n):
@@ -65,7 +65,7 @@ def attn_desc(q, k, v, o, kv_len, anc, *, T, HQ, HKV, D, kv_dtype, max_kv_len, k
     s_cap = k[0].shape[2]
     d = AttnDesc()
     d.n_layers, d.B, d.T, d.HQ, d.HKV, d.D = n, B, T, HQ, HKV, D
-    d.s_cap, d.max_kv_len, d.kv_dtype, d.splits = s_cap, int(max_kv_len), kv_dtype, int(splits)
+    d.s_cap, d.max_kv_len, d.kv_dtype, d.splits, d.path = s_cap, int(max_kv_len), kv_dtype, int(splits), int(path)
     kvt = KV_TORCH_DTYPE[kv_dtype]
     for l in range(n):
         _cuda(q[l], "q", torch.bfloat16, (B, T, HQ, D))
@@ -188,6 +188,7 @@ class VerifyRound:
     w_scales: torch.Tensor = None
     w_biases: torch.Tensor = None
     splits: int = 0
+    attn_path: int = 0
     outs: dict = field(default_factory=dict)
 
     def __post_init__(self):
@@ -200,7 +201,7 @@ class VerifyRound:
                          o=[torch.empty(B, T, self.HQ, self.D, dtype=torch.bfloat16, device=dev) for _ in range(n)])
         self.adesc = attn_desc(self.q, self.k, self.v, self.outs["o"], self.kv_len, self.outs["anc"], T=T, HQ=self.HQ,
                                HKV=self.HKV, D=self.D, kv_dtype=self.kv_dtype, max_kv_len=self.max_kv_len,
-                               k_scale=self.k_scale, v_scale=self.v_scale, splits=self.splits)
+                               k_scale=self.k_scale, v_scale=self.v_scale, splits=self.splits, path=self.attn_path)
         self.kdesc = kv_desc(self.k, self.v, HKV=self.HKV, D=self.D, kv_dtype=self.kv_dtype, k_scale=self.k_scale,
                              v_scale=self.v_scale)
         self.attn_ws = torch.empty(max(attention_workspace_size(self.adesc), 256), dtype=torch.uint8, device=dev)

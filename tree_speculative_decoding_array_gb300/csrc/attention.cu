@@ -28,27 +28,48 @@ constexpr int kBK = 32;   // keys per tile
 constexpr int kAttThreads = 256;
 
 struct AttnGeom {
-    int units, rgs, splits, chunk, rows_unit;
+    int units, rgs, splits, chunk, rows_unit, path;
 };
+
+// Defined in attention_tc.cu.
+bool tc_supported(const tsv_attn_desc* d);
+int tc_mtiles(const tsv_attn_desc* d);
+tsv_status launch_tc(const tsv_attn_desc* d, int splits, int chunk, float* ws_o, float* ws_ml, int32_t* status,
+                     cudaStream_t stream);
 
 static AttnGeom attn_geom(const tsv_attn_desc* d) {
     AttnGeom g;
     g.rows_unit = (d->HQ / d->HKV) * d->T;
     g.units = d->n_layers * d->B * d->HKV;
     g.rgs = (g.rows_unit + kRB - 1) / kRB;
-    const long long base = (long long)g.units * g.rgs;
-    const long long target = 4LL * sm_count();
+    g.path = (d->path == TSV_ATTN_TCGEN05 || (d->path == TSV_ATTN_AUTO && tc_supported(d))) ? TSV_ATTN_TCGEN05
+                                                                                           : TSV_ATTN_SIMT;
+    const int key_tile = g.path == TSV_ATTN_TCGEN05 ? 64 : kBK;
     int s = d->splits;
     if (s <= 0) {
-        s = (int)((target + base - 1) / base);
-        const int cap = (d->max_kv_len + 127) / 128;
-        if (s > cap) s = cap;
-        if (s > 64) s = 64;
+        const int cap_s = (d->max_kv_len + 255) / 256 < 64 ? (d->max_kv_len + 255) / 256 : 64;
+        if (g.path == TSV_ATTN_TCGEN05) {
+            // one CTA per SM: pick the fewest splits whose last wave is at least 85% full
+            const long long base = (long long)g.units * tc_mtiles(d);
+            const long long slots = sm_count();
+            s = 1;
+            for (int c = 1; c <= (cap_s > 1 ? cap_s : 1); ++c) {
+                const long long items = base * c;
+                const long long waves = (items + slots - 1) / slots;
+                s = c;
+                if ((double)items / (double)(waves * slots) >= 0.85) break;
+            }
+        } else {
+            const long long base = (long long)g.units * g.rgs;
+            const long long target = 4LL * sm_count();
+            s = (int)((target + base - 1) / base);
+            if (s > cap_s) s = cap_s;
+        }
     }
     if (s < 1) s = 1;
     int chunk = (d->max_kv_len + s - 1) / s;
-    chunk = ((chunk + kBK - 1) / kBK) * kBK;
-    if (chunk < kBK) chunk = kBK;
+    chunk = ((chunk + key_tile - 1) / key_tile) * key_tile;
+    if (chunk < key_tile) chunk = key_tile;
     g.splits = s;
     g.chunk = chunk;
     return g;
@@ -341,6 +362,11 @@ static tsv_status check_desc(const tsv_attn_desc* d) {
         return fail(TSV_EINVAL, "tree_verify_attention: max_kv_len=%d must be in [T, s_cap=%lld]", d->max_kv_len,
                     (long long)d->s_cap);
     if (d->splits < 0) return fail(TSV_EINVAL, "tree_verify_attention: splits=%d < 0", d->splits);
+    if (d->path < TSV_ATTN_AUTO || d->path > TSV_ATTN_TCGEN05)
+        return fail(TSV_EINVAL, "tree_verify_attention: path=%d", d->path);
+    if (d->path == TSV_ATTN_TCGEN05 && !tc_supported(d))
+        return fail(TSV_EUNSUPPORTED, "tree_verify_attention: the tcgen05 kernel needs D == 256 and an fp16 or bf16 "
+                                      "cache of fewer than 2^31 rows");
     if (!d->kv_len || !d->anc) return fail(TSV_EINVAL, "tree_verify_attention: kv_len and anc must be non-null");
     const int G = d->HQ / d->HKV;
     if ((long long)d->n_layers * d->B * d->HKV > 65535 || ((long long)G * d->T + kRB - 1) / kRB > 65535)
@@ -377,6 +403,13 @@ extern "C" tsv_status tsv_tree_verify_attention(const tsv_attn_desc* d, void* wo
         return fail(TSV_ECAPACITY, "tree_verify_attention: workspace %zu < %zu bytes", ws_bytes, need);
     float* ws_o = (float*)workspace;
     float* ws_ml = need ? (float*)((char*)workspace + ((((size_t)g.units * g.splits * g.rows_unit) * d->D * 4 + 255) & ~(size_t)255)) : nullptr;
+    if (g.path == TSV_ATTN_TCGEN05) {
+        st = launch_tc(d, g.splits, g.chunk, ws_o, ws_ml, dev_status, stream);
+        if (st != TSV_OK || g.splits == 1) return st;
+        dim3 cg(g.rows_unit, g.units);
+        attn_combine_kernel<<<cg, 128, 0, stream>>>(*d, g.splits, ws_o, ws_ml);
+        return check_launch("tree_verify_attention(combine)");
+    }
     switch (d->D) {
         case 64: launch_simt<64>(d, g, ws_o, ws_ml, dev_status, stream); break;
         case 128: launch_simt<128>(d, g, ws_o, ws_ml, dev_status, stream); break;

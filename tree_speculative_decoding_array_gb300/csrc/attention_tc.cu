@@ -1,0 +1,557 @@
+// Tensor-core (tcgen05) path of tsv_tree_verify_attention for 16-bit caches
+// with head dimension 256.
+//
+// Same operation as the CUDA-core path (see attention.cu): per (layer,
+// sequence, kv head) unit, the G*T query rows (node i, head g of the GQA
+// group) attend the S cached positions in full and the block positions of
+// their ancestors, split over key ranges with fp32 partials (Splash issue
+// #728, "Earlier shader evidence": split-KV tree attention with fp32 partials
+// and statistics; mlxcel issue #1204, "What this needs" item 1).
+//
+// One CTA = one 128-row tile of one unit and one key range; 192 threads:
+//   warps 0-3  softmax warpgroup: thread r owns query row r = TMEM lane r.
+//              Loads Q into shared memory, reads S from TMEM, applies the
+//              scale and the ancestor bits, runs the online softmax (fp32,
+//              log2 domain, lazy rescale of O when the max grows by > 2^8),
+//              writes P as 16-bit into shared memory, finally reads O.
+//   warp 4     TMA producer: K and V tiles of 64 keys x 256, 128-byte
+//              swizzled, two stages.
+//   warp 5     allocates TMEM (512 columns) and issues the MMAs:
+//              S[2 x 64 cols] = Q K^T (M=128, N=64, K=256) and
+//              O[256 cols] += P V (M=128, N=256, K=64, V read MN-major).
+// Int8 caches (Int8 codes with fp16 per-token scales) add warps 6-9, a
+// converter group: TMA brings the raw int8 tiles into a two-stage staging
+// ring, the converter writes the codes as fp16 (exact) into the operand
+// tiles and the tile's scales into shared memory; the softmax warpgroup
+// multiplies S column c by k_scale[c] and folds v_scale[c] into P.
+// Every mbarrier wait is bounded in time: on expiry the CTA raises a shared
+// abort flag, records TSV_DEV_TIMEOUT, drains its own MMAs and copies and
+// frees TMEM before returning.
+#include <cuda.h>
+
+#include "common.cuh"
+#include "tc.cuh"
+
+namespace tsv {
+
+constexpr int kTcRows = 128;
+constexpr int kTcBK = 64;
+constexpr int kTcD = 256;
+constexpr int kTcThreads16 = 192;
+constexpr int kTcThreadsI8 = 320;
+constexpr int kTcSmem = 1024 + 214016 + 256;
+constexpr uint32_t kTileBytes = kTcBK * kTcD * 2;  // one K (or V) tile: 32 KiB
+
+struct TcParams {
+    CUtensorMap kmap[TSV_MAX_LAYERS];
+    CUtensorMap vmap[TSV_MAX_LAYERS];
+    const uint16_t* q[TSV_MAX_LAYERS];
+    void* o[TSV_MAX_LAYERS];
+    const uint16_t* ks[TSV_MAX_LAYERS];
+    const uint16_t* vs[TSV_MAX_LAYERS];
+    const int32_t* kv_len;
+    const uint64_t* anc;
+    float* ws_o;
+    float* ws_ml;
+    int32_t* status;
+    int64_t s_cap;
+    int B, T, HQ, HKV, G, R, mtiles, splits, chunk, max_kv_len, mma_bf16;
+};
+
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+    uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        __half2 h = __floats2half2_rn(bf16_lo(w[k]), bf16_hi(w[k]));
+        w[k] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+__device__ __forceinline__ uint32_t pack2(float a, float b, bool bf) {
+    if (bf) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(a, b);
+        return *reinterpret_cast<uint32_t*>(&h);
+    }
+    __half2 h = __floats2half2_rn(a, b);
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// Bounded wait that ignores the abort flag (used only while draining).
+__device__ __forceinline__ void drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(bar, parity))
+        if (tc::globaltimer() - t0 > 200000000ull) break;  // 200 ms
+}
+
+// Int8 -> fp16 for 16 codes (one 16-byte chunk): exact, via 1024 + (code + 128) - 1152.
+__device__ __forceinline__ void i8x16_to_f16x16(uint4 in, uint32_t (&out)[8]) {
+    const uint32_t w[4] = {in.x, in.y, in.z, in.w};
+    const __half2 bias = __floats2half2_rn(1152.f, 1152.f);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const uint32_t x = w[k] ^ 0x80808080u;
+        uint32_t lo = __byte_perm(x, 0x64646464u, 0x5140);
+        uint32_t hi = __byte_perm(x, 0x64646464u, 0x7362);
+        __half2 a = __hsub2(*reinterpret_cast<__half2*>(&lo), bias);
+        __half2 c = __hsub2(*reinterpret_cast<__half2*>(&hi), bias);
+        out[2 * k] = *reinterpret_cast<uint32_t*>(&a);
+        out[2 * k + 1] = *reinterpret_cast<uint32_t*>(&c);
+    }
+}
+
+// Raw int8 tile [64 keys x 256] (row-major) -> fp16 operand tile in the
+// 128-byte-swizzled layout (4 blocks of [64 keys x 64]); keys >= nk become 0.
+__device__ __forceinline__ void convert_i8_tile(const uint8_t* raw, uint8_t* dst, int nk, int ct) {
+#pragma unroll 2
+    for (int s = 0; s < 8; ++s) {
+        const int id = s * 128 + ct;
+        const int key = id >> 4, c = id & 15;
+        const uint4 v = key < nk ? *reinterpret_cast<const uint4*>(raw + key * 256 + c * 16) : make_uint4(0, 0, 0, 0);
+        uint32_t w[8];
+        i8x16_to_f16x16(v, w);
+        if (key >= nk) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = 0;
+        }
+        const int kb = c >> 2, cc0 = (c & 3) * 2;
+        uint8_t* row = dst + kb * 8192 + key * 128;
+        *reinterpret_cast<uint4*>(row + ((cc0 ^ (key & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(row + (((cc0 + 1) ^ (key & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
+template <bool I8>
+__global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 16-bit caches: K stages [2 x 32K] at 64K, V stages [2 x 32K] at 128K.
+    // Int8 caches: fp16 K tile at 64K, fp16 V tile at 96K, raw stages [2 x (K 16K | V 16K)] at 128K.
+    uint8_t* sQ = sm;
+    uint8_t* sK = sm + 65536;
+    uint8_t* sV = sm + (I8 ? 98304 : 131072);
+    uint8_t* sRaw = sm + 131072;
+    uint8_t* sP = sm + 196608;
+    float* sScale = reinterpret_cast<float*>(sm + 212992);  // Int8: [2 slots][64 k-scales | 64 v-scales]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 214016);
+    uint64_t* kv_full = bars + 0;   // 16-bit: K/V tile landed.  Int8: raw tile landed.
+    uint64_t* kv_empty = bars + 2;  // 16-bit: P V done with the stage.  Int8: converter done with the raw stage.
+    uint64_t* s_full = bars + 4;
+    uint64_t* s_free = bars + 6;
+    uint64_t* p_full = bars + 8;
+    uint64_t* p_free = bars + 9;
+    uint64_t* o_done = bars + 10;
+    uint64_t* q_full = bars + 11;
+    uint64_t* drain = bars + 12;
+    uint64_t* kc_full = bars + 13;   // Int8: fp16 K tile written
+    uint64_t* kc_empty = bars + 14;  // Int8: Q K^T done with the fp16 K tile
+    uint64_t* vc_full = bars + 15;   // Int8: fp16 V tile written
+    uint64_t* vc_empty = bars + 16;  // Int8: P V done with the fp16 V tile
+    uint64_t* sc_full = bars + 17;   // Int8: [2] scale slot written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 20);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int item = blockIdx.x;
+    const int mt = item % p.mtiles;
+    item /= p.mtiles;
+    const int split = item % p.splits;
+    const int unit = item / p.splits;
+    const int kvh = unit % p.HKV;
+    const int b = (unit / p.HKV) % p.B;
+    const int layer = unit / (p.HKV * p.B);
+    const int T = p.T;
+    const int kvl = p.kv_len[b];
+    if (kvl < T || kvl > p.max_kv_len || (int64_t)kvl > p.s_cap) {
+        if (split == 0 && mt == 0 && kvh == 0 && layer == 0 && threadIdx.x == 0)
+            dev_fail(p.status, TSV_DEV_BAD_KV_LEN, b, kvl);
+        return;
+    }
+    const int S = kvl - T;
+    const int k_begin = split * p.chunk;
+    const int k_end = min(kvl, k_begin + p.chunk);
+    const int ntiles = k_end > k_begin ? (k_end - k_begin + kTcBK - 1) / kTcBK : 0;
+    const int row0 = mt * kTcRows;
+
+    // A CTA of this launch already timed out: do not start (keeps a broken launch short).
+    if (p.status != nullptr && *reinterpret_cast<volatile int32_t*>(p.status) == TSV_DEV_TIMEOUT) return;
+
+    if (ntiles == 0) {  // an empty key range contributes nothing to the combine
+        if (threadIdx.x < kTcRows && row0 + (int)threadIdx.x < p.R) {
+            const size_t slot = ((size_t)unit * p.splits + split) * p.R + row0 + threadIdx.x;
+            p.ws_ml[2 * slot] = -INFINITY;
+            p.ws_ml[2 * slot + 1] = 0.f;
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&kv_full[s], 1);
+            tc::mbar_init(&kv_empty[s], I8 ? kTcRows : 1);
+            tc::mbar_init(&s_full[s], 1);
+            tc::mbar_init(&s_free[s], kTcRows);
+            tc::mbar_init(&sc_full[s], kTcRows);
+        }
+        tc::mbar_init(p_full, kTcRows);
+        tc::mbar_init(p_free, 1);
+        tc::mbar_init(o_done, 1);
+        tc::mbar_init(q_full, kTcRows);
+        tc::mbar_init(drain, 1);
+        tc::mbar_init(kc_full, kTcRows);
+        tc::mbar_init(kc_empty, 1);
+        tc::mbar_init(vc_full, kTcRows);
+        tc::mbar_init(vc_empty, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 5) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ TMA producer
+        if (lane == 0) {
+            const CUtensorMap* km = &p.kmap[layer];
+            const CUtensorMap* vm = &p.vmap[layer];
+            tc::tma_prefetch_desc(km);
+            tc::tma_prefetch_desc(vm);
+            const int rowbase = (int)(((int64_t)b * p.HKV + kvh) * p.s_cap + k_begin);
+            int issued = 0;
+            for (int j = 0; j < ntiles; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !tc::mbar_wait(&kv_empty[st], ((j >> 1) - 1) & 1, abort_flag)) break;
+                const int row = rowbase + j * kTcBK;
+                if (I8) {
+                    tc::mbar_expect_tx(&kv_full[st], 2 * kTcBK * kTcD);
+                    tc::tma_load_2d(sRaw + st * 32768, km, &kv_full[st], 0, row);
+                    tc::tma_load_2d(sRaw + st * 32768 + 16384, vm, &kv_full[st], 0, row);
+                } else {
+                    tc::mbar_expect_tx(&kv_full[st], 2 * kTileBytes);
+#pragma unroll
+                    for (int db = 0; db < 4; ++db) {
+                        tc::tma_load_2d(sK + st * kTileBytes + db * 8192, km, &kv_full[st], db * 64, row);
+                        tc::tma_load_2d(sV + st * kTileBytes + db * 8192, vm, &kv_full[st], db * 64, row);
+                    }
+                }
+                issued = j + 1;
+            }
+            if (*abort_flag) {  // let our own copies land before the CTA goes away
+                for (int j = max(0, issued - 2); j < issued; ++j) drain_wait(&kv_full[j & 1], (j >> 1) & 1);
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const bool bf = p.mma_bf16 != 0;
+            const uint32_t id_qk = tc::idesc_f16(bf, false, false, kTcRows, kTcBK);
+            const uint32_t id_pv = tc::idesc_f16(bf, false, true, kTcRows, kTcD);
+            const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), aP = tc::smem_u32(sP);
+            bool ok = tc::mbar_wait(q_full, 0, abort_flag);
+            for (int j = 0; ok && j <= ntiles; ++j) {
+                if (j < ntiles) {
+                    const int st = j & 1;
+                    ok = I8 ? tc::mbar_wait(kc_full, j & 1, abort_flag)
+                            : tc::mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag);
+                    if (ok && j >= 2) ok = tc::mbar_wait(&s_free[st], ((j >> 1) - 1) & 1, abort_flag);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const uint32_t kbase = aK + (I8 ? 0 : st * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kTcD / 16; ++kk) {
+                        const uint64_t da = tc::sdesc_sw128(aQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                        const uint64_t db = tc::sdesc_sw128(kbase + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+                        tc::mma_f16(tmem + st * kTcBK, da, db, id_qk, kk > 0);
+                    }
+                    tc::mma_commit(&s_full[st]);
+                    if (I8) tc::mma_commit(kc_empty);
+                }
+                if (j >= 1) {
+                    const int t = j - 1, st = t & 1;
+                    ok = tc::mbar_wait(p_full, t & 1, abort_flag);
+                    if (ok && I8) ok = tc::mbar_wait(vc_full, t & 1, abort_flag);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const uint32_t vbase = aV + (I8 ? 0 : st * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                        const uint64_t da = tc::sdesc_sw128(aP + kk * 32, 16, 1024);
+                        const uint64_t db = tc::sdesc_sw128(vbase + kk * 2048, 8192, 1024);
+                        tc::mma_f16(tmem + 256, da, db, id_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::mma_commit(p_free);
+                    tc::mma_commit(I8 ? vc_empty : &kv_empty[st]);
+                }
+            }
+            if (ok) {
+                tc::mma_commit(o_done);
+            } else {  // wait for every MMA this thread issued before TMEM is freed
+                tc::mma_commit(drain);
+                drain_wait(drain, 0);
+            }
+        }
+    } else if (I8 && warp >= 6) {
+        // ------------------------------------------------------------ Int8 converter group
+        const int ct = threadIdx.x - 192;
+        const size_t seq_row = ((size_t)b * p.HKV + kvh) * (size_t)p.s_cap;
+        const uint16_t* ksg = p.ks[layer] + seq_row;
+        const uint16_t* vsg = p.vs[layer] + seq_row;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j & 1;
+            if (!tc::mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag)) break;
+            const int key0 = k_begin + j * kTcBK;
+            const int nk = min(kTcBK, k_end - key0);
+            if (j >= 1 && !tc::mbar_wait(kc_empty, (j - 1) & 1, abort_flag)) break;
+            {  // this tile's scales: threads 0-63 the K scales, 64-127 the V scales
+                const int key = ct & 63;
+                const uint16_t* src = ct < 64 ? ksg : vsg;
+                sScale[st * 128 + ct] = key < nk ? f16_bits_to_f32(src[key0 + key]) : 0.f;
+                tc::mbar_arrive(&sc_full[st]);
+            }
+            convert_i8_tile(sRaw + st * 32768, sK, nk, ct);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(kc_full);
+            if (j >= 1 && !tc::mbar_wait(vc_empty, (j - 1) & 1, abort_flag)) break;
+            convert_i8_tile(sRaw + st * 32768 + 16384, sV, nk, ct);
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(&kv_empty[st]);
+            tc::mbar_arrive(vc_full);
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ softmax warpgroup
+        const int r = threadIdx.x;  // row within the tile == TMEM lane
+        const int gr = row0 + r;
+        const bool row_ok = gr < p.R;
+        const int node = row_ok ? gr / p.G : 0;
+        const int head = kvh * p.G + (row_ok ? gr % p.G : 0);
+        const uint64_t anc = row_ok ? p.anc[(size_t)b * T + node] : 0ull;
+        const bool bf = p.mma_bf16 != 0;
+        {
+            const uint4* src = reinterpret_cast<const uint4*>(p.q[layer] + ((size_t)(b * T + node) * p.HQ + head) * kTcD);
+#pragma unroll 4
+            for (int c = 0; c < kTcD / 8; ++c) {
+                uint4 v = row_ok ? src[c] : make_uint4(0, 0, 0, 0);
+                if (!bf) v = bf16x8_to_f16x8(v);
+                const int kb = c >> 3, ch = c & 7;
+                *reinterpret_cast<uint4*>(sQ + kb * 16384 + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
+            }
+            tc::fence_proxy_async_smem();
+            tc::mbar_arrive(q_full);
+        }
+        const float qk_scale = 1.4426950408889634f * 0.0625f;  // log2(e) / sqrt(256)
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            const int sb = j & 1;
+            if (!tc::mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+            tc::tc_fence_after();
+            uint32_t s0[32], s1[32];
+            tc::tmem_ld32(tmem + lane_base + sb * kTcBK, s0);
+            tc::tmem_ld32(tmem + lane_base + sb * kTcBK + 32, s1);
+            tc::tmem_wait_ld();
+            tc::tc_fence_before();
+            tc::mbar_arrive(&s_free[sb]);
+            const float* ksc = sScale + sb * 128;
+            if (I8 && !tc::mbar_wait(&sc_full[sb], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+
+            const int c0 = k_begin + j * kTcBK;
+            float x[64];
+            float mt_ = -INFINITY;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) {
+                const int key = c0 + c;
+                const uint32_t raw = c < 32 ? s0[c] : s1[c - 32];
+                bool v = row_ok && key < k_end;
+                if (key >= S) v = v && ((anc >> ((key - S) & 63)) & 1ull);
+                const float sc = I8 ? qk_scale * ksc[c] : qk_scale;
+                x[c] = v ? __uint_as_float(raw) * sc : -INFINITY;
+                mt_ = fmaxf(mt_, x[c]);
+            }
+            float alpha = 1.f;
+            bool resc = false;
+            if (mt_ > m_ref + 8.f) {  // also when m_ref is still -inf
+                alpha = exp2f(m_ref - mt_);
+                m_ref = mt_;
+                resc = true;
+            }
+            uint32_t pk[32];
+            float ps = 0.f;
+#pragma unroll
+            for (int c = 0; c < 64; c += 2) {
+                const float p0 = x[c] == -INFINITY ? 0.f : exp2f(x[c] - m_ref);
+                const float p1 = x[c + 1] == -INFINITY ? 0.f : exp2f(x[c + 1] - m_ref);
+                ps += p0 + p1;
+                if (I8) pk[c >> 1] = pack2(p0 * ksc[64 + c], p1 * ksc[65 + c], false);
+                else pk[c >> 1] = pack2(p0, p1, bf);
+            }
+            l = l * alpha + ps;
+
+            if (j >= 1) {
+                if (!tc::mbar_wait(p_free, (j - 1) & 1, abort_flag)) { ok = false; break; }
+                tc::tc_fence_after();
+                if (__any_sync(0xFFFFFFFFu, resc)) {  // O *= alpha for this warp's rows
+#pragma unroll 1
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(tmem + lane_base + 256 + ch * 32, o);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tc::tmem_st32(tmem + lane_base + 256 + ch * 32, o);
+                    }
+                    tc::tmem_wait_st();
+                }
+            }
+            if (!I8 && c0 + kTcBK > k_end) {  // last tile: zero V rows past the key range (their bytes are not ours)
+                const int st = j & 1;
+                if (!tc::mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+                const int nk = k_end - c0;
+                uint8_t* vb = sV + st * kTileBytes;
+                for (int e = r; e < (kTcBK - nk) * 32; e += kTcRows) {
+                    const int row = nk + e / 32, chunk = e % 32;
+                    *reinterpret_cast<uint4*>(vb + (chunk >> 3) * 8192 + row * 128 + (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
+                }
+            }
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch)
+                *reinterpret_cast<uint4*>(sP + r * 128 + ((ch ^ (r & 7)) << 4)) =
+                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            tc::mbar_arrive(p_full);
+        }
+        if (ok && tc::mbar_wait(o_done, 0, abort_flag)) {
+            tc::tc_fence_after();
+            const size_t slot = ((size_t)unit * p.splits + split) * p.R + gr;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < 8; ++ch) {
+                uint32_t o[32];
+                tc::tmem_ld32(tmem + lane_base + 256 + ch * 32, o);
+                tc::tmem_wait_ld();
+                if (!row_ok) continue;
+                if (p.splits == 1) {
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o[layer]) +
+                                                          ((size_t)(b * T + node) * p.HQ + head) * kTcD + ch * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack2(__uint_as_float(o[8 * k + 2 * e]) * inv, __uint_as_float(o[8 * k + 2 * e + 1]) * inv, true);
+                        dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * kTcD + ch * 32);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                             __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+                }
+            }
+            if (row_ok && p.splits > 1) {
+                p.ws_ml[2 * slot] = m_ref;
+                p.ws_ml[2 * slot + 1] = l;
+            }
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) dev_fail(p.status, TSV_DEV_TIMEOUT, b, blockIdx.x);
+    if (warp == 5) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(f);
+    }
+    return fn;
+}
+
+// 2-D map over all (sequence, kv head, position) rows of one cache buffer:
+// [B * HKV * s_cap rows, 256 columns].  16-bit caches: boxes of 64 columns x
+// 64 rows with the 128-byte swizzle the MMA operands use.  Int8 caches:
+// whole 256-byte rows, 64 rows per box, unswizzled (the converter re-lays
+// them out).
+static bool make_kv_map(CUtensorMap* m, const void* base, long long rows, bool i8) {
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)kTcD, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)kTcD * (i8 ? 1 : 2)};
+    cuuint32_t box[2] = {i8 ? (cuuint32_t)kTcD : 64u, (cuuint32_t)kTcBK};
+    cuuint32_t es[2] = {1, 1};
+    return enc(m, i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims,
+               strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+               i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool tc_supported(const tsv_attn_desc* d) {
+    return d->D == kTcD && (d->kv_dtype == TSV_F16 || d->kv_dtype == TSV_BF16 || d->kv_dtype == TSV_I8_SCALED) &&
+           (long long)d->B * d->HKV * d->s_cap < (1LL << 31) - kTcBK;
+}
+
+int tc_mtiles(const tsv_attn_desc* d) { return ((d->HQ / d->HKV) * d->T + kTcRows - 1) / kTcRows; }
+
+tsv_status launch_tc(const tsv_attn_desc* d, int splits, int chunk, float* ws_o, float* ws_ml, int32_t* status,
+                     cudaStream_t stream) {
+    static thread_local TcParams prm;
+    const bool i8 = d->kv_dtype == TSV_I8_SCALED;
+    const long long rows = (long long)d->B * d->HKV * d->s_cap;
+    for (int l = 0; l < d->n_layers; ++l) {
+        if (!make_kv_map(&prm.kmap[l], d->k[l], rows, i8) || !make_kv_map(&prm.vmap[l], d->v[l], rows, i8))
+            return fail(TSV_ECUDA, "tree_verify_attention: tensor map encoding failed for layer %d", l);
+        prm.q[l] = reinterpret_cast<const uint16_t*>(d->q[l]);
+        prm.o[l] = d->o[l];
+        prm.ks[l] = reinterpret_cast<const uint16_t*>(d->k_scale[l]);
+        prm.vs[l] = reinterpret_cast<const uint16_t*>(d->v_scale[l]);
+    }
+    prm.kv_len = d->kv_len;
+    prm.anc = d->anc;
+    prm.ws_o = ws_o;
+    prm.ws_ml = ws_ml;
+    prm.status = status;
+    prm.s_cap = d->s_cap;
+    prm.B = d->B;
+    prm.T = d->T;
+    prm.HQ = d->HQ;
+    prm.HKV = d->HKV;
+    prm.G = d->HQ / d->HKV;
+    prm.R = prm.G * d->T;
+    prm.mtiles = tc_mtiles(d);
+    prm.splits = splits;
+    prm.chunk = chunk;
+    prm.max_kv_len = d->max_kv_len;
+    prm.mma_bf16 = d->kv_dtype == TSV_BF16;
+    const long long items = (long long)d->n_layers * d->B * d->HKV * splits * prm.mtiles;
+    if (items > 0x7FFFFFFFLL) return fail(TSV_ECAPACITY, "tree_verify_attention: too many work items");
+    if (i8) {
+        cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+        attn_tc_kernel<true><<<(unsigned)items, kTcThreadsI8, kTcSmem, stream>>>(prm);
+    } else {
+        cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+        attn_tc_kernel<false><<<(unsigned)items, kTcThreads16, kTcSmem, stream>>>(prm);
+    }
+    return check_launch("tree_verify_attention(tcgen05)");
+}
+
+}  // namespace tsv
