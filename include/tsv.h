@@ -173,6 +173,30 @@ tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32_t H, int32
                               float* maxlogit, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * tsv_lm_head_argmax_noalloc - tsv_lm_head_argmax without a workspace argument.
+ *   The pages have no counterpart: this entry point exists only in this
+ *   library, for callers that cannot allocate device memory themselves -
+ *   for example a plugin whose host framework owns every device buffer
+ *   through its own pool, or a latency-critical caller that may not pay for
+ *   cudaMalloc's implicit synchronisation.  Its scratch is a fixed array of
+ *   TSV_NOALLOC_MAX_ROWS 64-bit entries (32 KiB) inside this library's device
+ *   image, held by every GPU that loads the library until the process exits.
+ *   Arguments, results and errors are those of tsv_lm_head_argmax, plus
+ *   TSV_ECAPACITY when rows > TSV_NOALLOC_MAX_ROWS.  The library allocates
+ *   nothing for it: the first call on each device looks up the array's
+ *   device address (with that device current), and every call clears the
+ *   entries it uses on `stream` before the projection.  All calls share the
+ *   one array, so calls whose work overlaps on the GPU (on different streams,
+ *   or from different host threads) race and give wrong results; serialise
+ *   them on one stream.
+ */
+#define TSV_NOALLOC_MAX_ROWS 4096
+
+tsv_status tsv_lm_head_argmax_noalloc(const void* hidden, int32_t rows, int32_t H, int32_t V, int32_t w_dtype,
+                                      const void* W, const void* scales, const void* biases, int32_t* argmax,
+                                      float* maxlogit, cudaStream_t stream);
+
+/*
  * tsv_tree_accept_walk - descend the tree along the target's argmaxes.
  *   [1204] "What this needs" item 2 and "Increment 1" (the accepted set is a
  *   path, never a subtree); [1212] first commit; [728] "What it does" (every

@@ -17,6 +17,7 @@ DEV_OK, DEV_BAD_ROOT, DEV_BAD_PARENT, DEV_BAD_PATH, DEV_BAD_KV_LEN, DEV_TIMEOUT 
 ATTN_AUTO, ATTN_SIMT, ATTN_TCGEN05 = range(3)
 MAX_T = 64
 MAX_LAYERS = 64
+NOALLOC_MAX_ROWS = 4096
 
 STATUS_NAMES = {OK: "TSV_OK", EINVAL: "TSV_EINVAL", ETOPOLOGY: "TSV_ETOPOLOGY", EUNSUPPORTED: "TSV_EUNSUPPORTED",
                 ECAPACITY: "TSV_ECAPACITY", ECUDA: "TSV_ECUDA"}
@@ -51,6 +52,7 @@ SIGNATURES = {
     "tsv_tree_verify_attention": (C.c_int, [C.POINTER(AttnDesc), _vp, _sz, _vp, _vp]),
     "tsv_lm_head_workspace_size": (_sz, [_i32, _i32]),
     "tsv_lm_head_argmax": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "tsv_lm_head_argmax_noalloc": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "tsv_tree_accept_walk": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "tsv_kv_gather_positions": (C.c_int, [C.POINTER(KvDesc), _vp, _vp, _vp, _i32, _vp, _vp]),
 }

@@ -293,3 +293,59 @@ extern "C" tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32
     lm_unpack_kernel<<<(rows + 127) / 128, 128, 0, stream>>>(best, rows, argmax, maxlogit);
     return check_launch("lm_head_argmax(unpack)");
 }
+
+// ---------------------------------------------------------------------------
+// tsv_lm_head_argmax_noalloc: the same projection + argmax for callers that
+// cannot hand the library a workspace.  Its scratch (one 64-bit running best
+// per hidden row) lives in a fixed array in this library's device image
+// instead of caller memory; every GPU that loads the library keeps the array
+// until the process exits.
+// ---------------------------------------------------------------------------
+#include <mutex>
+
+namespace tsv {
+
+static __device__ __align__(256) unsigned long long g_lm_noalloc_best[TSV_NOALLOC_MAX_ROWS];
+
+// Device address of the scratch array on the current device, looked up once
+// per device with that device current.  The array's name in host code is only
+// a host-side handle, never a device address, so it is never passed to a
+// kernel directly.
+static tsv_status noalloc_scratch(void** out) {
+    static std::mutex mu;
+    static void* addr[64] = {nullptr};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return fail(TSV_ECUDA, "lm_head_argmax_noalloc: cudaGetDevice: %s", cudaGetErrorName(e));
+    if (dev < 0 || dev >= 64) return fail(TSV_EUNSUPPORTED, "lm_head_argmax_noalloc: device ordinal %d", dev);
+    std::lock_guard<std::mutex> lock(mu);
+    if (addr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_lm_noalloc_best);
+        if (e != cudaSuccess || p == nullptr)
+            return fail(TSV_ECUDA, "lm_head_argmax_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorName(e));
+        addr[dev] = p;
+    }
+    *out = addr[dev];
+    return TSV_OK;
+}
+
+}  // namespace tsv
+
+extern "C" tsv_status tsv_lm_head_argmax_noalloc(const void* hidden, int32_t rows, int32_t H, int32_t V,
+                                                 int32_t w_dtype, const void* W, const void* scales,
+                                                 const void* biases, int32_t* argmax, float* maxlogit,
+                                                 cudaStream_t stream) {
+    using namespace tsv;
+    clear_error();
+    if (rows > TSV_NOALLOC_MAX_ROWS)
+        return fail(TSV_ECAPACITY, "lm_head_argmax_noalloc: rows=%d exceeds the fixed scratch of %d rows "
+                                   "(use tsv_lm_head_argmax with a workspace)", rows, TSV_NOALLOC_MAX_ROWS);
+    if (rows < 1) return fail(TSV_EINVAL, "lm_head_argmax_noalloc: rows=%d", rows);
+    void* scratch = nullptr;
+    tsv_status st = noalloc_scratch(&scratch);
+    if (st != TSV_OK) return st;
+    // The workspace call clears the rows' entries on the stream before use.
+    return tsv_lm_head_argmax(hidden, rows, H, V, w_dtype, W, scales, biases, argmax, maxlogit, scratch,
+                              sizeof(g_lm_noalloc_best), stream);
+}
