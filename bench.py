@@ -175,13 +175,15 @@ def run_ours(args, rank, world, local_rank):
     e2e = run_e2e(args, wl, stream) if rank == 0 else None
 
     # launches of our kernels per step
-    lm_groups = 0
-    left = cfg.rows
-    while left > 0:
-        g = 8 if left >= 8 else (4 if left >= 4 else left)
-        left -= g
-        lm_groups += 1
-    launches = 1 + (1 + (tsv.attention_workspace_size(vr.adesc) > 0)) + (lm_groups + 1) + 1 + 2
+    if cfg.rows > 8:  # tensor-core LM head: (fp16 copy of hidden) + kernel + unpack
+        lm_launches = 1 + (cfg.w_dtype != configs.BF16) + 1
+    else:  # CUDA-core GEMV: one launch per group of up to 8 rows + unpack
+        lm_groups, left = 0, cfg.rows
+        while left > 0:
+            left -= 8 if left >= 8 else (4 if left >= 4 else left)
+            lm_groups += 1
+        lm_launches = lm_groups + 1
+    launches = 1 + (1 + (tsv.attention_workspace_size(vr.adesc) > 0)) + lm_launches + 1 + 2
     return dict(cfg=cfg, ms=ms, per_kernel=per_kernel, clocks=clk.summary(), e2e=e2e, launches=launches,
                 round_id=round_id)
 

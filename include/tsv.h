@@ -165,8 +165,15 @@ tsv_status tsv_tree_verify_attention(const tsv_attn_desc* d, void* workspace, si
  *   argmax  int32 [rows], out: index of the largest logit, ties -> lowest index.
  *   maxlogit float [rows] or NULL, out: that logit (fp32 accumulation).
  *   H % 64 == 0 (H % 256 == 0 for TSV_F16/TSV_BF16), 1 <= V < 2^31, rows >= 1.
+ *   Up to 8 rows stream the head once through CUDA cores; more rows use the
+ *   tcgen05 kernel (fp16 or bf16 operands, fp32 accumulation; 4-bit weights
+ *   are dequantised to fp16 with one rounding, and hidden is rounded to fp16
+ *   for fp16 and 4-bit heads).
  */
-size_t tsv_lm_head_workspace_size(int32_t rows, int32_t V);
+/* Workspace bytes for tsv_lm_head_argmax: 8 per hidden row (running bests), plus, when the tensor-core
+ * kernel applies (rows > 8) to an fp16 or 4-bit head, an fp16 copy of hidden (rows * H * 2).  A smaller
+ * workspace (at least 8 bytes per row) is accepted and selects the CUDA-core kernel. */
+size_t tsv_lm_head_workspace_size(int32_t rows, int32_t H, int32_t V, int32_t w_dtype);
 
 tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32_t H, int32_t V, int32_t w_dtype,
                               const void* W, const void* scales, const void* biases, int32_t* argmax,

@@ -85,4 +85,5 @@ def test_host_validation_refuses_without_launching():
     st = lib.tsv_lm_head_argmax(C.c_void_p(16), 1, 256, 10, 1, C.c_void_p(16), None, None, C.c_void_p(16), None,
                                 C.c_void_p(16), 0, None)
     assert st == _abi.ECAPACITY  # workspace too small
-    assert lib.tsv_lm_head_workspace_size(3, 1000) >= 24
+    assert lib.tsv_lm_head_workspace_size(3, 256, 1000, 1) >= 24
+    assert lib.tsv_lm_head_workspace_size(16, 512, 1000, 3) >= 16 * 8 + 16 * 512 * 2  # fp16 copy of hidden

@@ -36,7 +36,7 @@ def test_noalloc_matches_workspace_entry_point(gpu_lib):
             sc = bi = None
         ref_arg = torch.full((rows,), -7, dtype=torch.int32, device="cuda")
         ref_max = torch.zeros(rows, dtype=torch.float32, device="cuda")
-        ws = torch.empty(lib.tsv_lm_head_workspace_size(rows, V), dtype=torch.uint8, device="cuda")
+        ws = torch.empty(lib.tsv_lm_head_workspace_size(rows, H, V, w_dtype), dtype=torch.uint8, device="cuda")
         st = lib.tsv_lm_head_argmax(_p(hidden), rows, H, V, w_dtype, _p(W), _p(sc), _p(bi), _p(ref_arg), _p(ref_max),
                                     _p(ws), ws.numel(), stream)
         assert st == 0, lib.tsv_last_error()

@@ -50,7 +50,7 @@ SIGNATURES = {
     "tsv_tree_mask": (C.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp]),
     "tsv_attention_workspace_size": (_sz, [C.POINTER(AttnDesc)]),
     "tsv_tree_verify_attention": (C.c_int, [C.POINTER(AttnDesc), _vp, _sz, _vp, _vp]),
-    "tsv_lm_head_workspace_size": (_sz, [_i32, _i32]),
+    "tsv_lm_head_workspace_size": (_sz, [_i32, _i32, _i32, _i32]),
     "tsv_lm_head_argmax": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "tsv_lm_head_argmax_noalloc": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "tsv_tree_accept_walk": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),

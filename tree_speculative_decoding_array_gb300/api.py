@@ -95,8 +95,8 @@ def tree_verify_attention(desc: AttnDesc, workspace=None, dev_status=None, strea
 
 
 # ----------------------------------------------------------------------------- a3 LM head
-def lm_head_workspace_size(rows: int, V: int) -> int:
-    return int(load().tsv_lm_head_workspace_size(rows, V))
+def lm_head_workspace_size(rows: int, H: int, V: int, w_dtype: int) -> int:
+    return int(load().tsv_lm_head_workspace_size(rows, H, V, w_dtype))
 
 
 def lm_head_argmax(hidden, W, argmax, *, w_dtype, V, scales=None, biases=None, maxlogit=None, workspace=None,
@@ -115,7 +115,7 @@ def lm_head_argmax(hidden, W, argmax, *, w_dtype, V, scales=None, biases=None, m
     if maxlogit is not None:
         _cuda(maxlogit, "maxlogit", torch.float32, (rows,))
     if workspace is None:
-        workspace = torch.empty(lm_head_workspace_size(rows, V), dtype=torch.uint8, device=hidden.device)
+        workspace = torch.empty(lm_head_workspace_size(rows, H, V, w_dtype), dtype=torch.uint8, device=hidden.device)
     ws_bytes = workspace.numel() * workspace.element_size()
     check(lib.tsv_lm_head_argmax(_p(hidden), rows, H, V, w_dtype, _p(W), _p(scales), _p(biases), _p(argmax),
                                  _p(maxlogit), _p(workspace), ws_bytes, _stream(stream)), "lm_head_argmax")
@@ -205,7 +205,8 @@ class VerifyRound:
         self.kdesc = kv_desc(self.k, self.v, HKV=self.HKV, D=self.D, kv_dtype=self.kv_dtype, k_scale=self.k_scale,
                              v_scale=self.v_scale)
         self.attn_ws = torch.empty(max(attention_workspace_size(self.adesc), 256), dtype=torch.uint8, device=dev)
-        self.lm_ws = torch.empty(max(lm_head_workspace_size(B * T, self.V), 256), dtype=torch.uint8, device=dev)
+        self.lm_ws = torch.empty(max(lm_head_workspace_size(B * T, self.hidden.shape[1], self.V, self.w_dtype), 256),
+                                 dtype=torch.uint8, device=dev)
 
     def run(self, stream=None, stages=("mask", "attn", "lm", "walk", "gather")):
         o = self.outs

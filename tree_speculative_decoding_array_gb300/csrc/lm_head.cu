@@ -249,10 +249,21 @@ static void launch_group(int grid, cudaStream_t st, const uint16_t* hidden, int 
 
 }  // namespace tsv
 
-extern "C" size_t tsv_lm_head_workspace_size(int32_t rows, int32_t V) {
-    (void)V;
-    if (rows < 0) return 0;
-    return ((size_t)rows * sizeof(unsigned long long) + 255) & ~(size_t)255;
+namespace tsv {
+// Defined in lm_head_tc.cu.
+size_t lm_tc_extra_bytes(int rows, int H, int w_dtype);
+bool lm_tc_applies(int rows, int H, int V, int w_dtype);
+tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype, const void* W, const void* scales,
+                        const void* biases, unsigned long long* best, void* extra, cudaStream_t stream);
+static size_t best_bytes(int rows) { return ((size_t)rows * sizeof(unsigned long long) + 255) & ~(size_t)255; }
+}  // namespace tsv
+
+extern "C" size_t tsv_lm_head_workspace_size(int32_t rows, int32_t H, int32_t V, int32_t w_dtype) {
+    using namespace tsv;
+    if (rows < 1 || H < 1 || V < 1) return 0;
+    size_t n = best_bytes(rows);
+    if (lm_tc_applies(rows, H, V, w_dtype)) n += lm_tc_extra_bytes(rows, H, w_dtype);
+    return n;
 }
 
 extern "C" tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32_t H, int32_t V, int32_t w_dtype,
@@ -270,14 +281,21 @@ extern "C" tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32
     } else if (H % 256) {
         return fail(TSV_EINVAL, "lm_head_argmax: H=%d not a multiple of 256", H);
     }
-    if ((size_t)H * 8 * 16 / 8 > 200 * 1024) return fail(TSV_ECAPACITY, "lm_head_argmax: H=%d too large", H);
+    if ((size_t)H * 17 > 200 * 1024) return fail(TSV_ECAPACITY, "lm_head_argmax: H=%d above the supported 12,000", H);
     if (((uintptr_t)hidden | (uintptr_t)W) & 15) return fail(TSV_EINVAL, "lm_head_argmax: hidden/W not 16-byte aligned");
-    if (ws_bytes < tsv_lm_head_workspace_size(rows, V))
-        return fail(TSV_ECAPACITY, "lm_head_argmax: workspace %zu < %zu bytes", ws_bytes,
-                    tsv_lm_head_workspace_size(rows, V));
+    if (ws_bytes < best_bytes(rows))
+        return fail(TSV_ECAPACITY, "lm_head_argmax: workspace %zu < %zu bytes", ws_bytes, best_bytes(rows));
     unsigned long long* best = (unsigned long long*)workspace;
     if (cudaMemsetAsync(best, 0, (size_t)rows * sizeof(unsigned long long), stream) != cudaSuccess)
         return check_launch("lm_head_argmax(memset)");
+    // More than one 8-row pass: the tensor-core kernel, when the workspace also holds what it needs.
+    if (lm_tc_applies(rows, H, V, w_dtype) && ws_bytes >= best_bytes(rows) + lm_tc_extra_bytes(rows, H, w_dtype)) {
+        tsv_status st = launch_lm_tc(hidden, rows, H, V, w_dtype, W, scales, biases, best,
+                                     (char*)workspace + best_bytes(rows), stream);
+        if (st != TSV_OK) return st;
+        lm_unpack_kernel<<<(rows + 127) / 128, 128, 0, stream>>>(best, rows, argmax, maxlogit);
+        return check_launch("lm_head_argmax(unpack)");
+    }
     const int grid = sm_count() * 4;
     const uint16_t* hb = (const uint16_t*)hidden;
     for (int r0 = 0; r0 < rows;) {
