@@ -105,6 +105,21 @@ class ClockSampler:
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons), "samples": len(sm)}
 
 
+# ----------------------------------------------------------------------------- multi-rank helpers
+def max_over_ranks(ms: float, device="cpu") -> float:
+    """Slowest rank's timed-region length (every rank runs its own replica; no data-path exchange)."""
+    import torch
+
+    t = torch.tensor([ms], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def aggregate_nodes_per_s(world: int, nodes_per_round: int, steps: int, ms: float) -> float:
+    """Whole-job throughput: every rank verified ``steps`` rounds of ``nodes_per_round`` nodes in ``ms``."""
+    return world * nodes_per_round * steps / (ms * 1e-3)
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -125,10 +140,8 @@ def run_ours(args, rank, world, local_rank):
     stream = torch.cuda.current_stream()
     names = ["mask", "attn", "lm", "walk", "gather"]
 
-    def reset():
-        vr.kv_len.fill_(cfg.NKV)
-        if moved:
-            wl.restore_tail()
+    def reset():  # one launch: pristine tails of every cache and kv_len = S + T
+        wl.restore_tail()
 
     def step(evs=None):
         reset()
@@ -160,9 +173,7 @@ def run_ours(args, rank, world, local_rank):
     per_kernel = {n: statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
                   for i, n in enumerate(names)}
     if world > 1:
-        t = torch.tensor([ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, dev)
 
     # correctness of the timed state: one more round, check it against the planted walk
     step()
@@ -202,9 +213,7 @@ def run_e2e(args, wl, stream):
     moved = any(p != list(range(len(p))) for p in wl.round["paths"])
 
     def e2e_step():
-        vr.kv_len.fill_(cfg.NKV)
-        if moved:
-            wl.restore_tail()
+        wl.restore_tail()
         vr.parents.copy_(h_par, non_blocking=True)
         vr.tokens.copy_(h_tok, non_blocking=True)
         vr.hidden.copy_(h_hid, non_blocking=True)
@@ -353,7 +362,7 @@ def main():
         return
     cfg = r["cfg"]
     ms_step = r["ms"] / args.steps
-    nodes_per_s = world * cfg.rows * args.steps / (r["ms"] * 1e-3)
+    nodes_per_s = aggregate_nodes_per_s(world, cfg.rows, args.steps, r["ms"])
     peak, peak_kind = peaks()
     round_gbs = cfg.algorithmic_bytes() / (ms_step * 1e-3) / 1e9
     # dominant kernel: the LM head when its bytes dominate, else attention

@@ -29,6 +29,8 @@ def lib():
         _lib.tsv_synth_fill.restype = C.c_int
         _lib.tsv_synth_fill.argtypes = [C.c_void_p, C.c_int, C.c_uint64, C.c_uint64] + [C.c_int64] * 7 + \
             [C.c_float] * 4 + [C.c_void_p]
+        _lib.tsv_synth_copy_table.restype = C.c_int
+        _lib.tsv_synth_copy_table.argtypes = [C.c_void_p, C.c_int, C.c_void_p]
     return _lib
 
 
@@ -86,3 +88,11 @@ def alloc_head(cfg: Config, device) -> dict:
     fill(w, NORMAL_BF16 if cfg.w_dtype == BF16 else NORMAL_F16, st.key(cfg, st.KIND_W), (1, 1, V, H), (0, 0, H),
          (float(st.W_SIGMA), 0.0, 0.0, 0.0))
     return dict(W=w, scales=None, biases=None)
+
+
+def copy_table(table: torch.Tensor):
+    """Run the copies listed in ``table`` (int64 [n, 3] on the device: src, dst, bytes) in one launch."""
+    err = lib().tsv_synth_copy_table(C.c_void_p(table.data_ptr()), table.shape[0],
+                                     C.c_void_p(torch.cuda.current_stream().cuda_stream))
+    if err != 0:
+        raise RuntimeError(f"tsv_synth_copy_table failed with CUDA error {err}")

@@ -58,13 +58,26 @@ class Workload:
         self.hidden.copy_(bits_to_bf16(r["hidden"], "cpu"))
 
     def save_tail(self):
-        """Keep a copy of the verify block [S, S+T) of every cache (the gather rewrites it)."""
+        """Keep a pristine copy of the verify block [S, S+T) of every cache and of kv_len (the gather rewrites both).
+
+        ``restore_tail`` then puts them back with one batched copy launch.
+        """
         S, T = self.cfg.S, self.cfg.T
-        self._tail = [{k: (t[:, :, S:S + T].clone()) for k, t in c.items()} for c in self.caches]
+        rows = []
+        self._saved = []
+        for c in self.caches:
+            for name, t in c.items():
+                tail = t[:, :, S:S + T]
+                saved = tail.contiguous().clone()
+                self._saved.append(saved)
+                per = T * (t.shape[3] if t.dim() == 4 else 1) * t.element_size()  # bytes of one (b, kvh) tail
+                for b in range(t.shape[0]):
+                    for h in range(t.shape[1]):
+                        rows.append((saved[b, h].data_ptr(), tail[b, h].data_ptr(), per))
+        self._kv_len0 = self.kv_len.clone()
+        rows.append((self._kv_len0.data_ptr(), self.kv_len.data_ptr(), self.kv_len.numel() * 4))
+        self._table = torch.tensor(rows, dtype=torch.int64, device=self.device)
+        self._tail = True
 
     def restore_tail(self):
-        S, T = self.cfg.S, self.cfg.T
-        for c, saved in zip(self.caches, self._tail):
-            for k, t in c.items():
-                t[:, :, S:S + T].copy_(saved[k])
-        self.kv_len.fill_(self.cfg.NKV)
+        sd.copy_table(self._table)

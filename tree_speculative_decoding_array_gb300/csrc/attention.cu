@@ -49,15 +49,20 @@ static AttnGeom attn_geom(const tsv_attn_desc* d) {
     if (s <= 0) {
         const int cap_s = (d->max_kv_len + 255) / 256 < 64 ? (d->max_kv_len + 255) / 256 : 64;
         if (g.path == TSV_ATTN_TCGEN05) {
-            // one CTA per SM: pick the fewest splits whose last wave is at least 85% full
+            // One CTA per SM.  Estimated time of s splits: waves(s) x (fixed CTA cost + tiles per split x tile
+            // cost), with the fixed cost (TMEM, Q tile, pipeline fill, partial write) worth about 8 tiles.
             const long long base = (long long)g.units * tc_mtiles(d);
             const long long slots = sm_count();
+            const long long tiles = (d->max_kv_len + 63) / 64;
+            double best = 1e300;
             s = 1;
             for (int c = 1; c <= (cap_s > 1 ? cap_s : 1); ++c) {
-                const long long items = base * c;
-                const long long waves = (items + slots - 1) / slots;
-                s = c;
-                if ((double)items / (double)(waves * slots) >= 0.85) break;
+                const long long waves = (base * c + slots - 1) / slots;
+                const double t = (double)waves * (8.0 + (double)((tiles + c - 1) / c)) + (c > 1 ? 2.0 : 0.0);
+                if (t < best * 0.98) {
+                    best = t;
+                    s = c;
+                }
             }
         } else {
             const long long base = (long long)g.units * g.rgs;

@@ -10,20 +10,24 @@
 //
 // One CTA = one 128-row tile of one unit and one key range; 192 threads:
 //   warps 0-3  softmax warpgroup: thread r owns query row r = TMEM lane r.
-//              Loads Q into shared memory, reads S from TMEM, applies the
+//              Stores Q into TMEM, reads S from TMEM, applies the
 //              scale and the ancestor bits, runs the online softmax (fp32,
 //              log2 domain, lazy rescale of O when the max grows by > 2^8),
 //              writes P as 16-bit into shared memory, finally reads O.
-//   warp 4     TMA producer: K and V tiles of 64 keys x 256, 128-byte
-//              swizzled, two stages.
-//   warp 5     allocates TMEM (512 columns) and issues the MMAs:
-//              S[2 x 64 cols] = Q K^T (M=128, N=64, K=256) and
-//              O[256 cols] += P V (M=128, N=256, K=64, V read MN-major).
+//   warp 4     TMA producers (lane 0: K, lane 16: V): tiles of 64 keys x
+//              256, 128-byte swizzled, each in its own 3-stage ring (a K
+//              stage frees after Q K^T, a V stage after P V).
+//   warp 5     allocates TMEM (512 columns: Q 128 as 16-bit pairs, S 2 x 64,
+//              O 256) and issues the MMAs from an event loop:
+//              S = Q K^T (M=128, N=64, K=256, A read from TMEM) and
+//              O += P V (M=128, N=256, K=64, V read MN-major).
 // Int8 caches (Int8 codes with fp16 per-token scales) add warps 6-9, a
-// converter group: TMA brings the raw int8 tiles into a two-stage staging
-// ring, the converter writes the codes as fp16 (exact) into the operand
+// converter group: TMA brings the raw int8 tiles into 3-stage staging
+// rings, the converter writes the codes as fp16 (exact) into the operand
 // tiles and the tile's scales into shared memory; the softmax warpgroup
 // multiplies S column c by k_scale[c] and folds v_scale[c] into P.
+// Warp-collective roles take every wait decision warp-uniformly (__all_sync),
+// so that tcgen05.ld / __syncwarp never see a partial warp.
 // Every mbarrier wait is bounded in time: on expiry the CTA raises a shared
 // abort flag, records TSV_DEV_TIMEOUT, drains its own MMAs and copies and
 // frees TMEM before returning.
@@ -121,35 +125,42 @@ __device__ __forceinline__ void convert_i8_tile(const uint8_t* raw, uint8_t* dst
     }
 }
 
+constexpr int kNS = 3;  // stages of the K ring and of the V ring
+
 template <bool I8>
 __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    // 16-bit caches: K stages [2 x 32K] at 64K, V stages [2 x 32K] at 128K.
-    // Int8 caches: fp16 K tile at 64K, fp16 V tile at 96K, raw stages [2 x (K 16K | V 16K)] at 128K.
-    uint8_t* sQ = sm;
-    uint8_t* sK = sm + 65536;
-    uint8_t* sV = sm + (I8 ? 98304 : 131072);
-    uint8_t* sRaw = sm + 131072;
+    // Q lives in TMEM.  16-bit caches: K stages [3 x 32K] at 0, V stages [3 x 32K] at 96K.
+    // Int8 caches: fp16 K tile at 0, fp16 V tile at 32K, raw K stages [3 x 16K] at 64K, raw V stages [3 x 16K]
+    // at 112K.  P [128 x 64] 16-bit at 192K.
+    uint8_t* sK = sm;
+    uint8_t* sV = sm + (I8 ? 32768 : 98304);
+    uint8_t* sRawK = sm + 65536;
+    uint8_t* sRawV = sm + 114688;
     uint8_t* sP = sm + 196608;
-    float* sScale = reinterpret_cast<float*>(sm + 212992);  // Int8: [2 slots][64 k-scales | 64 v-scales]
+    float* sScale = reinterpret_cast<float*>(sm + 212992);  // Int8: [2 slots][64 K scales x log2(e)/16 | 64 V scales]
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 214016);
-    uint64_t* kv_full = bars + 0;   // 16-bit: K/V tile landed.  Int8: raw tile landed.
-    uint64_t* kv_empty = bars + 2;  // 16-bit: P V done with the stage.  Int8: converter done with the raw stage.
-    uint64_t* s_full = bars + 4;
-    uint64_t* s_free = bars + 6;
-    uint64_t* p_full = bars + 8;
-    uint64_t* p_free = bars + 9;
-    uint64_t* o_done = bars + 10;
-    uint64_t* q_full = bars + 11;
-    uint64_t* drain = bars + 12;
-    uint64_t* kc_full = bars + 13;   // Int8: fp16 K tile written
-    uint64_t* kc_empty = bars + 14;  // Int8: Q K^T done with the fp16 K tile
-    uint64_t* vc_full = bars + 15;   // Int8: fp16 V tile written
-    uint64_t* vc_empty = bars + 16;  // Int8: P V done with the fp16 V tile
-    uint64_t* sc_full = bars + 17;   // Int8: [2] scale slot written
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 19);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 20);
+    uint64_t* kfull = bars + 0;      // [3] K tile (16-bit) / raw K tile (Int8) landed
+    uint64_t* kempty = bars + 3;     // [3] stage free again: after Q K^T (16-bit) / after conversion (Int8)
+    uint64_t* vfull = bars + 6;      // [3] V tile / raw V tile landed
+    uint64_t* vempty = bars + 9;     // [3] stage free again: after P V (16-bit) / after conversion (Int8)
+    uint64_t* s_full = bars + 12;    // [2]
+    uint64_t* s_free = bars + 14;    // [2]
+    uint64_t* p_full = bars + 16;
+    uint64_t* p_free = bars + 17;
+    uint64_t* o_done = bars + 18;
+    uint64_t* q_full = bars + 19;
+    uint64_t* drain = bars + 20;
+    uint64_t* kc_full = bars + 21;   // Int8: fp16 K tile written
+    uint64_t* kc_empty = bars + 22;  // Int8: Q K^T done with the fp16 K tile
+    uint64_t* vc_full = bars + 23;   // Int8: fp16 V tile written
+    uint64_t* vc_empty = bars + 24;  // Int8: P V done with the fp16 V tile
+    uint64_t* sc_full = bars + 25;   // Int8: [2] scale slot written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 27);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 28);
+    // TMEM columns: Q [0, 128) as 16-bit pairs, S [128, 192) and [192, 256), O [256, 512).
+    constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int item = blockIdx.x;
@@ -186,21 +197,25 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
     }
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < 2; ++s) {
-            tc::mbar_init(&kv_full[s], 1);
-            tc::mbar_init(&kv_empty[s], I8 ? kTcRows : 1);
-            tc::mbar_init(&s_full[s], 1);
-            tc::mbar_init(&s_free[s], kTcRows);
-            tc::mbar_init(&sc_full[s], kTcRows);
+        for (int s = 0; s < kNS; ++s) {
+            tc::mbar_init(&kfull[s], 1);
+            tc::mbar_init(&kempty[s], I8 ? 4 : 1);
+            tc::mbar_init(&vfull[s], 1);
+            tc::mbar_init(&vempty[s], I8 ? 4 : 1);
         }
-        tc::mbar_init(p_full, kTcRows);
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&s_full[s], 1);
+            tc::mbar_init(&s_free[s], 4);
+            tc::mbar_init(&sc_full[s], 4);
+        }
+        tc::mbar_init(p_full, 4);
         tc::mbar_init(p_free, 1);
         tc::mbar_init(o_done, 1);
-        tc::mbar_init(q_full, kTcRows);
+        tc::mbar_init(q_full, 4);
         tc::mbar_init(drain, 1);
-        tc::mbar_init(kc_full, kTcRows);
+        tc::mbar_init(kc_full, 4);
         tc::mbar_init(kc_empty, 1);
-        tc::mbar_init(vc_full, kTcRows);
+        tc::mbar_init(vc_full, 4);
         tc::mbar_init(vc_empty, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
@@ -214,77 +229,96 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
     const uint32_t tmem = *tmem_slot;
 
     if (warp == 4) {
-        // ------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const CUtensorMap* km = &p.kmap[layer];
-            const CUtensorMap* vm = &p.vmap[layer];
-            tc::tma_prefetch_desc(km);
-            tc::tma_prefetch_desc(vm);
+        // ------------------------------------------------------------ TMA producers: lane 0 K, lane 16 V
+        if (lane == 0 || lane == 16) {
+            const bool isK = lane == 0;
+            const CUtensorMap* m = isK ? &p.kmap[layer] : &p.vmap[layer];
+            uint64_t* fullb = isK ? kfull : vfull;
+            uint64_t* emptyb = isK ? kempty : vempty;
+            tc::tma_prefetch_desc(m);
             const int rowbase = (int)(((int64_t)b * p.HKV + kvh) * p.s_cap + k_begin);
             int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
-                const int st = j & 1;
-                if (j >= 2 && !tc::mbar_wait(&kv_empty[st], ((j >> 1) - 1) & 1, abort_flag)) break;
+                const int st = j % kNS;
+                if (j >= kNS && !tc::mbar_wait(&emptyb[st], ((j / kNS) - 1) & 1, abort_flag)) break;
                 const int row = rowbase + j * kTcBK;
                 if (I8) {
-                    tc::mbar_expect_tx(&kv_full[st], 2 * kTcBK * kTcD);
-                    tc::tma_load_2d(sRaw + st * 32768, km, &kv_full[st], 0, row);
-                    tc::tma_load_2d(sRaw + st * 32768 + 16384, vm, &kv_full[st], 0, row);
+                    tc::mbar_expect_tx(&fullb[st], kTcBK * kTcD);
+                    tc::tma_load_2d((isK ? sRawK : sRawV) + st * 16384, m, &fullb[st], 0, row);
                 } else {
-                    tc::mbar_expect_tx(&kv_full[st], 2 * kTileBytes);
+                    tc::mbar_expect_tx(&fullb[st], kTileBytes);
+                    uint8_t* dst = (isK ? sK : sV) + st * kTileBytes;
 #pragma unroll
-                    for (int db = 0; db < 4; ++db) {
-                        tc::tma_load_2d(sK + st * kTileBytes + db * 8192, km, &kv_full[st], db * 64, row);
-                        tc::tma_load_2d(sV + st * kTileBytes + db * 8192, vm, &kv_full[st], db * 64, row);
-                    }
+                    for (int db = 0; db < 4; ++db) tc::tma_load_2d(dst + db * 8192, m, &fullb[st], db * 64, row);
                 }
                 issued = j + 1;
             }
             if (*abort_flag) {  // let our own copies land before the CTA goes away
-                for (int j = max(0, issued - 2); j < issued; ++j) drain_wait(&kv_full[j & 1], (j >> 1) & 1);
+                for (int j = max(0, issued - kNS); j < issued; ++j) drain_wait(&fullb[j % kNS], (j / kNS) & 1);
             }
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
+        // Event loop: issue whichever of the next Q K^T and the next P V is ready, so that a P V never waits
+        // behind a K tile that is still in flight.  Q K^T reads Q from TMEM.
         if (lane == 0) {
             const bool bf = p.mma_bf16 != 0;
             const uint32_t id_qk = tc::idesc_f16(bf, false, false, kTcRows, kTcBK);
             const uint32_t id_pv = tc::idesc_f16(bf, false, true, kTcRows, kTcD);
-            const uint32_t aQ = tc::smem_u32(sQ), aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), aP = tc::smem_u32(sP);
+            const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), aP = tc::smem_u32(sP);
             bool ok = tc::mbar_wait(q_full, 0, abort_flag);
-            for (int j = 0; ok && j <= ntiles; ++j) {
-                if (j < ntiles) {
-                    const int st = j & 1;
-                    ok = I8 ? tc::mbar_wait(kc_full, j & 1, abort_flag)
-                            : tc::mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag);
-                    if (ok && j >= 2) ok = tc::mbar_wait(&s_free[st], ((j >> 1) - 1) & 1, abort_flag);
-                    if (!ok) break;
-                    tc::tc_fence_after();
-                    const uint32_t kbase = aK + (I8 ? 0 : st * kTileBytes);
+            if (ok) tc::tc_fence_after();
+            int sj = 0, pj = 0;
+            uint32_t idle = 0;
+            uint64_t t_idle = 0;
+            while (ok && pj < ntiles) {
+                bool prog = false;
+                if (sj < ntiles) {
+                    const int sb = sj & 1, st = sj % kNS;
+                    bool ready = I8 ? tc::mbar_test(kc_full, sj & 1) : tc::mbar_test(&kfull[st], (sj / kNS) & 1);
+                    if (ready && sj >= 2) ready = tc::mbar_test(&s_free[sb], ((sj >> 1) - 1) & 1);
+                    if (ready) {
+                        tc::tc_fence_after();
+                        const uint32_t kbase = aK + (I8 ? 0 : st * kTileBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kTcD / 16; ++kk) {
-                        const uint64_t da = tc::sdesc_sw128(aQ + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
-                        const uint64_t db = tc::sdesc_sw128(kbase + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                        tc::mma_f16(tmem + st * kTcBK, da, db, id_qk, kk > 0);
+                        for (int kk = 0; kk < kTcD / 16; ++kk) {
+                            const uint64_t db = tc::sdesc_sw128(kbase + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+                            tc::mma_f16_ts(tmem + kColS + sb * kTcBK, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
+                        }
+                        tc::mma_commit(&s_full[sb]);
+                        tc::mma_commit(I8 ? kc_empty : &kempty[st]);
+                        ++sj;
+                        prog = true;
                     }
-                    tc::mma_commit(&s_full[st]);
-                    if (I8) tc::mma_commit(kc_empty);
                 }
-                if (j >= 1) {
-                    const int t = j - 1, st = t & 1;
-                    ok = tc::mbar_wait(p_full, t & 1, abort_flag);
-                    if (ok && I8) ok = tc::mbar_wait(vc_full, t & 1, abort_flag);
-                    if (!ok) break;
-                    tc::tc_fence_after();
-                    const uint32_t vbase = aV + (I8 ? 0 : st * kTileBytes);
+                if (pj < sj) {
+                    const int st = pj % kNS;
+                    bool ready = tc::mbar_test(p_full, pj & 1);
+                    if (ready) ready = I8 ? tc::mbar_test(vc_full, pj & 1) : tc::mbar_test(&vfull[st], (pj / kNS) & 1);
+                    if (ready) {
+                        tc::tc_fence_after();
+                        const uint32_t vbase = aV + (I8 ? 0 : st * kTileBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                        const uint64_t da = tc::sdesc_sw128(aP + kk * 32, 16, 1024);
-                        const uint64_t db = tc::sdesc_sw128(vbase + kk * 2048, 8192, 1024);
-                        tc::mma_f16(tmem + 256, da, db, id_pv, (t > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                            const uint64_t da = tc::sdesc_sw128(aP + kk * 32, 16, 1024);
+                            const uint64_t db = tc::sdesc_sw128(vbase + kk * 2048, 8192, 1024);
+                            tc::mma_f16(tmem + kColO, da, db, id_pv, (pj > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc::mma_commit(p_free);
+                        tc::mma_commit(I8 ? vc_empty : &vempty[st]);
+                        ++pj;
+                        prog = true;
                     }
-                    tc::mma_commit(p_free);
-                    tc::mma_commit(I8 ? vc_empty : &kv_empty[st]);
+                }
+                if (prog) {
+                    idle = 0;
+                } else if ((++idle & 63) == 1) {  // bounded: give up after kWaitNs without progress
+                    const uint64_t now = tc::globaltimer();
+                    if (idle == 1) t_idle = now;
+                    if (*abort_flag || now - t_idle > tc::kWaitNs) {
+                        *abort_flag = 1;
+                        ok = false;
+                    }
                 }
             }
             if (ok) {
@@ -301,25 +335,36 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
         const uint16_t* ksg = p.ks[layer] + seq_row;
         const uint16_t* vsg = p.vs[layer] + seq_row;
         for (int j = 0; j < ntiles; ++j) {
-            const int st = j & 1;
-            if (!tc::mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag)) break;
+            const int st = j % kNS, slot = j & 1;
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kfull[st], (j / kNS) & 1, abort_flag))) break;
             const int key0 = k_begin + j * kTcBK;
             const int nk = min(kTcBK, k_end - key0);
-            if (j >= 1 && !tc::mbar_wait(kc_empty, (j - 1) & 1, abort_flag)) break;
+            if (j >= 1 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(kc_empty, (j - 1) & 1, abort_flag))) break;
             {  // this tile's scales: threads 0-63 the K scales, 64-127 the V scales
                 const int key = ct & 63;
                 const uint16_t* src = ct < 64 ? ksg : vsg;
-                sScale[st * 128 + ct] = key < nk ? f16_bits_to_f32(src[key0 + key]) : 0.f;
-                tc::mbar_arrive(&sc_full[st]);
+                float v = key < nk ? f16_bits_to_f32(src[key0 + key]) : 0.f;
+                if (ct < 64) v *= 1.4426950408889634f * 0.0625f;  // K scales carry log2(e) / sqrt(256)
+                sScale[slot * 128 + ct] = v;
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&sc_full[slot]);
             }
-            convert_i8_tile(sRaw + st * 32768, sK, nk, ct);
+            convert_i8_tile(sRawK + st * 16384, sK, nk, ct);
             tc::fence_proxy_async_smem();
-            tc::mbar_arrive(kc_full);
-            if (j >= 1 && !tc::mbar_wait(vc_empty, (j - 1) & 1, abort_flag)) break;
-            convert_i8_tile(sRaw + st * 32768 + 16384, sV, nk, ct);
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&kempty[st]);
+                tc::mbar_arrive(kc_full);
+            }
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / kNS) & 1, abort_flag))) break;
+            if (j >= 1 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(vc_empty, (j - 1) & 1, abort_flag))) break;
+            convert_i8_tile(sRawV + st * 16384, sV, nk, ct);
             tc::fence_proxy_async_smem();
-            tc::mbar_arrive(&kv_empty[st]);
-            tc::mbar_arrive(vc_full);
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&vempty[st]);
+                tc::mbar_arrive(vc_full);
+            }
         }
     } else if (warp < 4) {
         // ------------------------------------------------------------ softmax warpgroup
@@ -330,86 +375,123 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
         const int head = kvh * p.G + (row_ok ? gr % p.G : 0);
         const uint64_t anc = row_ok ? p.anc[(size_t)b * T + node] : 0ull;
         const bool bf = p.mma_bf16 != 0;
-        {
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        {  // Q row -> TMEM lane r, 16-bit pairs (rounded to fp16 when the MMA runs in fp16)
             const uint4* src = reinterpret_cast<const uint4*>(p.q[layer] + ((size_t)(b * T + node) * p.HQ + head) * kTcD);
-#pragma unroll 4
-            for (int c = 0; c < kTcD / 8; ++c) {
-                uint4 v = row_ok ? src[c] : make_uint4(0, 0, 0, 0);
-                if (!bf) v = bf16x8_to_f16x8(v);
-                const int kb = c >> 3, ch = c & 7;
-                *reinterpret_cast<uint4*>(sQ + kb * 16384 + r * 128 + ((ch ^ (r & 7)) << 4)) = v;
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint4 v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = row_ok ? src[half * 16 + i] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        uint4 x = v[c2 * 8 + i];
+                        if (!bf) x = bf16x8_to_f16x8(x);
+                        w[4 * i] = x.x;
+                        w[4 * i + 1] = x.y;
+                        w[4 * i + 2] = x.z;
+                        w[4 * i + 3] = x.w;
+                    }
+                    tc::tmem_st32(tmem + lane_base + kColQ + (half * 2 + c2) * 32, w);
+                }
             }
-            tc::fence_proxy_async_smem();
-            tc::mbar_arrive(q_full);
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(q_full);
         }
         const float qk_scale = 1.4426950408889634f * 0.0625f;  // log2(e) / sqrt(256)
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
         for (int j = 0; j < ntiles; ++j) {
             const int sb = j & 1;
-            if (!tc::mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag))) { ok = false; break; }
             tc::tc_fence_after();
             uint32_t s0[32], s1[32];
-            tc::tmem_ld32(tmem + lane_base + sb * kTcBK, s0);
-            tc::tmem_ld32(tmem + lane_base + sb * kTcBK + 32, s1);
+            tc::tmem_ld32(tmem + lane_base + kColS + sb * kTcBK, s0);
+            tc::tmem_ld32(tmem + lane_base + kColS + sb * kTcBK + 32, s1);
             tc::tmem_wait_ld();
             tc::tc_fence_before();
-            tc::mbar_arrive(&s_free[sb]);
-            const float* ksc = sScale + sb * 128;
-            if (I8 && !tc::mbar_wait(&sc_full[sb], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&s_free[sb]);
+            const float* ksc = sScale + sb * 128;  // Int8: [64 K scales x log2(e)/16 | 64 V scales]
+            if (I8 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&sc_full[sb], (j >> 1) & 1, abort_flag))) { ok = false; break; }
 
             const int c0 = k_begin + j * kTcBK;
+            // Scores in the log2 domain.  Tiles whose 64 keys are all history keys inside the range need no mask.
             float x[64];
-            float mt_ = -INFINITY;
+            if (row_ok && c0 + kTcBK <= k_end && c0 + kTcBK <= S) {
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
-                const int key = c0 + c;
-                const uint32_t raw = c < 32 ? s0[c] : s1[c - 32];
-                bool v = row_ok && key < k_end;
-                if (key >= S) v = v && ((anc >> ((key - S) & 63)) & 1ull);
-                const float sc = I8 ? qk_scale * ksc[c] : qk_scale;
-                x[c] = v ? __uint_as_float(raw) * sc : -INFINITY;
-                mt_ = fmaxf(mt_, x[c]);
+                for (int c = 0; c < 64; ++c) {
+                    const float raw = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
+                    x[c] = raw * (I8 ? ksc[c] : qk_scale);
+                }
+            } else {
+#pragma unroll
+                for (int c = 0; c < 64; ++c) {
+                    const int key = c0 + c;
+                    bool v = row_ok && key < k_end;
+                    if (key >= S) v = v && ((anc >> ((key - S) & 63)) & 1ull);
+                    const float raw = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
+                    x[c] = v ? raw * (I8 ? ksc[c] : qk_scale) : -INFINITY;
+                }
             }
+            float mx[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c) mx[c] = fmaxf(x[c], x[c + 32]);
+#pragma unroll
+            for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+                for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
+            const float mt_ = mx[0];
             float alpha = 1.f;
             bool resc = false;
             if (mt_ > m_ref + 8.f) {  // also when m_ref is still -inf
-                alpha = exp2f(m_ref - mt_);
+                alpha = tc::ex2_approx(m_ref - mt_);
                 m_ref = mt_;
                 resc = true;
             }
+            // m_ref == -inf only while every score so far was masked (then every p below is 0)
+            const float msub = m_ref == -INFINITY ? 0.f : m_ref;
             uint32_t pk[32];
-            float ps = 0.f;
+            float sm2[32];
 #pragma unroll
             for (int c = 0; c < 64; c += 2) {
-                const float p0 = x[c] == -INFINITY ? 0.f : exp2f(x[c] - m_ref);
-                const float p1 = x[c + 1] == -INFINITY ? 0.f : exp2f(x[c + 1] - m_ref);
-                ps += p0 + p1;
+                const float p0 = tc::ex2_approx(x[c] - msub);
+                const float p1 = tc::ex2_approx(x[c + 1] - msub);
+                sm2[c >> 1] = p0 + p1;
                 if (I8) pk[c >> 1] = pack2(p0 * ksc[64 + c], p1 * ksc[65 + c], false);
                 else pk[c >> 1] = pack2(p0, p1, bf);
             }
+#pragma unroll
+            for (int w = 16; w >= 1; w >>= 1)
+#pragma unroll
+                for (int c = 0; c < w; ++c) sm2[c] += sm2[c + w];
+            const float ps = sm2[0];
             l = l * alpha + ps;
 
             if (j >= 1) {
-                if (!tc::mbar_wait(p_free, (j - 1) & 1, abort_flag)) { ok = false; break; }
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(p_free, (j - 1) & 1, abort_flag))) { ok = false; break; }
                 tc::tc_fence_after();
                 if (__any_sync(0xFFFFFFFFu, resc)) {  // O *= alpha for this warp's rows
 #pragma unroll 1
                     for (int ch = 0; ch < 8; ++ch) {
                         uint32_t o[32];
-                        tc::tmem_ld32(tmem + lane_base + 256 + ch * 32, o);
+                        tc::tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
                         tc::tmem_wait_ld();
 #pragma unroll
                         for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tc::tmem_st32(tmem + lane_base + 256 + ch * 32, o);
+                        tc::tmem_st32(tmem + lane_base + kColO + ch * 32, o);
                     }
                     tc::tmem_wait_st();
                 }
             }
             if (!I8 && c0 + kTcBK > k_end) {  // last tile: zero V rows past the key range (their bytes are not ours)
-                const int st = j & 1;
-                if (!tc::mbar_wait(&kv_full[st], (j >> 1) & 1, abort_flag)) { ok = false; break; }
+                const int st = j % kNS;
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / kNS) & 1, abort_flag))) { ok = false; break; }
                 const int nk = k_end - c0;
                 uint8_t* vb = sV + st * kTileBytes;
                 for (int e = r; e < (kTcBK - nk) * 32; e += kTcRows) {
@@ -423,16 +505,17 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                     make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
-            tc::mbar_arrive(p_full);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(p_full);
         }
-        if (ok && tc::mbar_wait(o_done, 0, abort_flag)) {
+        if (ok && __all_sync(0xFFFFFFFFu, tc::mbar_wait(o_done, 0, abort_flag))) {
             tc::tc_fence_after();
             const size_t slot = ((size_t)unit * p.splits + split) * p.R + gr;
             const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
             for (int ch = 0; ch < 8; ++ch) {
                 uint32_t o[32];
-                tc::tmem_ld32(tmem + lane_base + 256 + ch * 32, o);
+                tc::tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
                 tc::tmem_wait_ld();
                 if (!row_ok) continue;
                 if (p.splits == 1) {

@@ -13,11 +13,13 @@
 //         warp-shuffle max of the packed (logit, ~index) key, then a shared
 //         atomic max; the CTA's bests go to global memory once at the end.
 //   4     TMA producer (W block [128 x 64] swizzled, or the raw 4-bit block
-//         [128 x 32 bytes]; hidden block [NP x 64] swizzled), 4 / 3 stages.
+//         [128 x 32 bytes]; hidden block [NP x 64] swizzled) into a ring of
+//         as many stages (up to 16) as shared memory holds for this NP, so
+//         that narrow hidden chunks still keep ~100 KB per SM in flight.
 //   5     TMEM allocation and MMA issue.
 //   6-13  (4-bit heads) converter: w = scale * q + bias evaluated in fp16
 //         with one rounding (q exact via the 1024 + q trick), written into
-//         the swizzled A block.  The hidden rows arrive as fp16 too (a copy
+//         a separate 3-stage ring of swizzled A blocks.  The hidden rows arrive as fp16 too (a copy
 //         made by a small kernel into the workspace); fp16 keeps the
 //         dequantised weights within 2^-11 relative.
 // A CTA keeps one chunk of hidden rows and walks vocabulary tiles strided
@@ -41,19 +43,19 @@ struct LmTcParams {
     const uint16_t* scales;
     const uint16_t* biases;
     unsigned long long* best;
-    int rows, H, V, NP, nchunks, vtiles, mma_bf16, q4, stages;
+    int rows, H, V, NP, nchunks, vtiles, mma_bf16, stages, stage_bytes;
+    int sb_vec;  // scales/biases 16-byte aligned with H / 64 a multiple of 8: 8 groups per vector load
 };
+
+constexpr int kLmMaxStages = 16;
+constexpr int kLmConvStages = 3;
+constexpr int kLmSmem = 224 * 1024;     // dynamic shared memory requested
+constexpr int kLmUsable = kLmSmem - 1024 - 4096;  // minus alignment slack and the tail (bests + barriers)
 
 template <bool Q4>
 struct LmLayout {
-    static constexpr int kStages = Q4 ? 3 : 4;
-    static constexpr int kA = 16384;        // one A block [128 x 64] 16-bit
-    static constexpr int kB = 256 * 128;    // one B block [NP <= 256 x 64] 16-bit
-    static constexpr int kRaw = Q4 ? 4096 : 0;  // raw 4-bit block [128 x 32 bytes]
-    static constexpr int kStage = kA + kB + kRaw;
-    static constexpr int kBest = kStages * kStage;  // 256 x u64
-    static constexpr int kBars = kBest + 2048;
-    static constexpr int kSmem = 1024 + kBars + 256;
+    static constexpr int kW = Q4 ? 4096 : 16384;  // per stage: raw 4-bit block [128 x 32 B] or W block [128 x 64]
+    static constexpr int kConv = Q4 ? kLmConvStages * 16384 : 0;  // dequantised fp16 A blocks
     static constexpr int kThreads = Q4 ? kLmEpi + 64 + kLmConv : kLmEpi + 64;
 };
 
@@ -63,22 +65,27 @@ __device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
     return ((uint64_t)hi << 32) | lo;
 }
 
+// Shared memory: [conv ring (4-bit)] [TMA ring: stages x (W or raw block | hidden block)] ... [bests | barriers]
 template <bool Q4>
 __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const __grid_constant__ LmTcParams p) {
     using L = LmLayout<Q4>;
-    constexpr int S = L::kStages;
+    const int S = p.stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    unsigned long long* s_best = reinterpret_cast<unsigned long long*>(sm + L::kBest);
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + L::kBars);
-    uint64_t* full = bars;              // [S]
-    uint64_t* empty = bars + 4;         // [S]
-    uint64_t* conv_full = bars + 8;     // [S]
-    uint64_t* acc_full = bars + 12;     // [2]
-    uint64_t* acc_empty = bars + 14;    // [2]
-    uint64_t* drain = bars + 16;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 18);
+    uint8_t* conv = sm;                // [kLmConvStages][128 x 64] fp16 (4-bit heads)
+    uint8_t* ring = sm + L::kConv;     // [S][stage_bytes]
+    uint8_t* tail = sm + kLmUsable;
+    unsigned long long* s_best = reinterpret_cast<unsigned long long*>(tail);  // [256]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tail + 2048);
+    uint64_t* full = bars;                       // [16]
+    uint64_t* empty = bars + 16;                 // [16]
+    uint64_t* conv_full = bars + 32;             // [3]
+    uint64_t* conv_empty = bars + 35;            // [3]
+    uint64_t* acc_full = bars + 38;              // [2]
+    uint64_t* acc_empty = bars + 40;             // [2]
+    uint64_t* drain = bars + 42;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 43);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 44);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = blockIdx.x % p.nchunks;
@@ -86,19 +93,20 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
     const int groups = gridDim.x / p.nchunks;
     const int KB = p.H / kLmKB;
     const int nrows = min(p.NP, p.rows - chunk * p.NP);  // real hidden rows of this chunk
-    int n_items = 0;
-    for (int vt = group; vt < p.vtiles; vt += groups) ++n_items;
-    if (n_items == 0 || nrows <= 0) return;
+    if (group >= p.vtiles || nrows <= 0) return;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], 1);
-            tc::mbar_init(&conv_full[s], kLmConv);
+            tc::mbar_init(&empty[s], Q4 ? 1 + kLmConv / 32 : 1);
+        }
+        for (int s = 0; s < kLmConvStages; ++s) {
+            tc::mbar_init(&conv_full[s], kLmConv / 32);
+            tc::mbar_init(&conv_empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&acc_full[s], 1);
-            tc::mbar_init(&acc_empty[s], kLmEpi);
+            tc::mbar_init(&acc_empty[s], kLmEpi / 32);
         }
         tc::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -112,7 +120,6 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
     __syncthreads();
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const uint32_t a_bytes = Q4 ? L::kRaw : L::kA;
     const uint32_t b_bytes = (uint32_t)p.NP * 128;
 
     if (warp == 4) {
@@ -126,11 +133,11 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
                 for (int kb = 0; kb < KB; ++kb, ++g) {
                     const int st = g % S;
                     if (g >= S && !tc::mbar_wait(&empty[st], ((g / S) - 1) & 1, abort_flag)) { ok = false; break; }
-                    uint8_t* stage = sm + st * L::kStage;
-                    tc::mbar_expect_tx(&full[st], a_bytes + b_bytes);
-                    if (Q4) tc::tma_load_2d(stage + L::kA + L::kB, &p.wmap, &full[st], kb * 32, vt * kLmM);
+                    uint8_t* stage = ring + st * p.stage_bytes;
+                    tc::mbar_expect_tx(&full[st], L::kW + b_bytes);
+                    if (Q4) tc::tma_load_2d(stage, &p.wmap, &full[st], kb * 32, vt * kLmM);
                     else tc::tma_load_2d(stage, &p.wmap, &full[st], kb * kLmKB, vt * kLmM);
-                    tc::tma_load_2d(stage + L::kA, &p.hmap, &full[st], kb * kLmKB, chunk * p.NP);
+                    tc::tma_load_2d(stage + L::kW, &p.hmap, &full[st], kb * kLmKB, chunk * p.NP);
                     issued = g + 1;
                 }
             }
@@ -145,7 +152,7 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_f16(p.mma_bf16 != 0, false, false, kLmM, p.NP);
-            const uint32_t base = tc::smem_u32(sm);
+            const uint32_t rbase = tc::smem_u32(ring), cbase = tc::smem_u32(conv);
             int g = 0, it = 0;
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups, ++it) {
@@ -153,16 +160,18 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
                 if (it >= 2 && !tc::mbar_wait(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
                 for (int kb = 0; kb < KB; ++kb, ++g) {
-                    const int st = g % S;
+                    const int st = g % S, cs = g % kLmConvStages;
                     if (!tc::mbar_wait(&full[st], (g / S) & 1, abort_flag)) { ok = false; break; }
-                    if (Q4 && !tc::mbar_wait(&conv_full[st], (g / S) & 1, abort_flag)) { ok = false; break; }
+                    if (Q4 && !tc::mbar_wait(&conv_full[cs], (g / kLmConvStages) & 1, abort_flag)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t sa = base + st * L::kStage, sb = sa + L::kA;
+                    const uint32_t sa = Q4 ? cbase + cs * 16384 : rbase + st * p.stage_bytes;
+                    const uint32_t sb = rbase + st * p.stage_bytes + L::kW;
 #pragma unroll
                     for (int kk = 0; kk < kLmKB / 16; ++kk)
                         tc::mma_f16(tmem + buf * 256, tc::sdesc_sw128(sa + kk * 32, 16, 1024),
                                     tc::sdesc_sw128(sb + kk * 32, 16, 1024), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                     tc::mma_commit(&empty[st]);
+                    if (Q4) tc::mma_commit(&conv_empty[cs]);
                 }
                 if (ok) tc::mma_commit(&acc_full[buf]);
             }
@@ -177,18 +186,45 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
         const int row = ct >> 1, half = ct & 1;
         const int ng = p.H >> 6;
         const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+        // Scales and biases of this thread's row, 8 groups per 16-byte load, fetched one group of 8 ahead.
+        const bool vec = p.sb_vec != 0;
+        uint4 s_cur = make_uint4(0, 0, 0, 0), b_cur = s_cur, s_nxt = s_cur, b_nxt = s_cur;
+        auto fetch8 = [&](int vt_, int kb_) {
+            const int v_ = vt_ * kLmM + row;
+            if (vt_ < p.vtiles && v_ < p.V && kb_ < KB) {
+                s_nxt = *reinterpret_cast<const uint4*>(p.scales + (size_t)v_ * ng + kb_);
+                b_nxt = *reinterpret_cast<const uint4*>(p.biases + (size_t)v_ * ng + kb_);
+            }
+        };
+        if (vec) fetch8(group, 0);
         int g = 0;
         bool ok = true;
         for (int vt = group; ok && vt < p.vtiles; vt += groups) {
             const int v = vt * kLmM + row;
             const bool vok = v < p.V;
             for (int kb = 0; kb < KB; ++kb, ++g) {
-                const int st = g % S;
-                const float sc = vok ? bf16_bits_to_f32(p.scales[(size_t)v * ng + kb]) : 0.f;
-                const float bi = vok ? bf16_bits_to_f32(p.biases[(size_t)v * ng + kb]) : 0.f;
-                if (!tc::mbar_wait(&full[st], (g / S) & 1, abort_flag)) { ok = false; break; }
-                uint8_t* stage = sm + st * L::kStage;
-                const uint4 raw = *reinterpret_cast<const uint4*>(stage + L::kA + L::kB + row * 32 + half * 16);
+                const int st = g % S, cs = g % kLmConvStages;
+                float sc, bi;
+                if (vec) {
+                    if ((kb & 7) == 0) {
+                        s_cur = s_nxt;
+                        b_cur = b_nxt;
+                        if (kb + 8 < KB) fetch8(vt, kb + 8);
+                        else fetch8(vt + groups, 0);
+                    }
+                    const int e = kb & 7, wsel = e >> 1;
+                    const uint32_t sw = wsel == 0 ? s_cur.x : wsel == 1 ? s_cur.y : wsel == 2 ? s_cur.z : s_cur.w;
+                    const uint32_t bw = wsel == 0 ? b_cur.x : wsel == 1 ? b_cur.y : wsel == 2 ? b_cur.z : b_cur.w;
+                    sc = vok ? ((e & 1) ? bf16_hi(sw) : bf16_lo(sw)) : 0.f;
+                    bi = vok ? ((e & 1) ? bf16_hi(bw) : bf16_lo(bw)) : 0.f;
+                } else {
+                    sc = vok ? bf16_bits_to_f32(p.scales[(size_t)v * ng + kb]) : 0.f;
+                    bi = vok ? bf16_bits_to_f32(p.biases[(size_t)v * ng + kb]) : 0.f;
+                }
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&full[st], (g / S) & 1, abort_flag))) { ok = false; break; }
+                if (g >= kLmConvStages &&
+                    !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&conv_empty[cs], ((g / kLmConvStages) - 1) & 1, abort_flag))) { ok = false; break; }
+                const uint4 raw = *reinterpret_cast<const uint4*>(ring + st * p.stage_bytes + row * 32 + half * 16);
                 const __half2 s2 = __floats2half2_rn(sc, sc), b2 = __floats2half2_rn(bi, bi);
                 const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
                 uint32_t out[16];
@@ -202,7 +238,7 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
                         __half2 r = __hfma2(q, s2, b2);
                         out[4 * k + by] = *reinterpret_cast<uint32_t*>(&r);
                     }
-                uint8_t* arow = stage + row * 128;
+                uint8_t* arow = conv + cs * 16384 + row * 128;
 #pragma unroll
                 for (int q = 0; q < 4; ++q) {
                     const int chk = half * 4 + q;
@@ -210,7 +246,11 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
                         make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
                 }
                 tc::fence_proxy_async_smem();
-                tc::mbar_arrive(&conv_full[st]);
+                __syncwarp();
+                if (lane == 0) {
+                    tc::mbar_arrive(&empty[st]);
+                    tc::mbar_arrive(&conv_full[cs]);
+                }
             }
         }
     } else if (warp < 4) {
@@ -219,7 +259,7 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
         int it = 0;
         for (int vt = group; vt < p.vtiles; vt += groups, ++it) {
             const int buf = it & 1;
-            if (!tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag)) break;
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag))) break;
             tc::tc_fence_after();
             const int v = vt * kLmM + warp * 32 + lane;
             for (int c0 = 0; c0 < nrows; c0 += 32) {
@@ -240,7 +280,8 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
                 }
             }
             tc::tc_fence_before();
-            tc::mbar_arrive(&acc_empty[buf]);
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
         }
     }
 
@@ -330,6 +371,7 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
                      (uint32_t)NP, true);
     if (!ok) return fail(TSV_ECUDA, "lm_head_argmax: tensor map encoding failed");
     prm.scales = (const uint16_t*)scales;
+    prm.sb_vec = q4 && (H / 64) % 8 == 0 && (((uintptr_t)scales | (uintptr_t)biases) & 15) == 0;
     prm.biases = (const uint16_t*)biases;
     prm.best = best;
     prm.rows = rows;
@@ -339,16 +381,21 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
     prm.nchunks = nchunks;
     prm.vtiles = (V + kLmM - 1) / kLmM;
     prm.mma_bf16 = w_dtype == TSV_BF16;
-    prm.q4 = q4;
+    const int wbytes = q4 ? LmLayout<true>::kW : LmLayout<false>::kW;
+    const int conv_bytes = q4 ? LmLayout<true>::kConv : 0;
+    prm.stage_bytes = wbytes + NP * 128;  // multiples of 1024: every block stays 1024-aligned
+    int stages = (kLmUsable - conv_bytes) / prm.stage_bytes;
+    prm.stages = stages > kLmMaxStages ? kLmMaxStages : stages;
+    if (prm.stages < 2) return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the pipeline");
     const int sms = sm_count();
     const int groups = sms / nchunks > 0 ? sms / nchunks : 1;
     const int grid = groups * nchunks;
     if (q4) {
-        cudaFuncSetAttribute(lm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, LmLayout<true>::kSmem);
-        lm_tc_kernel<true><<<grid, LmLayout<true>::kThreads, LmLayout<true>::kSmem, stream>>>(prm);
+        cudaFuncSetAttribute(lm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+        lm_tc_kernel<true><<<grid, LmLayout<true>::kThreads, kLmSmem, stream>>>(prm);
     } else {
-        cudaFuncSetAttribute(lm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, LmLayout<false>::kSmem);
-        lm_tc_kernel<false><<<grid, LmLayout<false>::kThreads, LmLayout<false>::kSmem, stream>>>(prm);
+        cudaFuncSetAttribute(lm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+        lm_tc_kernel<false><<<grid, LmLayout<false>::kThreads, kLmSmem, stream>>>(prm);
     }
     return check_launch("lm_head_argmax(tcgen05)");
 }
