@@ -266,7 +266,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             const uint32_t id_qk = tc::idesc_f16(bf, false, false, kTcRows, kTcBK);
             const uint32_t id_pv = tc::idesc_f16(bf, false, true, kTcRows, kTcD);
             const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), aP = tc::smem_u32(sP);
-            bool ok = tc::mbar_wait(q_full, 0, abort_flag);
+            bool ok = tc::mbar_wait_spin(q_full, 0, abort_flag);
             if (ok) tc::tc_fence_after();
             int sj = 0, pj = 0;
             uint32_t idle = 0;
@@ -423,7 +423,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             const int c0 = k_begin + j * kTcBK;
             // Scores in the log2 domain.  Tiles whose 64 keys are all history keys inside the range need no mask.
             float x[64];
-            if (row_ok && c0 + kTcBK <= k_end && c0 + kTcBK <= S) {
+            // (padding rows past the unit's G*T rows take it too: their Q is zero and their results are dropped)
+            if (c0 + kTcBK <= k_end && c0 + kTcBK <= S) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const float raw = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);

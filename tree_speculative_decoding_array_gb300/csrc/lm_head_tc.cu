@@ -157,12 +157,12 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups, ++it) {
                 const int buf = it & 1;
-                if (it >= 2 && !tc::mbar_wait(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+                if (it >= 2 && !tc::mbar_wait_spin(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
                 for (int kb = 0; kb < KB; ++kb, ++g) {
                     const int st = g % S, cs = g % kLmConvStages;
-                    if (!tc::mbar_wait(&full[st], (g / S) & 1, abort_flag)) { ok = false; break; }
-                    if (Q4 && !tc::mbar_wait(&conv_full[cs], (g / kLmConvStages) & 1, abort_flag)) { ok = false; break; }
+                    if (!tc::mbar_wait_spin(&full[st], (g / S) & 1, abort_flag)) { ok = false; break; }
+                    if (Q4 && !tc::mbar_wait_spin(&conv_full[cs], (g / kLmConvStages) & 1, abort_flag)) { ok = false; break; }
                     tc::tc_fence_after();
                     const uint32_t sa = Q4 ? cbase + cs * 16384 : rbase + st * p.stage_bytes;
                     const uint32_t sb = rbase + st * p.stage_bytes + L::kW;
