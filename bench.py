@@ -132,6 +132,8 @@ def run_ours(args, rank, world, local_rank):
     dev = f"cuda:{local_rank}"
     torch.cuda.set_device(dev)
     cfg = configs.CONFIGS[args.config]
+    if args.layers:
+        cfg = configs.scaled(cfg, n_layers=args.layers)
     round_id = args.round if args.round is not None else ({1: 2}.get(args.config, 0))
     wl = Workload(cfg, device=dev, round_id=round_id, attn_path=args.attn_path)
     vr = wl.vr
@@ -320,6 +322,8 @@ def main():
     ap.add_argument("--round", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--attn-path", type=int, default=0, help="0 auto, 1 CUDA-core kernel, 2 tcgen05 kernel")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="attention layers (default: the workload's); fewer only for small profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -330,6 +334,8 @@ def main():
     from synth import configs
 
     cfg = configs.CONFIGS[args.config]
+    if args.layers:
+        cfg = configs.scaled(cfg, n_layers=args.layers)
     config = {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "layers": cfg.n_layers, "HQ": cfg.HQ, "HKV": cfg.HKV,
               "D": cfg.D, "S": cfg.S, "H": cfg.H, "V": cfg.V, "kv": configs.DTYPE_NAMES[cfg.kv_dtype],
               "lm_head": configs.DTYPE_NAMES[cfg.w_dtype], "topology": cfg.topology,

@@ -22,8 +22,8 @@
 //              S = Q K^T (M=128, N=64, K=256, A read from TMEM) and
 //              O += P V (M=128, N=256, K=64, V read MN-major).
 // Int8 caches (Int8 codes with fp16 per-token scales) add warps 6-9, a
-// converter group: TMA brings the raw int8 tiles into 3-stage staging
-// rings, the converter writes the codes as fp16 (exact) into the operand
+// converter group: TMA brings the raw int8 tiles into 2-stage staging
+// rings, the converter writes them as fp16 into 2-stage operand rings, the converter writes the codes as fp16 (exact) into the operand
 // tiles and the tile's scales into shared memory; the softmax warpgroup
 // multiplies S column c by k_scale[c] and folds v_scale[c] into P.
 // Warp-collective roles take every wait decision warp-uniformly (__all_sync),
@@ -43,7 +43,7 @@ constexpr int kTcBK = 64;
 constexpr int kTcD = 256;
 constexpr int kTcThreads16 = 192;
 constexpr int kTcThreadsI8 = 320;
-constexpr int kTcSmem = 1024 + 214016 + 256;
+constexpr int kTcSmem = 1024 + 215040 + 512;
 constexpr uint32_t kTileBytes = kTcBK * kTcD * 2;  // one K (or V) tile: 32 KiB
 
 struct TcParams {
@@ -132,15 +132,16 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // Q lives in TMEM.  16-bit caches: K stages [3 x 32K] at 0, V stages [3 x 32K] at 96K.
-    // Int8 caches: fp16 K tile at 0, fp16 V tile at 32K, raw K stages [3 x 16K] at 64K, raw V stages [3 x 16K]
-    // at 112K.  P [128 x 64] 16-bit at 192K.
+    // Int8 caches: fp16 K tiles [2 x 32K] at 0, fp16 V tiles [2 x 32K] at 64K, raw K stages [2 x 16K] at 128K,
+    // raw V stages [2 x 16K] at 160K.  P [128 x 64] 16-bit at 192K.
+    constexpr int NS = I8 ? 2 : kNS;  // stages of the TMA rings
     uint8_t* sK = sm;
-    uint8_t* sV = sm + (I8 ? 32768 : 98304);
-    uint8_t* sRawK = sm + 65536;
-    uint8_t* sRawV = sm + 114688;
+    uint8_t* sV = sm + (I8 ? 65536 : 98304);
+    uint8_t* sRawK = sm + 131072;
+    uint8_t* sRawV = sm + 163840;
     uint8_t* sP = sm + 196608;
-    float* sScale = reinterpret_cast<float*>(sm + 212992);  // Int8: [2 slots][64 K scales x log2(e)/16 | 64 V scales]
-    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 214016);
+    float* sScale = reinterpret_cast<float*>(sm + 212992);  // Int8: [4 slots][64 K scales x log2(e)/16 | 64 V scales]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 215040);
     uint64_t* kfull = bars + 0;      // [3] K tile (16-bit) / raw K tile (Int8) landed
     uint64_t* kempty = bars + 3;     // [3] stage free again: after Q K^T (16-bit) / after conversion (Int8)
     uint64_t* vfull = bars + 6;      // [3] V tile / raw V tile landed
@@ -152,13 +153,13 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
     uint64_t* o_done = bars + 18;
     uint64_t* q_full = bars + 19;
     uint64_t* drain = bars + 20;
-    uint64_t* kc_full = bars + 21;   // Int8: fp16 K tile written
-    uint64_t* kc_empty = bars + 22;  // Int8: Q K^T done with the fp16 K tile
-    uint64_t* vc_full = bars + 23;   // Int8: fp16 V tile written
-    uint64_t* vc_empty = bars + 24;  // Int8: P V done with the fp16 V tile
-    uint64_t* sc_full = bars + 25;   // Int8: [2] scale slot written
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 27);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 28);
+    uint64_t* kc_full = bars + 21;   // Int8: [2] fp16 K tile written
+    uint64_t* kc_empty = bars + 23;  // Int8: [2] Q K^T done with the fp16 K tile
+    uint64_t* vc_full = bars + 25;   // Int8: [2] fp16 V tile written
+    uint64_t* vc_empty = bars + 27;  // Int8: [2] P V done with the fp16 V tile
+    uint64_t* sc_full = bars + 29;   // Int8: [4] scale slot written
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 34);
     // TMEM columns: Q [0, 128) as 16-bit pairs, S [128, 192) and [192, 256), O [256, 512).
     constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
 
@@ -197,7 +198,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
     }
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kNS; ++s) {
+        for (int s = 0; s < NS; ++s) {
             tc::mbar_init(&kfull[s], 1);
             tc::mbar_init(&kempty[s], I8 ? 4 : 1);
             tc::mbar_init(&vfull[s], 1);
@@ -206,17 +207,17 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&s_full[s], 1);
             tc::mbar_init(&s_free[s], 4);
-            tc::mbar_init(&sc_full[s], 4);
+            tc::mbar_init(&kc_full[s], 4);
+            tc::mbar_init(&kc_empty[s], 1);
+            tc::mbar_init(&vc_full[s], 4);
+            tc::mbar_init(&vc_empty[s], 1);
         }
+        for (int s = 0; s < 4; ++s) tc::mbar_init(&sc_full[s], 4);
         tc::mbar_init(p_full, 4);
         tc::mbar_init(p_free, 1);
         tc::mbar_init(o_done, 1);
         tc::mbar_init(q_full, 4);
         tc::mbar_init(drain, 1);
-        tc::mbar_init(kc_full, 4);
-        tc::mbar_init(kc_empty, 1);
-        tc::mbar_init(vc_full, 4);
-        tc::mbar_init(vc_empty, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -239,8 +240,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             const int rowbase = (int)(((int64_t)b * p.HKV + kvh) * p.s_cap + k_begin);
             int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
-                const int st = j % kNS;
-                if (j >= kNS && !tc::mbar_wait(&emptyb[st], ((j / kNS) - 1) & 1, abort_flag)) break;
+                const int st = j % NS;
+                if (j >= NS && !tc::mbar_wait(&emptyb[st], ((j / NS) - 1) & 1, abort_flag)) break;
                 const int row = rowbase + j * kTcBK;
                 if (I8) {
                     tc::mbar_expect_tx(&fullb[st], kTcBK * kTcD);
@@ -254,13 +255,13 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                 issued = j + 1;
             }
             if (*abort_flag) {  // let our own copies land before the CTA goes away
-                for (int j = max(0, issued - kNS); j < issued; ++j) drain_wait(&fullb[j % kNS], (j / kNS) & 1);
+                for (int j = max(0, issued - NS); j < issued; ++j) drain_wait(&fullb[j % NS], (j / NS) & 1);
             }
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
-        // Event loop: issue whichever of the next Q K^T and the next P V is ready, so that a P V never waits
-        // behind a K tile that is still in flight.  Q K^T reads Q from TMEM.
+        // Event loop: issue whichever of the next P V and the next Q K^T is ready (P V first), so that a P V
+        // never waits behind a K tile that is still in flight.  Q K^T reads Q from TMEM.
         if (lane == 0) {
             const bool bf = p.mma_bf16 != 0;
             const uint32_t id_qk = tc::idesc_f16(bf, false, false, kTcRows, kTcBK);
@@ -273,31 +274,15 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             uint64_t t_idle = 0;
             while (ok && pj < ntiles) {
                 bool prog = false;
-                if (sj < ntiles) {
-                    const int sb = sj & 1, st = sj % kNS;
-                    bool ready = I8 ? tc::mbar_test(kc_full, sj & 1) : tc::mbar_test(&kfull[st], (sj / kNS) & 1);
-                    if (ready && sj >= 2) ready = tc::mbar_test(&s_free[sb], ((sj >> 1) - 1) & 1);
-                    if (ready) {
-                        tc::tc_fence_after();
-                        const uint32_t kbase = aK + (I8 ? 0 : st * kTileBytes);
-#pragma unroll
-                        for (int kk = 0; kk < kTcD / 16; ++kk) {
-                            const uint64_t db = tc::sdesc_sw128(kbase + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
-                            tc::mma_f16_ts(tmem + kColS + sb * kTcBK, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
-                        }
-                        tc::mma_commit(&s_full[sb]);
-                        tc::mma_commit(I8 ? kc_empty : &kempty[st]);
-                        ++sj;
-                        prog = true;
-                    }
-                }
+                // P V first: it is on the critical path (the softmax waits for it before writing the next P);
+                // an issued Q K^T would hold the tensor pipe for its whole duration in front of it.
                 if (pj < sj) {
-                    const int st = pj % kNS;
+                    const int st = pj % NS, cb = pj & 1;
                     bool ready = tc::mbar_test(p_full, pj & 1);
-                    if (ready) ready = I8 ? tc::mbar_test(vc_full, pj & 1) : tc::mbar_test(&vfull[st], (pj / kNS) & 1);
+                    if (ready) ready = I8 ? tc::mbar_test(&vc_full[cb], (pj >> 1) & 1) : tc::mbar_test(&vfull[st], (pj / NS) & 1);
                     if (ready) {
                         tc::tc_fence_after();
-                        const uint32_t vbase = aV + (I8 ? 0 : st * kTileBytes);
+                        const uint32_t vbase = aV + (I8 ? cb : st) * kTileBytes;
 #pragma unroll
                         for (int kk = 0; kk < kTcBK / 16; ++kk) {
                             const uint64_t da = tc::sdesc_sw128(aP + kk * 32, 16, 1024);
@@ -305,8 +290,26 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                             tc::mma_f16(tmem + kColO, da, db, id_pv, (pj > 0 || kk > 0) ? 1u : 0u);
                         }
                         tc::mma_commit(p_free);
-                        tc::mma_commit(I8 ? vc_empty : &vempty[st]);
+                        tc::mma_commit(I8 ? &vc_empty[cb] : &vempty[st]);
                         ++pj;
+                        prog = true;
+                    }
+                }
+                if (sj < ntiles) {
+                    const int sb = sj & 1, st = sj % NS;
+                    bool ready = I8 ? tc::mbar_test(&kc_full[sb], (sj >> 1) & 1) : tc::mbar_test(&kfull[st], (sj / NS) & 1);
+                    if (ready && sj >= 2) ready = tc::mbar_test(&s_free[sb], ((sj >> 1) - 1) & 1);
+                    if (ready) {
+                        tc::tc_fence_after();
+                        const uint32_t kbase = aK + (I8 ? sb : st) * kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kTcD / 16; ++kk) {
+                            const uint64_t db = tc::sdesc_sw128(kbase + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+                            tc::mma_f16_ts(tmem + kColS + sb * kTcBK, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
+                        }
+                        tc::mma_commit(&s_full[sb]);
+                        tc::mma_commit(I8 ? &kc_empty[sb] : &kempty[st]);
+                        ++sj;
                         prog = true;
                     }
                 }
@@ -335,12 +338,14 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
         const uint16_t* ksg = p.ks[layer] + seq_row;
         const uint16_t* vsg = p.vs[layer] + seq_row;
         for (int j = 0; j < ntiles; ++j) {
-            const int st = j % kNS, slot = j & 1;
-            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kfull[st], (j / kNS) & 1, abort_flag))) break;
+            const int st = j % NS, cb = j & 1, slot = j & 3;
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kfull[st], (j / NS) & 1, abort_flag))) break;
             const int key0 = k_begin + j * kTcBK;
             const int nk = min(kTcBK, k_end - key0);
-            if (j >= 1 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(kc_empty, (j - 1) & 1, abort_flag))) break;
-            {  // this tile's scales: threads 0-63 the K scales, 64-127 the V scales
+            if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kc_empty[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
+            {  // this tile's scales: threads 0-63 the K scales, 64-127 the V scales.  Slot j & 3 was last read by
+               // the softmax of tile j - 4, which finished before P V of tile j - 3 that the previous V
+               // conversion waited for.
                 const int key = ct & 63;
                 const uint16_t* src = ct < 64 ? ksg : vsg;
                 float v = key < nk ? f16_bits_to_f32(src[key0 + key]) : 0.f;
@@ -349,21 +354,21 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&sc_full[slot]);
             }
-            convert_i8_tile(sRawK + st * 16384, sK, nk, ct);
+            convert_i8_tile(sRawK + st * 16384, sK + cb * kTileBytes, nk, ct);
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 tc::mbar_arrive(&kempty[st]);
-                tc::mbar_arrive(kc_full);
+                tc::mbar_arrive(&kc_full[cb]);
             }
-            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / kNS) & 1, abort_flag))) break;
-            if (j >= 1 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(vc_empty, (j - 1) & 1, abort_flag))) break;
-            convert_i8_tile(sRawV + st * 16384, sV, nk, ct);
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / NS) & 1, abort_flag))) break;
+            if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vc_empty[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
+            convert_i8_tile(sRawV + st * 16384, sV + cb * kTileBytes, nk, ct);
             tc::fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
                 tc::mbar_arrive(&vempty[st]);
-                tc::mbar_arrive(vc_full);
+                tc::mbar_arrive(&vc_full[cb]);
             }
         }
     } else if (warp < 4) {
@@ -417,8 +422,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&s_free[sb]);
-            const float* ksc = sScale + sb * 128;  // Int8: [64 K scales x log2(e)/16 | 64 V scales]
-            if (I8 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&sc_full[sb], (j >> 1) & 1, abort_flag))) { ok = false; break; }
+            const float* ksc = sScale + (j & 3) * 128;  // Int8: [64 K scales x log2(e)/16 | 64 V scales]
+            if (I8 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&sc_full[j & 3], (j >> 2) & 1, abort_flag))) { ok = false; break; }
 
             const int c0 = k_begin + j * kTcBK;
             // Scores in the log2 domain.  Tiles whose 64 keys are all history keys inside the range need no mask.
@@ -491,8 +496,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                 }
             }
             if (!I8 && c0 + kTcBK > k_end) {  // last tile: zero V rows past the key range (their bytes are not ours)
-                const int st = j % kNS;
-                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / kNS) & 1, abort_flag))) { ok = false; break; }
+                const int st = j % NS;
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / NS) & 1, abort_flag))) { ok = false; break; }
                 const int nk = k_end - c0;
                 uint8_t* vb = sV + st * kTileBytes;
                 for (int e = r; e < (kTcBK - nk) * 32; e += kTcRows) {

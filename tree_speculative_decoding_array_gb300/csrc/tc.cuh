@@ -50,15 +50,18 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Waits for the phase with the given parity to complete.  Gives up (returns
-// false and raises *abort) after kWaitNs nanoseconds of waiting, or as soon as
-// another thread of the CTA raised *abort; no wait can hang the kernel.
+// Waits for the phase with the given parity to complete, polling with the non-suspending test_wait (a warp
+// parked in a suspending try_wait was seen to resume microseconds after the phase completed, which puts that
+// latency on every hand-off of a pipeline) and backing off with short sleeps after the first polls.  Gives up
+// (returns false and raises *abort) after kWaitNs nanoseconds, or as soon as another thread of the CTA raised
+// *abort; no wait can hang the kernel.
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s: far above any legitimate wait
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_test(bar, parity)) return true;
+        if (i > 16) __nanosleep(32);
         if ((i & 63) == 0) {
             if (*abort) return false;
             if (globaltimer() - t0 > kWaitNs) {
@@ -69,8 +72,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
 }
 
-// As mbar_wait, but polling with the non-suspending test_wait: for the single MMA-issuing thread, whose
-// reaction time to a completed phase is on the critical path.
+// The MMA-issuing thread polls without sleeping: its reaction time is on the critical path of every MMA.
 __device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity, volatile int* abort) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
