@@ -8,24 +8,25 @@
 // #728, "Earlier shader evidence": split-KV tree attention with fp32 partials
 // and statistics; mlxcel issue #1204, "What this needs" item 1).
 //
-// One CTA = one 128-row tile of one unit and one key range; 192 threads:
+// One CTA = one 128-row tile of one unit and one key range; 224 threads:
 //   warps 0-3  softmax warpgroup: thread r owns query row r = TMEM lane r.
 //              Stores Q into TMEM, reads S from TMEM, applies the
 //              scale and the ancestor bits, runs the online softmax (fp32,
 //              log2 domain, lazy rescale of O when the max grows by > 2^8),
 //              writes P as 16-bit into shared memory, finally reads O.
-//   warp 4     TMA producers (lane 0: K, lane 16: V): tiles of 64 keys x
+//   warp 4, 6  TMA producers (4: K, 6: V; one lane each): tiles of 64 keys x
 //              256, 128-byte swizzled, each in its own 3-stage ring (a K
 //              stage frees after Q K^T, a V stage after P V).
 //   warp 5     allocates TMEM (512 columns: Q 128 as 16-bit pairs, S 2 x 64,
 //              O 256) and issues the MMAs from an event loop:
 //              S = Q K^T (M=128, N=64, K=256, A read from TMEM) and
 //              O += P V (M=128, N=256, K=64, V read MN-major).
-// Int8 caches (Int8 codes with fp16 per-token scales) add warps 6-9, a
-// converter group: TMA brings the raw int8 tiles into 2-stage staging
-// rings, the converter writes them as fp16 into 2-stage operand rings, the converter writes the codes as fp16 (exact) into the operand
-// tiles and the tile's scales into shared memory; the softmax warpgroup
-// multiplies S column c by k_scale[c] and folds v_scale[c] into P.
+// Int8 caches (Int8 codes with fp16 per-token scales) use 352 threads: warps
+// 6-9 are a converter group and warp 10 the V producer.  TMA brings the raw
+// int8 tiles into 2-stage staging rings; the converter writes the codes as
+// fp16 (exact) into 2-stage operand rings and the tile's scales into shared
+// memory; the softmax warpgroup multiplies S column c by k_scale[c] and folds
+// v_scale[c] into P.
 // Warp-collective roles take every wait decision warp-uniformly (__all_sync),
 // so that tcgen05.ld / __syncwarp never see a partial warp.
 // Every mbarrier wait is bounded in time: on expiry the CTA raises a shared
@@ -41,8 +42,8 @@ namespace tsv {
 constexpr int kTcRows = 128;
 constexpr int kTcBK = 64;
 constexpr int kTcD = 256;
-constexpr int kTcThreads16 = 192;
-constexpr int kTcThreadsI8 = 320;
+constexpr int kTcThreads16 = 224;  // + warp 6: V producer
+constexpr int kTcThreadsI8 = 352;  // + warps 6-9: converters, warp 10: V producer
 constexpr int kTcSmem = 1024 + 215040 + 512;
 constexpr uint32_t kTileBytes = kTcBK * kTcD * 2;  // one K (or V) tile: 32 KiB
 
@@ -229,10 +230,12 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ TMA producers: lane 0 K, lane 16 V
-        if (lane == 0 || lane == 16) {
-            const bool isK = lane == 0;
+    const int vwarp = I8 ? 10 : 6;
+    if (warp == 4 || warp == vwarp) {
+        // ------------------------------------------------------------ TMA producers: warp 4 K, the last warp V
+        // (a warp each: a lane that sleeps in its wait would hold up the other producer)
+        if (lane == 0) {
+            const bool isK = warp == 4;
             const CUtensorMap* m = isK ? &p.kmap[layer] : &p.vmap[layer];
             uint64_t* fullb = isK ? kfull : vfull;
             uint64_t* emptyb = isK ? kempty : vempty;
@@ -241,7 +244,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             int issued = 0;
             for (int j = 0; j < ntiles; ++j) {
                 const int st = j % NS;
-                if (j >= NS && !tc::mbar_wait(&emptyb[st], ((j / NS) - 1) & 1, abort_flag)) break;
+                if (j >= NS && !tc::mbar_wait(&emptyb[st], ((j / NS) - 1) & 1, abort_flag, 256)) break;
                 const int row = rowbase + j * kTcBK;
                 if (I8) {
                     tc::mbar_expect_tx(&fullb[st], kTcBK * kTcD);
@@ -331,7 +334,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                 drain_wait(drain, 0);
             }
         }
-    } else if (I8 && warp >= 6) {
+    } else if (I8 && warp >= 6 && warp < 10) {
         // ------------------------------------------------------------ Int8 converter group
         const int ct = threadIdx.x - 192;
         const size_t seq_row = ((size_t)b * p.HKV + kvh) * (size_t)p.s_cap;

@@ -289,7 +289,9 @@ extern "C" tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32
     if (cudaMemsetAsync(best, 0, (size_t)rows * sizeof(unsigned long long), stream) != cudaSuccess)
         return check_launch("lm_head_argmax(memset)");
     // More than one 8-row pass: the tensor-core kernel, when the workspace also holds what it needs.
-    if (lm_tc_applies(rows, H, V, w_dtype) && ws_bytes >= best_bytes(rows) + lm_tc_extra_bytes(rows, H, w_dtype)) {
+    const bool sb_aligned = w_dtype != TSV_Q4_G64 || ((((uintptr_t)scales | (uintptr_t)biases) & 15) == 0);
+    if (lm_tc_applies(rows, H, V, w_dtype) && sb_aligned &&
+        ws_bytes >= best_bytes(rows) + lm_tc_extra_bytes(rows, H, w_dtype)) {
         tsv_status st = launch_lm_tc(hidden, rows, H, V, w_dtype, W, scales, biases, best,
                                      (char*)workspace + best_bytes(rows), stream);
         if (st != TSV_OK) return st;

@@ -1,4 +1,4 @@
-// Tensor-core (tcgen05) path of tsv_lm_head_argmax for many hidden rows.
+// Tensor-core (tcgen05) paths of tsv_lm_head_argmax for many hidden rows.
 //
 // Same operation as the CUDA-core GEMV in lm_head.cu (mlxcel issue #1185,
 // "Phase 2" item 2a: projection fused with the argmax, logits never written;
@@ -7,24 +7,29 @@
 //
 // Swap-AB: one MMA tile is D[128 vocabulary rows x NP hidden rows] =
 // W_tile[128 x 64] . hidden_chunk[NP x 64]^T, accumulated over H / 64
-// k-blocks in TMEM (two 256-column buffers, so the argmax of one vocabulary
-// tile overlaps the MMAs of the next).  Warps:
-//   0-3   epilogue: TMEM lane = vocabulary row; per hidden row (column) a
-//         warp-shuffle max of the packed (logit, ~index) key, then a shared
-//         atomic max; the CTA's bests go to global memory once at the end.
-//   4     TMA producer (W block [128 x 64] swizzled, or the raw 4-bit block
-//         [128 x 32 bytes]; hidden block [NP x 64] swizzled) into a ring of
-//         as many stages (up to 16) as shared memory holds for this NP, so
-//         that narrow hidden chunks still keep ~100 KB per SM in flight.
-//   5     TMEM allocation and MMA issue.
-//   6-13  (4-bit heads) converter: w = scale * q + bias evaluated in fp16
-//         with one rounding (q exact via the 1024 + q trick), written into
-//         a separate 3-stage ring of swizzled A blocks.  The hidden rows arrive as fp16 too (a copy
-//         made by a small kernel into the workspace); fp16 keeps the
-//         dequantised weights within 2^-11 relative.
-// A CTA keeps one chunk of hidden rows and walks vocabulary tiles strided
-// by the number of CTAs per chunk, so CTAs working on one tile run together
-// and the tile's second and later reads hit L2.
+// k-blocks in TMEM (two accumulator buffers, so the argmax of one vocabulary
+// tile overlaps the MMAs of the next).  A CTA keeps one chunk of hidden rows
+// and walks vocabulary tiles strided by the number of CTAs per chunk, so CTAs
+// working on one tile run together and the tile's second and later reads hit
+// L2.  The epilogue (warps 0-3, TMEM lane = vocabulary row) finds, per hidden
+// row, the warp's largest logit with a 32-bit warp maximum and the lowest lane
+// holding it, and merges the packed (logit, ~index) key with a shared atomic
+// maximum; the CTA's bests go to global memory once at the end.
+//
+// 16-bit heads (lm_tc_kernel): warp 4 streams W block [128 x 64] and hidden
+// block [NP x 64] (both 128-byte swizzled) through one ring of as many stages
+// (up to 16) as shared memory holds; warp 5 issues the MMAs from shared memory.
+//
+// 4-bit heads (lm_q4_kernel): the dequantised weights never touch shared
+// memory.  Warp 4 streams the raw codes of 8 k-blocks plus their scales and
+// biases per stage, warp 14 the hidden blocks, through separate rings;
+// 8 converter warps (6-13) evaluate w = scale * q + bias in fp16 with one
+// rounding (q exact via the 1024 + q bit trick) and store the A operand
+// straight into TMEM slots with tcgen05.st; warp 5 issues MMAs whose A
+// operand is read from TMEM.  The converter emits a code word's 8 features in
+// the order (0,4,1,5,2,6,3,7) (one mask per pair of features); the fp16 copy
+// of the hidden rows is written in the same order, so both operands agree.
+// fp16 keeps the dequantised weights within 2^-11 relative.
 #include <cuda.h>
 
 #include "common.cuh"
@@ -35,57 +40,72 @@ namespace tsv {
 constexpr int kLmM = 128;
 constexpr int kLmKB = 64;
 constexpr int kLmEpi = 128;
-constexpr int kLmConv = 256;
+constexpr int kLmSmem = 224 * 1024;               // dynamic shared memory requested
+constexpr int kLmUsable = kLmSmem - 1024 - 4096;  // minus alignment slack and the tail (bests + barriers)
+
+// ------------------------------------------------------------------ shared pieces
+__device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
+    return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
+}
+
+// Argmax of one accumulator tile over this warp's 32 vocabulary rows, for each of the nrows hidden rows
+// (TMEM columns starting at taddr).  v = this lane's vocabulary row; rows >= V never win.
+__device__ __forceinline__ void lm_epilogue_tile(uint32_t taddr, int nrows, int v, int V,
+                                                 unsigned long long* s_best, int lane) {
+    const uint32_t v0 = (uint32_t)(v - lane);
+    for (int c0 = 0; c0 < nrows; c0 += 32) {
+        uint32_t d[32];
+        tc::tmem_ld32(taddr + c0, d);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            if (c0 + k < nrows) {  // uniform across the warp
+                const uint32_t o = v < V ? orderable(__uint_as_float(d[k])) : 0u;
+                const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, o);
+                const uint32_t who = __ballot_sync(0xFFFFFFFFu, o == mx);
+                if (lane == 0 && mx != 0u) {
+                    const uint32_t idx = v0 + (uint32_t)(__ffs(who) - 1);
+                    atomicMax(&s_best[c0 + k], ((unsigned long long)mx << 32) | (unsigned long long)(0xFFFFFFFFu - idx));
+                }
+            }
+        }
+    }
+}
+
+// Bounded wait used only while draining after an abort.
+__device__ __forceinline__ void lm_drain_wait(uint64_t* bar, uint32_t parity) {
+    const uint64_t t0 = tc::globaltimer();
+    while (!tc::mbar_try_wait(bar, parity))
+        if (tc::globaltimer() - t0 > 200000000ull) break;  // 200 ms
+}
+
+// ------------------------------------------------------------------ 16-bit heads
+constexpr int kLmMaxStages = 16;
+constexpr int kLmThreads16 = kLmEpi + 64;
 
 struct LmTcParams {
     CUtensorMap wmap;
     CUtensorMap hmap;
-    const uint16_t* scales;
-    const uint16_t* biases;
     unsigned long long* best;
     int rows, H, V, NP, nchunks, vtiles, mma_bf16, stages, stage_bytes;
-    int sb_vec;  // scales/biases 16-byte aligned with H / 64 a multiple of 8: 8 groups per vector load
 };
 
-constexpr int kLmMaxStages = 16;
-constexpr int kLmConvStages = 3;
-constexpr int kLmSmem = 224 * 1024;     // dynamic shared memory requested
-constexpr int kLmUsable = kLmSmem - 1024 - 4096;  // minus alignment slack and the tail (bests + barriers)
-
-template <bool Q4>
-struct LmLayout {
-    static constexpr int kW = Q4 ? 4096 : 16384;  // per stage: raw 4-bit block [128 x 32 B] or W block [128 x 64]
-    static constexpr int kConv = Q4 ? kLmConvStages * 16384 : 0;  // dequantised fp16 A blocks
-    static constexpr int kThreads = Q4 ? kLmEpi + 64 + kLmConv : kLmEpi + 64;
-};
-
-__device__ __forceinline__ uint64_t shfl_xor_u64(uint64_t v, int o) {
-    const uint32_t lo = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)v, o);
-    const uint32_t hi = __shfl_xor_sync(0xFFFFFFFFu, (uint32_t)(v >> 32), o);
-    return ((uint64_t)hi << 32) | lo;
-}
-
-// Shared memory: [conv ring (4-bit)] [TMA ring: stages x (W or raw block | hidden block)] ... [bests | barriers]
-template <bool Q4>
-__global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const __grid_constant__ LmTcParams p) {
-    using L = LmLayout<Q4>;
+// Shared memory: [TMA ring: stages x (W block 16 KB | hidden block NP x 128 B)] ... [bests | barriers]
+__global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_constant__ LmTcParams p) {
     const int S = p.stages;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t* conv = sm;                // [kLmConvStages][128 x 64] fp16 (4-bit heads)
-    uint8_t* ring = sm + L::kConv;     // [S][stage_bytes]
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* ring = sm;  // [S][stage_bytes]
     uint8_t* tail = sm + kLmUsable;
     unsigned long long* s_best = reinterpret_cast<unsigned long long*>(tail);  // [256]
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail + 2048);
-    uint64_t* full = bars;                       // [16]
-    uint64_t* empty = bars + 16;                 // [16]
-    uint64_t* conv_full = bars + 32;             // [3]
-    uint64_t* conv_empty = bars + 35;            // [3]
-    uint64_t* acc_full = bars + 38;              // [2]
-    uint64_t* acc_empty = bars + 40;             // [2]
-    uint64_t* drain = bars + 42;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 43);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 44);
+    uint64_t* full = bars;            // [16]
+    uint64_t* empty = bars + 16;      // [16]
+    uint64_t* acc_full = bars + 32;   // [2]
+    uint64_t* acc_empty = bars + 34;  // [2]
+    uint64_t* drain = bars + 36;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 37);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 38);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = blockIdx.x % p.nchunks;
@@ -98,11 +118,7 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
             tc::mbar_init(&full[s], 1);
-            tc::mbar_init(&empty[s], Q4 ? 1 + kLmConv / 32 : 1);
-        }
-        for (int s = 0; s < kLmConvStages; ++s) {
-            tc::mbar_init(&conv_full[s], kLmConv / 32);
-            tc::mbar_init(&conv_empty[s], 1);
+            tc::mbar_init(&empty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&acc_full[s], 1);
@@ -132,153 +148,314 @@ __global__ void __launch_bounds__(LmLayout<Q4>::kThreads, 1) lm_tc_kernel(const 
             for (int vt = group; ok && vt < p.vtiles; vt += groups) {
                 for (int kb = 0; kb < KB; ++kb, ++g) {
                     const int st = g % S;
-                    if (g >= S && !tc::mbar_wait(&empty[st], ((g / S) - 1) & 1, abort_flag)) { ok = false; break; }
+                    if (g >= S && !tc::mbar_wait(&empty[st], ((g / S) - 1) & 1, abort_flag, 256)) { ok = false; break; }
                     uint8_t* stage = ring + st * p.stage_bytes;
-                    tc::mbar_expect_tx(&full[st], L::kW + b_bytes);
-                    if (Q4) tc::tma_load_2d(stage, &p.wmap, &full[st], kb * 32, vt * kLmM);
-                    else tc::tma_load_2d(stage, &p.wmap, &full[st], kb * kLmKB, vt * kLmM);
-                    tc::tma_load_2d(stage + L::kW, &p.hmap, &full[st], kb * kLmKB, chunk * p.NP);
+                    tc::mbar_expect_tx(&full[st], 16384 + b_bytes);
+                    tc::tma_load_2d(stage, &p.wmap, &full[st], kb * kLmKB, vt * kLmM);
+                    tc::tma_load_2d(stage + 16384, &p.hmap, &full[st], kb * kLmKB, chunk * p.NP);
                     issued = g + 1;
                 }
             }
             if (*abort_flag)
-                for (int q = max(0, issued - S); q < issued; ++q) {
-                    const uint64_t t0 = tc::globaltimer();
-                    while (!tc::mbar_try_wait(&full[q % S], (q / S) & 1))
-                        if (tc::globaltimer() - t0 > 200000000ull) break;
-                }
+                for (int q = max(0, issued - S); q < issued; ++q) lm_drain_wait(&full[q % S], (q / S) & 1);
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_f16(p.mma_bf16 != 0, false, false, kLmM, p.NP);
-            const uint32_t rbase = tc::smem_u32(ring), cbase = tc::smem_u32(conv);
-            int g = 0, it = 0;
+            const uint32_t rbase = tc::smem_u32(ring);
+            int it = 0, st = 0;
+            uint32_t ph = 0;  // phase parity of the ring
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups, ++it) {
                 const int buf = it & 1;
                 if (it >= 2 && !tc::mbar_wait_spin(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
-                for (int kb = 0; kb < KB; ++kb, ++g) {
-                    const int st = g % S, cs = g % kLmConvStages;
-                    if (!tc::mbar_wait_spin(&full[st], (g / S) & 1, abort_flag)) { ok = false; break; }
-                    if (Q4 && !tc::mbar_wait_spin(&conv_full[cs], (g / kLmConvStages) & 1, abort_flag)) { ok = false; break; }
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!tc::mbar_wait_spin(&full[st], ph, abort_flag)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t sa = Q4 ? cbase + cs * 16384 : rbase + st * p.stage_bytes;
-                    const uint32_t sb = rbase + st * p.stage_bytes + L::kW;
+                    const uint32_t sa = rbase + st * p.stage_bytes;
 #pragma unroll
                     for (int kk = 0; kk < kLmKB / 16; ++kk)
                         tc::mma_f16(tmem + buf * 256, tc::sdesc_sw128(sa + kk * 32, 16, 1024),
-                                    tc::sdesc_sw128(sb + kk * 32, 16, 1024), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                                    tc::sdesc_sw128(sa + 16384 + kk * 32, 16, 1024), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
                     tc::mma_commit(&empty[st]);
-                    if (Q4) tc::mma_commit(&conv_empty[cs]);
+                    if (++st == S) { st = 0; ph ^= 1u; }
                 }
                 if (ok) tc::mma_commit(&acc_full[buf]);
             }
             tc::mma_commit(drain);
-            const uint64_t t0 = tc::globaltimer();
-            while (!tc::mbar_try_wait(drain, 0))
-                if (tc::globaltimer() - t0 > 200000000ull) break;
+            lm_drain_wait(drain, 0);
         }
-    } else if (Q4 && warp >= 6) {
-        // ------------------------------------------------------------ 4-bit converter
-        const int ct = threadIdx.x - (kLmEpi + 64);
-        const int row = ct >> 1, half = ct & 1;
-        const int ng = p.H >> 6;
-        const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
-        // Scales and biases of this thread's row, 8 groups per 16-byte load, fetched one group of 8 ahead.
-        const bool vec = p.sb_vec != 0;
-        uint4 s_cur = make_uint4(0, 0, 0, 0), b_cur = s_cur, s_nxt = s_cur, b_nxt = s_cur;
-        auto fetch8 = [&](int vt_, int kb_) {
-            const int v_ = vt_ * kLmM + row;
-            if (vt_ < p.vtiles && v_ < p.V && kb_ < KB) {
-                s_nxt = *reinterpret_cast<const uint4*>(p.scales + (size_t)v_ * ng + kb_);
-                b_nxt = *reinterpret_cast<const uint4*>(p.biases + (size_t)v_ * ng + kb_);
-            }
-        };
-        if (vec) fetch8(group, 0);
-        int g = 0;
-        bool ok = true;
-        for (int vt = group; ok && vt < p.vtiles; vt += groups) {
-            const int v = vt * kLmM + row;
-            const bool vok = v < p.V;
-            for (int kb = 0; kb < KB; ++kb, ++g) {
-                const int st = g % S, cs = g % kLmConvStages;
-                float sc, bi;
-                if (vec) {
-                    if ((kb & 7) == 0) {
-                        s_cur = s_nxt;
-                        b_cur = b_nxt;
-                        if (kb + 8 < KB) fetch8(vt, kb + 8);
-                        else fetch8(vt + groups, 0);
-                    }
-                    const int e = kb & 7, wsel = e >> 1;
-                    const uint32_t sw = wsel == 0 ? s_cur.x : wsel == 1 ? s_cur.y : wsel == 2 ? s_cur.z : s_cur.w;
-                    const uint32_t bw = wsel == 0 ? b_cur.x : wsel == 1 ? b_cur.y : wsel == 2 ? b_cur.z : b_cur.w;
-                    sc = vok ? ((e & 1) ? bf16_hi(sw) : bf16_lo(sw)) : 0.f;
-                    bi = vok ? ((e & 1) ? bf16_hi(bw) : bf16_lo(bw)) : 0.f;
-                } else {
-                    sc = vok ? bf16_bits_to_f32(p.scales[(size_t)v * ng + kb]) : 0.f;
-                    bi = vok ? bf16_bits_to_f32(p.biases[(size_t)v * ng + kb]) : 0.f;
-                }
-                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&full[st], (g / S) & 1, abort_flag))) { ok = false; break; }
-                if (g >= kLmConvStages &&
-                    !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&conv_empty[cs], ((g / kLmConvStages) - 1) & 1, abort_flag))) { ok = false; break; }
-                const uint4 raw = *reinterpret_cast<const uint4*>(ring + st * p.stage_bytes + row * 32 + half * 16);
-                const __half2 s2 = __floats2half2_rn(sc, sc), b2 = __floats2half2_rn(bi, bi);
-                const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
-                uint32_t out[16];
-#pragma unroll
-                for (int k = 0; k < 4; ++k)
-#pragma unroll
-                    for (int by = 0; by < 4; ++by) {
-                        const uint32_t x = w[k] >> (8 * by);
-                        uint32_t h = (x & 0xFu) | ((x & 0xF0u) << 12) | 0x64006400u;  // (1024 + lo, 1024 + hi)
-                        __half2 q = __hsub2(*reinterpret_cast<__half2*>(&h), k1024);
-                        __half2 r = __hfma2(q, s2, b2);
-                        out[4 * k + by] = *reinterpret_cast<uint32_t*>(&r);
-                    }
-                uint8_t* arow = conv + cs * 16384 + row * 128;
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const int chk = half * 4 + q;
-                    *reinterpret_cast<uint4*>(arow + ((chk ^ (row & 7)) << 4)) =
-                        make_uint4(out[4 * q], out[4 * q + 1], out[4 * q + 2], out[4 * q + 3]);
-                }
-                tc::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    tc::mbar_arrive(&empty[st]);
-                    tc::mbar_arrive(&conv_full[cs]);
-                }
-            }
-        }
-    } else if (warp < 4) {
+    } else {
         // ------------------------------------------------------------ argmax epilogue
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         int it = 0;
         for (int vt = group; vt < p.vtiles; vt += groups, ++it) {
             const int buf = it & 1;
-            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag))) break;
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, 1024))) break;
             tc::tc_fence_after();
-            const int v = vt * kLmM + warp * 32 + lane;
-            for (int c0 = 0; c0 < nrows; c0 += 32) {
-                uint32_t d[32];
-                tc::tmem_ld32(tmem + lane_base + buf * 256 + c0, d);
-                tc::tmem_wait_ld();
+            lm_epilogue_tile(tmem + lane_base + buf * 256, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane);
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
+        }
+    }
+
+    __syncthreads();
+    if (!*abort_flag)
+        for (int c = threadIdx.x; c < nrows; c += blockDim.x)
+            if (s_best[c]) atomicMax(&p.best[chunk * p.NP + c], s_best[c]);
+    if (warp == 5) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ 4-bit heads
+constexpr int kQ4Conv = 256;                          // 8 converter warps (two sets of the four TMEM lane quarters)
+constexpr int kQ4Threads = kLmEpi + 64 + kQ4Conv + 32;  // + warp 14: hidden-block producer
+constexpr int kQ4KBPerStage = 8;                      // k-blocks of 64 features per W stage
+constexpr int kQ4WStages = 3;
+constexpr int kQ4WStage = 2 * 16384 + 2 * 2048;       // codes [128 rows x 256 B] as two swizzled boxes, scales, biases
+constexpr int kQ4HOff = kQ4WStages * kQ4WStage;       // hidden ring after the W ring
+constexpr int kQ4MaxHStages = 16;
+constexpr int kQ4MaxASlots = 14;
+constexpr int kQ4MaxNP = 128;
+
+struct LmQ4Params {
+    CUtensorMap wmap;  // codes, UINT8 [V][H/2], box {128 B, 128 rows}, 128-byte swizzle
+    CUtensorMap smap;  // scales, UINT16 [V][H/64], box {8, 128}
+    CUtensorMap bmap;  // biases, same
+    CUtensorMap hmap;  // fp16 hidden copy in converter feature order, UINT16 [rows][H], box {64, NP}, swizzled
+    unsigned long long* best;
+    int rows, H, V, NP, DC, NA, HS, nchunks, vtiles;
+};
+
+// One 32-bit word of codes (features 8j..8j+7, feature 8j+i in bits 4i..4i+3) -> four fp16 pairs
+// (8j+m, 8j+m+4), m = 0..3, each w = scale * q + bias with a single rounding.
+__device__ __forceinline__ void q4_word(uint32_t x, __half2 s2, __half2 b2, __half2 k1024, uint32_t* out) {
 #pragma unroll
-                for (int k = 0; k < 32; ++k) {
-                    if (c0 + k < nrows) {  // uniform across the warp
-                        uint64_t key = v < p.V ? pack_best(__uint_as_float(d[k]), (uint32_t)v) : 0ull;
-#pragma unroll
-                        for (int o = 16; o > 0; o >>= 1) {
-                            const uint64_t other = shfl_xor_u64(key, o);
-                            key = other > key ? other : key;
-                        }
-                        if (lane == 0) atomicMax(&s_best[c0 + k], (unsigned long long)key);
+    for (int m = 0; m < 4; ++m) {
+        uint32_t h = ((x >> (4 * m)) & 0x000F000Fu) | 0x64006400u;  // (1024 + q_m, 1024 + q_{m+4}), exact
+        const __half2 q = __hsub2(*reinterpret_cast<__half2*>(&h), k1024);
+        const __half2 w = __hfma2(q, s2, b2);
+        out[m] = *reinterpret_cast<const uint32_t*>(&w);
+    }
+}
+
+__device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
+    return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Shared memory: [W ring: 3 x 36 KB] [hidden ring: HS x NP*128 B] ... [bests | barriers].
+// TMEM: accumulators [0, DC) and [DC, 2 DC); A slots of 32 columns (one k-block) from 2 DC.
+__global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_constant__ LmQ4Params p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* wring = sm;
+    uint8_t* hring = sm + kQ4HOff;
+    uint8_t* tail = sm + kLmUsable;
+    unsigned long long* s_best = reinterpret_cast<unsigned long long*>(tail);  // [256]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tail + 2048);
+    uint64_t* wfull = bars;           // [3] codes, scales and biases of a stage landed
+    uint64_t* wempty = bars + 3;      // [3] every converter warp is done with the stage
+    uint64_t* hfull = bars + 6;       // [16] hidden block landed
+    uint64_t* hempty = bars + 22;     // [16] MMAs done with the hidden block
+    uint64_t* afull = bars + 38;      // [14] A slot written (4 converter warps)
+    uint64_t* aempty = bars + 52;     // [14] MMAs done with the A slot
+    uint64_t* acc_full = bars + 66;   // [2]
+    uint64_t* acc_empty = bars + 68;  // [2]
+    uint64_t* drain = bars + 70;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 71);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 72);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunk = blockIdx.x % p.nchunks;
+    const int group = blockIdx.x / p.nchunks;
+    const int groups = gridDim.x / p.nchunks;
+    const int KB = p.H / kLmKB;
+    const int NSt = KB / kQ4KBPerStage;  // W stages per vocabulary tile
+    const int NA = p.NA, HS = p.HS;
+    const int nrows = min(p.NP, p.rows - chunk * p.NP);
+    if (group >= p.vtiles || nrows <= 0) return;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kQ4WStages; ++s) {
+            tc::mbar_init(&wfull[s], 1);
+            tc::mbar_init(&wempty[s], kQ4Conv / 32);
+        }
+        for (int s = 0; s < HS; ++s) {
+            tc::mbar_init(&hfull[s], 1);
+            tc::mbar_init(&hempty[s], 1);
+        }
+        for (int s = 0; s < NA; ++s) {
+            tc::mbar_init(&afull[s], 4);
+            tc::mbar_init(&aempty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&acc_full[s], 1);
+            tc::mbar_init(&acc_empty[s], kLmEpi / 32);
+        }
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    for (int c = threadIdx.x; c < 256; c += blockDim.x) s_best[c] = 0ull;
+    if (warp == 5) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t a_col = 2u * (uint32_t)p.DC;
+    const uint32_t h_bytes = (uint32_t)p.NP * 128;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            // -------------------------------------------------------- W stages: codes, scales, biases of 8 k-blocks
+            // (each producer has a warp of its own: a lane that sleeps in its wait holds up the other lanes)
+            tc::tma_prefetch_desc(&p.wmap);
+            tc::tma_prefetch_desc(&p.smap);
+            tc::tma_prefetch_desc(&p.bmap);
+            int c = 0, issued = 0;
+            bool ok = true;
+            for (int vt = group; ok && vt < p.vtiles; vt += groups) {
+                for (int i = 0; i < NSt; ++i, ++c) {
+                    const int s = c % kQ4WStages;
+                    if (c >= kQ4WStages && !tc::mbar_wait(&wempty[s], ((c / kQ4WStages) - 1) & 1, abort_flag, 512)) {
+                        ok = false;
+                        break;
                     }
+                    uint8_t* st = wring + s * kQ4WStage;
+                    tc::mbar_expect_tx(&wfull[s], kQ4WStage);
+                    tc::tma_load_2d(st, &p.wmap, &wfull[s], i * 256, vt * kLmM);
+                    tc::tma_load_2d(st + 16384, &p.wmap, &wfull[s], i * 256 + 128, vt * kLmM);
+                    tc::tma_load_2d(st + 32768, &p.smap, &wfull[s], i * kQ4KBPerStage, vt * kLmM);
+                    tc::tma_load_2d(st + 34816, &p.bmap, &wfull[s], i * kQ4KBPerStage, vt * kLmM);
+                    issued = c + 1;
                 }
             }
+            if (*abort_flag)
+                for (int q = max(0, issued - kQ4WStages); q < issued; ++q)
+                    lm_drain_wait(&wfull[q % kQ4WStages], (q / kQ4WStages) & 1);
+        }
+    } else if (warp == 14) {
+        if (lane == 0) {
+            // -------------------------------------------------------- hidden blocks, one per k-block
+            tc::tma_prefetch_desc(&p.hmap);
+            int g = 0, issued = 0;
+            bool ok = true;
+            for (int vt = group; ok && vt < p.vtiles; vt += groups) {
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    const int s = g % HS;
+                    if (g >= HS && !tc::mbar_wait(&hempty[s], ((g / HS) - 1) & 1, abort_flag, 512)) { ok = false; break; }
+                    tc::mbar_expect_tx(&hfull[s], h_bytes);
+                    tc::tma_load_2d(hring + s * h_bytes, &p.hmap, &hfull[s], kb * kLmKB, chunk * p.NP);
+                    issued = g + 1;
+                }
+            }
+            if (*abort_flag)
+                for (int q = max(0, issued - HS); q < issued; ++q) lm_drain_wait(&hfull[q % HS], (q / HS) & 1);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer: A from TMEM, hidden from smem
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_f16(false, false, false, kLmM, p.NP);
+            const uint32_t hbase = tc::smem_u32(hring);
+            int it = 0, as = 0, hs = 0;
+            uint32_t aph = 0, hph = 0;  // phase parities of the A-slot and hidden rings
+            bool ok = true;
+            for (int vt = group; ok && vt < p.vtiles; vt += groups, ++it) {
+                const int buf = it & 1;
+                if (it >= 2 && !tc::mbar_wait_spin(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+                tc::tc_fence_after();
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!tc::mbar_wait_spin(&afull[as], aph, abort_flag)) { ok = false; break; }
+                    if (!tc::mbar_wait_spin(&hfull[hs], hph, abort_flag)) { ok = false; break; }
+                    tc::tc_fence_after();
+                    const uint32_t a = tmem + a_col + (uint32_t)as * 32;
+                    const uint32_t b = hbase + (uint32_t)hs * h_bytes;
+#pragma unroll
+                    for (int kk = 0; kk < kLmKB / 16; ++kk)
+                        tc::mma_f16_ts(tmem + buf * p.DC, a + kk * 8, tc::sdesc_sw128(b + kk * 32, 16, 1024), idesc,
+                                       (kb > 0 || kk > 0) ? 1u : 0u);
+                    tc::mma_commit(&aempty[as]);
+                    tc::mma_commit(&hempty[hs]);
+                    if (++as == NA) { as = 0; aph ^= 1u; }
+                    if (++hs == HS) { hs = 0; hph ^= 1u; }
+                }
+                if (ok) tc::mma_commit(&acc_full[buf]);
+            }
+            tc::mma_commit(drain);
+            lm_drain_wait(drain, 0);
+        }
+    } else if (warp >= 6) {
+        // ------------------------------------------------------------ converters (warps 6-13): codes -> fp16 A slots
+        // Set `par` converts the k-blocks g with g % 2 == par; its four warps cover the four TMEM lane quarters.
+        const int par = (warp - 6) >> 2, quad = warp & 3;
+        const int r = quad * 32 + lane;  // vocabulary row within the tile = TMEM lane
+        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+        int c = 0, g = 0;
+        bool ok = true;
+        for (int vt = group; ok && vt < p.vtiles; vt += groups) {
+            for (int i = 0; ok && i < NSt; ++i, ++c) {
+                const int s = c % kQ4WStages;
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&wfull[s], (c / kQ4WStages) & 1, abort_flag, 256))) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* st = wring + s * kQ4WStage;
+                const uint4 sc8 = *reinterpret_cast<const uint4*>(st + 32768 + r * 16);
+                const uint4 bi8 = *reinterpret_cast<const uint4*>(st + 34816 + r * 16);
+                for (int kk = 0; kk < kQ4KBPerStage; ++kk, ++g) {
+                    if ((g & 1) != par) continue;
+                    const int as = g % NA;
+                    if (g >= NA &&
+                        !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&aempty[as], ((g / NA) - 1) & 1, abort_flag, 256))) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t sw = u4_word(sc8, kk >> 1), bw = u4_word(bi8, kk >> 1);
+                    const float sf = (kk & 1) ? bf16_hi(sw) : bf16_lo(sw);
+                    const float bf = (kk & 1) ? bf16_hi(bw) : bf16_lo(bw);
+                    const __half2 s2 = __floats2half2_rn(sf, sf), b2 = __floats2half2_rn(bf, bf);
+                    // this row's 32 bytes of codes: 16-byte chunks c0, c0 + 1 of box kk / 4 (128-byte swizzle)
+                    const uint8_t* rowp = st + (kk >> 2) * 16384 + r * 128;
+                    const int c0 = (kk & 3) * 2;
+                    const uint4 lo = *reinterpret_cast<const uint4*>(rowp + ((c0 ^ (r & 7)) << 4));
+                    const uint4 hi = *reinterpret_cast<const uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4));
+                    uint32_t out[32];
+                    q4_word(lo.x, s2, b2, k1024, out + 0);
+                    q4_word(lo.y, s2, b2, k1024, out + 4);
+                    q4_word(lo.z, s2, b2, k1024, out + 8);
+                    q4_word(lo.w, s2, b2, k1024, out + 12);
+                    q4_word(hi.x, s2, b2, k1024, out + 16);
+                    q4_word(hi.y, s2, b2, k1024, out + 20);
+                    q4_word(hi.z, s2, b2, k1024, out + 24);
+                    q4_word(hi.w, s2, b2, k1024, out + 28);
+                    tc::tmem_st32(tmem + lane_base + a_col + (uint32_t)as * 32, out);
+                    tc::tmem_wait_st();
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&afull[as]);
+                }
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&wempty[s]);
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ argmax epilogue
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        int it = 0;
+        for (int vt = group; vt < p.vtiles; vt += groups, ++it) {
+            const int buf = it & 1;
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, 1024))) break;
+            tc::tc_fence_after();
+            lm_epilogue_tile(tmem + lane_base + buf * p.DC, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
@@ -301,6 +478,19 @@ __global__ void hidden_to_f16_kernel(const uint16_t* __restrict__ in, uint16_t* 
         const uint32_t w = reinterpret_cast<const uint32_t*>(in)[i];
         __half2 h = __floats2half2_rn(bf16_lo(w), bf16_hi(w));
         reinterpret_cast<uint32_t*>(out)[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+}
+
+// bf16 hidden rows -> fp16 copy with every 8 features in the 4-bit converter's order (0,4,1,5,2,6,3,7).
+__global__ void hidden_to_f16_q4order_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, size_t n8) {
+    for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
+        const uint4 w = in[i];
+        const __half2 a = __floats2half2_rn(bf16_lo(w.x), bf16_lo(w.z));  // features 0, 4
+        const __half2 b = __floats2half2_rn(bf16_hi(w.x), bf16_hi(w.z));  // 1, 5
+        const __half2 c = __floats2half2_rn(bf16_lo(w.y), bf16_lo(w.w));  // 2, 6
+        const __half2 d = __floats2half2_rn(bf16_hi(w.y), bf16_hi(w.w));  // 3, 7
+        out[i] = make_uint4(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&b),
+                            *reinterpret_cast<const uint32_t*>(&c), *reinterpret_cast<const uint32_t*>(&d));
     }
 }
 
@@ -335,20 +525,67 @@ static bool map2d(CUtensorMap* m, const void* base, CUtensorMapDataType dt, uint
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// Bytes of workspace the tensor-core path needs beyond the per-row bests
+// Bytes of workspace the tensor-core paths need beyond the per-row bests
 // (the fp16 copy of hidden when the MMA runs in fp16).
 size_t lm_tc_extra_bytes(int rows, int H, int w_dtype) {
     return w_dtype == TSV_BF16 ? 0 : (((size_t)rows * H * 2 + 255) & ~(size_t)255);
 }
 
+// Shape conditions of the tensor-core paths.  The 4-bit path reads scales and biases 8 groups of a row at a
+// time, so H must be a multiple of 512 and (checked by the caller) both pointers 16-byte aligned.
 bool lm_tc_applies(int rows, int H, int V, int w_dtype) {
-    return rows > 8 && H % 64 == 0 && V >= 1 && (w_dtype == TSV_Q4_G64 || H % 64 == 0);
+    if (rows <= 8 || V < 1) return false;
+    return w_dtype == TSV_Q4_G64 ? H % (kLmKB * kQ4KBPerStage) == 0 : H % kLmKB == 0;
+}
+
+static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const void* W, const void* scales,
+                               const void* biases, unsigned long long* best, void* extra, cudaStream_t stream) {
+    static thread_local LmQ4Params prm;
+    const int nchunks = (rows + kQ4MaxNP - 1) / kQ4MaxNP;
+    int NP = (rows + nchunks - 1) / nchunks;
+    NP = ((NP + 15) / 16) * 16;
+    const int DC = ((NP + 31) / 32) * 32;
+    int NA = (512 - 2 * DC) / 32;
+    NA = (NA > kQ4MaxASlots ? kQ4MaxASlots : NA) & ~1;  // even: a slot is always refilled by the same converter set
+    int HS = (kLmUsable - kQ4HOff) / (NP * 128);
+    HS = HS > kQ4MaxHStages ? kQ4MaxHStages : HS;
+    if (NA < 2 || HS < 2) return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the 4-bit pipeline");
+
+    const size_t n8 = (size_t)rows * H / 8;
+    hidden_to_f16_q4order_kernel<<<sm_count() * 4, 256, 0, stream>>>((const uint4*)hidden, (uint4*)extra, n8);
+    tsv_status st = check_launch("lm_head_argmax(hidden fp16)");
+    if (st != TSV_OK) return st;
+
+    bool ok = map2d(&prm.wmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)H / 2, (uint64_t)V, (uint64_t)H / 2, 128,
+                    kLmM, true);
+    ok = ok && map2d(&prm.smap, scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)H / 64, (uint64_t)V,
+                     (uint64_t)H / 64 * 2, kQ4KBPerStage, kLmM, false);
+    ok = ok && map2d(&prm.bmap, biases, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)H / 64, (uint64_t)V,
+                     (uint64_t)H / 64 * 2, kQ4KBPerStage, kLmM, false);
+    ok = ok && map2d(&prm.hmap, extra, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)H, (uint64_t)rows, (uint64_t)H * 2,
+                     64, (uint32_t)NP, true);
+    if (!ok) return fail(TSV_ECUDA, "lm_head_argmax: tensor map encoding failed");
+    prm.best = best;
+    prm.rows = rows;
+    prm.H = H;
+    prm.V = V;
+    prm.NP = NP;
+    prm.DC = DC;
+    prm.NA = NA;
+    prm.HS = HS;
+    prm.nchunks = nchunks;
+    prm.vtiles = (V + kLmM - 1) / kLmM;
+    const int sms = sm_count();
+    const int groups = sms / nchunks > 0 ? sms / nchunks : 1;
+    cudaFuncSetAttribute(lm_q4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+    lm_q4_kernel<<<groups * nchunks, kQ4Threads, kLmSmem, stream>>>(prm);
+    return check_launch("lm_head_argmax(tcgen05, 4-bit)");
 }
 
 tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype, const void* W, const void* scales,
                         const void* biases, unsigned long long* best, void* extra, cudaStream_t stream) {
+    if (w_dtype == TSV_Q4_G64) return launch_lm_q4(hidden, rows, H, V, W, scales, biases, best, extra, stream);
     static thread_local LmTcParams prm;
-    const bool q4 = w_dtype == TSV_Q4_G64;
     const int nchunks = (rows + 255) / 256;
     int NP = (rows + nchunks - 1) / nchunks;
     NP = ((NP + 15) / 16) * 16;
@@ -360,19 +597,11 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
         if (st != TSV_OK) return st;
         hsrc = extra;
     }
-    bool ok;
-    if (q4)
-        ok = map2d(&prm.wmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT8, (uint64_t)H / 2, (uint64_t)V, (uint64_t)H / 2, 32,
-                   kLmM, false);
-    else
-        ok = map2d(&prm.wmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, 64, kLmM,
-                   true);
+    bool ok = map2d(&prm.wmap, W, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)H, (uint64_t)V, (uint64_t)H * 2, 64, kLmM,
+                    true);
     ok = ok && map2d(&prm.hmap, hsrc, CU_TENSOR_MAP_DATA_TYPE_UINT16, (uint64_t)H, (uint64_t)rows, (uint64_t)H * 2, 64,
                      (uint32_t)NP, true);
     if (!ok) return fail(TSV_ECUDA, "lm_head_argmax: tensor map encoding failed");
-    prm.scales = (const uint16_t*)scales;
-    prm.sb_vec = q4 && (H / 64) % 8 == 0 && (((uintptr_t)scales | (uintptr_t)biases) & 15) == 0;
-    prm.biases = (const uint16_t*)biases;
     prm.best = best;
     prm.rows = rows;
     prm.H = H;
@@ -381,22 +610,14 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
     prm.nchunks = nchunks;
     prm.vtiles = (V + kLmM - 1) / kLmM;
     prm.mma_bf16 = w_dtype == TSV_BF16;
-    const int wbytes = q4 ? LmLayout<true>::kW : LmLayout<false>::kW;
-    const int conv_bytes = q4 ? LmLayout<true>::kConv : 0;
-    prm.stage_bytes = wbytes + NP * 128;  // multiples of 1024: every block stays 1024-aligned
-    int stages = (kLmUsable - conv_bytes) / prm.stage_bytes;
+    prm.stage_bytes = 16384 + NP * 128;  // multiples of 1024: every block stays 1024-aligned
+    const int stages = kLmUsable / prm.stage_bytes;
     prm.stages = stages > kLmMaxStages ? kLmMaxStages : stages;
     if (prm.stages < 2) return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the pipeline");
     const int sms = sm_count();
     const int groups = sms / nchunks > 0 ? sms / nchunks : 1;
-    const int grid = groups * nchunks;
-    if (q4) {
-        cudaFuncSetAttribute(lm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
-        lm_tc_kernel<true><<<grid, LmLayout<true>::kThreads, kLmSmem, stream>>>(prm);
-    } else {
-        cudaFuncSetAttribute(lm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
-        lm_tc_kernel<false><<<grid, LmLayout<false>::kThreads, kLmSmem, stream>>>(prm);
-    }
+    cudaFuncSetAttribute(lm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+    lm_tc_kernel<<<groups * nchunks, kLmThreads16, kLmSmem, stream>>>(prm);
     return check_launch("lm_head_argmax(tcgen05)");
 }
 

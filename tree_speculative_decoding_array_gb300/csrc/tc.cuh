@@ -52,16 +52,24 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 
 // Waits for the phase with the given parity to complete, polling with the non-suspending test_wait (a warp
 // parked in a suspending try_wait was seen to resume microseconds after the phase completed, which puts that
-// latency on every hand-off of a pipeline) and backing off with short sleeps after the first polls.  Gives up
-// (returns false and raises *abort) after kWaitNs nanoseconds, or as soon as another thread of the CTA raised
-// *abort; no wait can hang the kernel.
+// latency on every hand-off of a pipeline).  After the first polls it sleeps between polls, doubling the sleep
+// up to max_sleep_ns: every poll is a shared-memory operation, and many warps polling at a high rate delay the
+// shared-memory and tensor-core instructions of the thread on the critical path.  Waiters that are far ahead
+// of the pipeline pass a long maximum, waiters on the critical path a short one.  Gives up (returns false and
+// raises *abort) after kWaitNs nanoseconds, or as soon as another thread of the CTA raised *abort; no wait can
+// hang the kernel.
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s: far above any legitimate wait
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort) {
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
+                                          uint32_t max_sleep_ns = 32) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
+    uint32_t sleep_ns = 32;
     for (uint32_t i = 1;; ++i) {
         if (mbar_test(bar, parity)) return true;
-        if (i > 16) __nanosleep(32);
+        if (i > 16) {
+            __nanosleep(sleep_ns);
+            if (sleep_ns < max_sleep_ns) sleep_ns <<= 1;
+        }
         if ((i & 63) == 0) {
             if (*abort) return false;
             if (globaltimer() - t0 > kWaitNs) {
