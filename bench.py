@@ -134,6 +134,9 @@ def run_ours(args, rank, world, local_rank):
     cfg = configs.CONFIGS[args.config]
     if args.layers:
         cfg = configs.scaled(cfg, n_layers=args.layers)
+    if args.sliding:
+        w, e = (int(x) for x in args.sliding.split(":"))
+        cfg = configs.with_sliding_layers(cfg, w, e)
     round_id = args.round if args.round is not None else ({1: 2}.get(args.config, 0))
     wl = Workload(cfg, device=dev, round_id=round_id, attn_path=args.attn_path)
     vr = wl.vr
@@ -322,6 +325,9 @@ def main():
     ap.add_argument("--round", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--attn-path", type=int, default=0, help="0 auto, 1 CUDA-core kernel, 2 tcgen05 kernel")
+    ap.add_argument("--sliding", default=None,
+                    help="W:E = a hybrid model where of every E layers the last is full attention and the others "
+                         "slide over W positions")
     ap.add_argument("--layers", type=int, default=None,
                     help="attention layers (default: the workload's); fewer only for small profiler captures")
     args = ap.parse_args()
@@ -336,6 +342,9 @@ def main():
     cfg = configs.CONFIGS[args.config]
     if args.layers:
         cfg = configs.scaled(cfg, n_layers=args.layers)
+    if args.sliding:
+        w, e = (int(x) for x in args.sliding.split(":"))
+        cfg = configs.with_sliding_layers(cfg, w, e)
     config = {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "layers": cfg.n_layers, "HQ": cfg.HQ, "HKV": cfg.HKV,
               "D": cfg.D, "S": cfg.S, "H": cfg.H, "V": cfg.V, "kv": configs.DTYPE_NAMES[cfg.kv_dtype],
               "lm_head": configs.DTYPE_NAMES[cfg.w_dtype], "topology": cfg.topology,
@@ -396,7 +405,9 @@ def main():
         "clocks": r["clocks"],
         "e2e": r["e2e"],
     }
-    if not args.no_cpu_baseline:
+    if args.sliding:
+        config["sliding"] = {"window": int(args.sliding.split(":")[0]), "every": int(args.sliding.split(":")[1])}
+    if not args.no_cpu_baseline and not args.sliding:
         try:
             o = run_oracle(args.config, r["round_id"])
             line["cpu_baseline"] = {"value": o["nodes_per_s"], "unit": "nodes/s", "cores": 1, "kind": "oracle",

@@ -108,6 +108,23 @@ tsv_status tsv_tree_mask(const int32_t* parents, int32_t B, int32_t T, uint64_t*
                          float* dense_mask, int32_t mask_offset, int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * tsv_sliding_band_mask - the mask a sliding-window layer attends with, in place.
+ *   [1212], the commit on caller masks and the sliding-window band: a
+ *   sliding-window layer takes the intersection of the caller's mask (here the
+ *   dense tree mask of tsv_tree_mask) with its band, by element-wise minimum
+ *   of the additive masks, and only where the two can disagree.  Query row q
+ *   sits at position mask_offset + q; its band keeps columns c with
+ *   mask_offset + q - window < c <= mask_offset + q, all else becomes
+ *   min(mask, -1e9).  Every row keeps its own position.
+ *   dense_mask float [B, T, mask_offset + T], in/out.  window >= 1; when
+ *   mask_offset + T <= window the mask is left untouched (nothing is launched).
+ *   The attention call applies the same band itself from tsv_attn_desc.window;
+ *   this call is provided for parity checks.
+ */
+tsv_status tsv_sliding_band_mask(float* dense_mask, int32_t B, int32_t T, int32_t mask_offset, int32_t window,
+                                 cudaStream_t stream);
+
+/*
  * Tree-masked GQA attention of the verify block, for n_layers layers at once.
  *   [1204] "What this needs" item 1 and "Increment 3"; [1212] history-mask and
  *   verify_forward_with_mask commits; [728] "Earlier shader evidence" (split-KV
@@ -117,6 +134,11 @@ tsv_status tsv_tree_mask(const int32_t* parents, int32_t B, int32_t T, uint64_t*
  *   over c in [0, S_b) and c = S_b + j for every j set in anc[b][i], where
  *   S_b = kv_len[b] - T (the block was appended in topological order at
  *   [S_b, S_b + T)).  G = HQ / HKV.  Int8: K = code * k_scale[c], V = code * v_scale[c].
+ *   Sliding-window layers ([1212], the commit on caller masks and the
+ *   sliding-window band): with window[l] > 0, node i (at cache position
+ *   S_b + i) keeps only those of the keys above whose position c satisfies
+ *   c > S_b + i - window[l]: the intersection of the tree mask with the
+ *   layer's band.  Every node keeps itself.  window[l] == 0 is a full-attention layer.
  *   Accumulation is fp32; O is rounded to bf16 once.
  */
 typedef struct {
@@ -135,6 +157,7 @@ typedef struct {
     void* o[TSV_MAX_LAYERS];             /* per layer: bf16 [B, T, HQ, D], out */
     const int32_t* kv_len;               /* int32 [B]: S_b + T */
     const uint64_t* anc;                 /* uint64 [B, T] from tsv_tree_mask */
+    int32_t window[TSV_MAX_LAYERS];      /* per layer: sliding window in positions, 0 = full attention */
 } tsv_attn_desc;
 
 /* Kernel choice.  AUTO takes the tensor-core (tcgen05) kernel where it applies

@@ -44,15 +44,34 @@ def attend_dense_mask(q, K, V, mask_row) -> np.ndarray:
     return (p / p.sum()) @ V
 
 
-def tree_verify_attention(q, K, V, parents, S: int) -> np.ndarray:
-    """All rows of one (sequence, layer).  q [T, HQ, D]; K, V [HKV, S + T, D] -> [T, HQ, D]."""
+def attend_cols(q, K, V, cols) -> np.ndarray:
+    """One query row over an explicit list of cache positions."""
+    k = K[cols]
+    v = V[cols]
+    s = (k @ np.asarray(q, dtype=np.float64)) / math.sqrt(K.shape[1])
+    s = s - s.max()
+    p = np.exp(s)
+    return (p / p.sum()) @ v
+
+
+def tree_verify_attention(q, K, V, parents, S: int, window: int = 0) -> np.ndarray:
+    """All rows of one (sequence, layer).  q [T, HQ, D]; K, V [HKV, S + T, D] -> [T, HQ, D].
+
+    window > 0: a sliding-window layer; node i (at position S + i) sees only the keys of its tree mask that lie
+    inside its band, positions > S + i - window (PR #1212, caller masks and the sliding-window band).
+    """
     T, HQ, D = q.shape
     HKV = K.shape[0]
     G = HQ // HKV
     out = np.zeros((T, HQ, D), dtype=np.float64)
     for i in range(T):
-        vis = _tree.ancestors(parents, i)
+        if window == 0:
+            vis = _tree.ancestors(parents, i)
+        cols = _tree.visible_keys(parents, i, S, window)
         for h in range(HQ):
             kv = h // G
-            out[i, h] = attend_row(q[i, h], K[kv], V[kv], S, vis)
+            if window == 0:
+                out[i, h] = attend_row(q[i, h], K[kv], V[kv], S, vis)
+            else:
+                out[i, h] = attend_cols(q[i, h], K[kv], V[kv], cols)
     return out

@@ -13,6 +13,10 @@ Definitions followed:
   q + offset, the first ``offset`` columns (the cached history) are attended in
   full by every node, and the last n follow the tree.  PR #1212's verify
   commit: blocked entries hold -1e9, not -inf.
+* Sliding-window layers - PR #1212, the commit on caller masks and the
+  sliding-window band: such a layer attends the intersection of the caller's
+  (tree) mask and its band; the band of query q (at position offset + q) keeps
+  the window positions ending at the query, so every row keeps itself.
 * Walk - issue #1204, "What this needs" item 2, and PR #1212's first commit:
   descend the branch the target agreed with; the accepted set is a path, never
   a subtree.  Reading for two siblings that both match: the one with the lower
@@ -79,6 +83,45 @@ def history_mask(parents, offset: int) -> np.ndarray:
     m = np.zeros((n, offset + n), dtype=np.float64)
     m[:, offset:] = tree_mask(parents)
     return m
+
+
+def sliding_band(n: int, offset: int, window: int) -> np.ndarray:
+    """The [n, offset + n] additive sliding-window band of a block of n queries after ``offset`` cached positions.
+
+    Query row q sits at position offset + q (PR #1212, history-mask commit).  Column c is inside the band iff
+    offset + q - window < c <= offset + q: the query and the window - 1 positions before it.  window >= 1.
+    """
+    m = np.full((n, offset + n), BLOCKED, dtype=np.float64)
+    for q in range(n):
+        pos = offset + q
+        for c in range(max(0, pos - window + 1), pos + 1):
+            m[q, c] = 0.0
+    return m
+
+
+def sliding_mask_from_caller(mask, offset: int, window: int) -> np.ndarray:
+    """What a sliding-window layer attends with: the caller's mask intersected with the band.
+
+    PR #1212, the commit on caller masks and the sliding-window band: additive masks intersect by their
+    element-wise minimum, and only where the two can disagree - a block of n queries after ``offset`` cached
+    positions is left untouched while offset + n <= window (the band then blocks nothing the causal order
+    allows).  window == 0 means a full-attention layer (no band).
+    """
+    mask = np.asarray(mask, dtype=np.float64)
+    n = mask.shape[0]
+    if window == 0 or offset + n <= window:
+        return mask.copy()
+    return np.minimum(mask, sliding_band(n, offset, window))
+
+
+def visible_keys(parents, i: int, offset: int, window: int = 0) -> list[int]:
+    """Cache positions node i attends to: every history position and its ancestors' block positions, and with
+    a window > 0 only those inside the band (position > offset + i - window)."""
+    cols = list(range(offset)) + [offset + j for j in sorted(ancestors(parents, i))]
+    if window > 0:
+        lo = offset + i - window + 1
+        cols = [c for c in cols if c >= lo]
+    return cols
 
 
 def children(parents, u: int) -> list[int]:

@@ -38,6 +38,7 @@ class Config:
     accept: str = ""       # accept-length rule
     plant_c: float = 0.25  # planting strength of the target direction in hidden
     min_gap: float = 1e-2  # required top-1/top-2 logit gap (fp64)
+    window: tuple = ()     # per-layer sliding windows (0 = full attention); empty = every layer full
     notes: str = ""
 
     @property
@@ -58,15 +59,26 @@ class Config:
     def kv_elem_bytes(self) -> int:
         return 1 if self.kv_dtype == I8 else 2
 
+    def layer_window(self, layer: int) -> int:
+        return int(self.window[layer]) if self.window else 0
+
+    def kv_positions(self) -> int:
+        """Cache positions read per (sequence, KV head), summed over layers: all S+T for a full layer; for a
+        sliding-window layer only those inside some node's band, the last window + T - 1."""
+        tot = 0
+        for l in range(self.n_layers):
+            w = self.layer_window(l)
+            tot += self.NKV if w == 0 else min(self.NKV, w + self.T - 1)
+        return tot
+
     def kv_bytes(self) -> int:
-        """K and V of every layer, sequence and KV head over all S+T positions."""
-        per = self.n_layers * self.B * self.HKV * self.NKV * self.D * self.kv_elem_bytes()
-        return 2 * per
+        """K and V of every layer, sequence and KV head over the positions the layer attends."""
+        return 2 * self.B * self.HKV * self.kv_positions() * self.D * self.kv_elem_bytes()
 
     def kv_scale_bytes(self) -> int:
         if self.kv_dtype != I8:
             return 0
-        return 2 * self.n_layers * self.B * self.HKV * self.NKV * 2
+        return 2 * self.B * self.HKV * self.kv_positions() * 2
 
     def lm_bytes(self) -> int:
         if self.w_dtype == Q4:
@@ -120,4 +132,13 @@ def scaled(cfg: Config, **kw) -> Config:
     """A copy of ``cfg`` with some fields replaced (reduced-size parity cases)."""
     d = dict(cfg.__dict__)
     d.update(kw)
+    if d.get("window") and len(d["window"]) != d["n_layers"]:
+        d["window"] = tuple(d["window"][l % len(d["window"])] for l in range(d["n_layers"]))
     return Config(**d)
+
+
+def with_sliding_layers(cfg: Config, window: int, every: int) -> Config:
+    """A hybrid model: of every ``every`` layers the last is full attention and the others slide over
+    ``window`` positions (the sliding/full interleave of the hybrid targets the pages verify against)."""
+    pattern = tuple(0 if (l % every) == every - 1 else window for l in range(cfg.n_layers))
+    return scaled(cfg, name=f"{cfg.name}+sliding{window}x{every - 1}", window=pattern)

@@ -46,7 +46,8 @@ class Workload:
             W=self.head["W"], kv_len=self.kv_len,
             k_scale=[c["ks"] for c in self.caches] if i8 else None,
             v_scale=[c["vs"] for c in self.caches] if i8 else None,
-            w_scales=self.head["scales"], w_biases=self.head["biases"], splits=splits, attn_path=attn_path)
+            w_scales=self.head["scales"], w_biases=self.head["biases"], splits=splits, attn_path=attn_path,
+            window=tuple(cfg.layer_window(l) for l in range(L)) if cfg.window else None)
         self._tail = None
 
     def set_round(self, round_id: int):

@@ -54,11 +54,13 @@ def oracle_attention_rows(cfg, layer, b, kvh, nodes, parents_b):
     G = cfg.G
     heads = [kvh * G + g for g in range(G)]
     res = {}
+    w = cfg.layer_window(layer)
     for i in nodes:
         q = osd.bf16(tensors.q_rows(cfg, layer, b, i, heads))
         vis = ot.ancestors(parents_b, i)
+        cols = ot.visible_keys(parents_b, i, cfg.S, w)
         for gi, h in enumerate(heads):
-            res[(i, h)] = oa.attend_row(q[gi], K, V, cfg.S, vis)
+            res[(i, h)] = oa.attend_row(q[gi], K, V, cfg.S, vis) if w == 0 else oa.attend_cols(q[gi], K, V, cols)
     return res
 
 

@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported():
 
 def test_version_and_error_string():
     lib = tsv.load()
-    assert lib.tsv_version() == 100
+    assert lib.tsv_version() == 101
     assert lib.tsv_last_error() == b""
 
 
@@ -75,6 +75,12 @@ def test_host_validation_refuses_without_launching():
     assert st == _abi.EUNSUPPORTED and b"96" in lib.tsv_last_error()
     d.D, d.kv_dtype = 64, 3  # a weight format for a cache
     assert lib.tsv_tree_verify_attention(C.byref(d), None, 0, None, None) == _abi.EUNSUPPORTED
+    d.kv_dtype, d.max_kv_len, d.s_cap, d.window[0] = 0, 8, 8, -1  # a negative sliding window
+    st = lib.tsv_tree_verify_attention(C.byref(d), None, 0, None, None)
+    assert st == _abi.EINVAL and b"window" in lib.tsv_last_error()
+    assert lib.tsv_sliding_band_mask(None, 1, 4, 10, 0, None) == _abi.EINVAL  # window must be >= 1
+    assert lib.tsv_sliding_band_mask(None, 1, 4, 10, 14, None) == _abi.OK  # below the window: untouched
+    assert lib.tsv_sliding_band_mask(None, 1, 4, 10, 13, None) == _abi.EINVAL  # past it: needs the mask
     k = _abi.KvDesc()
     k.n_layers, k.B, k.HKV, k.D, k.s_cap, k.kv_dtype = 1, 1, 1, 64, 10, 3
     st = lib.tsv_kv_gather_positions(C.byref(k), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), 4, None, None)

@@ -140,3 +140,16 @@ def test_eagle64x32_int8_q4_long_context(gpu_lib):
     assert rep["ok"], rep
     del wl, out
     _free()
+
+
+@pytest.mark.parametrize("idx,window,every", [(3, 1024, 6), (2, 2048, 4)])
+def test_sliding_hybrid_full_size(gpu_lib, idx, window, every):
+    """Hybrid sliding/full models at full size: sliding layers see the tree mask intersected with their band."""
+    cfg = configs.with_sliding_layers(configs.CONFIGS[idx], window, every)
+    assert cfg.layer_window(0) == window and cfg.layer_window(every - 1) == 0
+    wl = Workload(cfg)
+    out = _run(wl)
+    rep = check_round(wl, out, layers=[0, every - 1, every], attn_rows=3, kv_heads=[1], seqs=[0], lm="planted")
+    assert rep["ok"], rep
+    del wl, out
+    _free()

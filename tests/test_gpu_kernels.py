@@ -101,7 +101,8 @@ def make_attn_case(rng, *, B, T, HQ, HKV, D, S_list, kv_dtype, layers=1, cap_ext
     return s_cap, data, trees
 
 
-def run_attn_case(gpu_lib, rng, *, B, T, HQ, HKV, D, S_list, kv_dtype, splits, layers=1, path=0, cap_extra=3):
+def run_attn_case(gpu_lib, rng, *, B, T, HQ, HKV, D, S_list, kv_dtype, splits, layers=1, path=0, cap_extra=3,
+                  window=None):
     s_cap, data, trees = make_attn_case(rng, B=B, T=T, HQ=HQ, HKV=HKV, D=D, S_list=S_list, kv_dtype=kv_dtype,
                                         layers=layers, cap_extra=cap_extra)
     qs, ks_, vs_, kss, vss, os_ = [], [], [], [], [], []
@@ -123,7 +124,7 @@ def run_attn_case(gpu_lib, rng, *, B, T, HQ, HKV, D, S_list, kv_dtype, splits, l
     kv_len = i32([S + T for S in S_list])
     desc = gpu_lib.attn_desc(qs, ks_, vs_, os_, kv_len, anc, T=T, HQ=HQ, HKV=HKV, D=D, kv_dtype=kv_dtype,
                              max_kv_len=max(S_list) + T, k_scale=kss or None, v_scale=vss or None, splits=splits,
-                             path=path)
+                             path=path, window=window)
     ws = torch.empty(max(gpu_lib.attention_workspace_size(desc), 16), dtype=torch.uint8, device=DEV)
     st = status()
     gpu_lib.tree_verify_attention(desc, ws, dev_status=st)
@@ -144,11 +145,16 @@ def run_attn_case(gpu_lib, rng, *, B, T, HQ, HKV, D, S_list, kv_dtype, splits, l
                 else:
                     K = ks_[l][b, kvh, :S + T].double().cpu().numpy()
                     V = vs_[l][b, kvh, :S + T].double().cpu().numpy()
+                w = 0 if window is None else window[l]
                 for i in range(T):
                     vis = ot.ancestors(trees[b], i)
+                    cols = ot.visible_keys(trees[b], i, S, w)
                     for g in range(G):
                         h = kvh * G + g
-                        ref[i, h] = oa.attend_row(qd[b, i, h], K, V, S, vis)
+                        if w == 0:
+                            ref[i, h] = oa.attend_row(qd[b, i, h], K, V, S, vis)
+                        else:
+                            ref[i, h] = oa.attend_cols(qd[b, i, h], K, V, cols)
             a, r = attn_stats(o[b].reshape(-1, D), ref.reshape(-1, D))
             worst = (max(worst[0], a), max(worst[1], r))
     assert worst[0] <= ATT_MAX_ABS and worst[1] <= ATT_REL_L2, worst
@@ -189,6 +195,37 @@ def test_attention_tcgen05_refuses_what_it_cannot_do(gpu_lib):
 def test_attention_head_dims_and_layers(gpu_lib, D):
     rng = np.random.default_rng(D)
     run_attn_case(gpu_lib, rng, B=1, T=5, HQ=8, HKV=2, D=D, S_list=[77], kv_dtype=0, splits=0, layers=3)
+
+
+@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("kv_dtype", [0, 1, 2])
+@pytest.mark.parametrize("T,S_list,splits,window", [(7, [300, 129], 0, [64]), (16, [1000, 33], 3, [5]),
+                                                    (33, [500, 200], 0, [1, 100, 0]), (64, [1337, 64], 2, [200]),
+                                                    (3, [4096, 70], 0, [1024, 0])])
+def test_attention_sliding_window(gpu_lib, path, kv_dtype, T, S_list, splits, window):
+    """Sliding-window layers: the tree mask intersected with each layer's band, mixed with full layers."""
+    rng = np.random.default_rng(T * 13 + kv_dtype + len(window))
+    run_attn_case(gpu_lib, rng, B=2, T=T, HQ=24, HKV=4, D=256, S_list=S_list, kv_dtype=kv_dtype, splits=splits,
+                  path=path, cap_extra=70, layers=len(window), window=window)
+
+
+@pytest.mark.parametrize("window", [1, 3, 8, 40, 100])
+def test_sliding_band_mask_exact(gpu_lib, window):
+    rng = np.random.default_rng(window)
+    B, T, offset = 3, 9, 37
+    par = np.array([random_tree(rng, T, s) for s in ("random", "chain", "star")], dtype=np.int32)
+    anc = torch.zeros(B, T, dtype=torch.int64, device=DEV)
+    depth = torch.zeros(B, T, dtype=torch.int32, device=DEV)
+    dense = torch.zeros(B, T, offset + T, dtype=torch.float32, device=DEV)
+    gpu_lib.tree_mask(i32(par), anc, depth, dense_mask=dense, mask_offset=offset)
+    gpu_lib.sliding_band_mask(dense, offset, window)
+    torch.cuda.synchronize()
+    dm = dense.cpu().numpy()
+    for b in range(B):
+        want = ot.sliding_mask_from_caller(ot.history_mask(par[b].tolist(), offset), offset, window)
+        assert np.array_equal(dm[b], want.astype(np.float32)), b
+    with pytest.raises(gpu_lib.TsvError, match="TSV_EINVAL"):
+        gpu_lib.sliding_band_mask(dense, offset, 0)
 
 
 def test_attention_splits_agree(gpu_lib):

@@ -196,3 +196,63 @@ def test_tail_form_equals_absolute_form_and_scales_move():
     # rows past the new length keep their bytes (in-place tail rewrite)
     assert np.array_equal(bc[n:], codes[n:])
     assert not og.is_identity(path)
+
+
+# ----------------------------------------------------------------------------- sliding-window layers
+@pytest.mark.parametrize("S,T,window", [(0, 3, 2), (10, 4, 3), (30, 5, 8), (40, 6, 1), (12, 3, 15)])
+def test_sliding_linear_tree_is_banded_causal_sdpa(S, T, window):
+    # A linear tree on a sliding-window layer is textbook sliding-window causal attention: query at position
+    # S + q sees the `window` positions ending at itself (band built here from numpy's triangle routines).
+    rng = np.random.default_rng(S + 7 * T + 31 * window)
+    D = 16
+    q = rng.standard_normal((T, 1, D))
+    K = rng.standard_normal((1, S + T, D))
+    V = rng.standard_normal((1, S + T, D))
+    par = [-1] + list(range(T - 1))
+    out = oa.tree_verify_attention(q, K, V, par, S, window=window)
+    ones = np.ones((T, S + T), dtype=bool)
+    allowed = np.tril(ones, k=S) & np.triu(ones, k=S - window + 1)
+    ref = torch_sdpa(q[:, 0], K[0], V[0], allowed)
+    assert np.allclose(out[:, 0], ref, rtol=1e-12, atol=1e-12)
+
+
+def test_sliding_window_of_one_returns_own_value_and_wide_window_changes_nothing():
+    rng = np.random.default_rng(8)
+    par = [-1, 0, 0, 1, 2, 2, 5]
+    T, S, D = len(par), 20, 8
+    q = rng.standard_normal((T, 2, D))
+    K = rng.standard_normal((1, S + T, D))
+    V = rng.standard_normal((1, S + T, D))
+    own = oa.tree_verify_attention(q, K, V, par, S, window=1)
+    for i in range(T):
+        assert np.allclose(own[i], V[0, S + i], rtol=0, atol=1e-15)  # only the node itself survives the band
+    full = oa.tree_verify_attention(q, K, V, par, S)
+    assert np.allclose(oa.tree_verify_attention(q, K, V, par, S, window=S + T), full, rtol=1e-13, atol=1e-13)
+
+
+def test_sliding_mask_from_caller_properties():
+    # The properties PR #1212 states for the intersection of a caller mask with the band.
+    par = [-1, 0, 0, 1, 1, 2, 2, 4]
+    T = len(par)
+    for S in (0, 3, 9, 40):
+        caller = ot.history_mask(par, S)
+        for window in (1, 2, 5, 9, 16, 48, 60):
+            got = ot.sliding_mask_from_caller(caller, S, window)
+            if S + T <= window:  # below the window the caller mask comes back untouched
+                assert np.array_equal(got, caller)
+            # intersecting again changes nothing (masks that already carry the band)
+            assert np.array_equal(ot.sliding_mask_from_caller(got, S, window), got)
+            # every row keeps its own position, so no row is all-masked
+            for i in range(T):
+                assert got[i, S + i] == 0.0
+            # an all-attend caller mask (the draft-tree history shape) reduces to the band past the window
+            allatt = np.zeros((T, S + T))
+            band_only = ot.sliding_mask_from_caller(allatt, S, window)
+            if S + T > window:
+                ones = np.ones((T, S + T), dtype=bool)
+                inband = np.tril(ones, k=S) & np.triu(ones, k=S - window + 1)  # the causal sliding band
+                assert np.array_equal(band_only == 0.0, inband)
+            # the dense form and the key lists the attention uses agree
+            for i in range(T):
+                cols = np.flatnonzero(got[i] == 0.0).tolist()
+                assert cols == ot.visible_keys(par, i, S, window)

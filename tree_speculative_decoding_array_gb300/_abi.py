@@ -32,7 +32,7 @@ class AttnDesc(C.Structure):
         ("s_cap", _i64), ("max_kv_len", _i32), ("kv_dtype", _i32), ("splits", _i32), ("path", _i32),
         ("q", _vp * MAX_LAYERS), ("k", _vp * MAX_LAYERS), ("v", _vp * MAX_LAYERS),
         ("k_scale", _vp * MAX_LAYERS), ("v_scale", _vp * MAX_LAYERS), ("o", _vp * MAX_LAYERS),
-        ("kv_len", _vp), ("anc", _vp),
+        ("kv_len", _vp), ("anc", _vp), ("window", _i32 * MAX_LAYERS),
     ]
 
 
@@ -48,6 +48,7 @@ SIGNATURES = {
     "tsv_last_error": (C.c_char_p, []),
     "tsv_version": (C.c_int, []),
     "tsv_tree_mask": (C.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp]),
+    "tsv_sliding_band_mask": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp]),
     "tsv_attention_workspace_size": (_sz, [C.POINTER(AttnDesc)]),
     "tsv_tree_verify_attention": (C.c_int, [C.POINTER(AttnDesc), _vp, _sz, _vp, _vp]),
     "tsv_lm_head_workspace_size": (_sz, [_i32, _i32, _i32, _i32]),

@@ -54,13 +54,26 @@ def tree_mask(parents, anc, depth, dense_mask=None, mask_offset=0, dev_status=No
                             _p(dev_status), _stream(stream)), "tree_mask")
 
 
+def sliding_band_mask(dense_mask, mask_offset, window, stream=None):
+    """In place: intersect a dense [B, T, mask_offset + T] fp32 mask with a sliding-window band."""
+    B, T = dense_mask.shape[0], dense_mask.shape[1]
+    _cuda(dense_mask, "dense_mask", torch.float32, (B, T, mask_offset + T))
+    check(load().tsv_sliding_band_mask(_p(dense_mask), B, T, int(mask_offset), int(window), _stream(stream)),
+          "sliding_band_mask")
+
+
 # ----------------------------------------------------------------------------- a2 attention
 def attn_desc(q, k, v, o, kv_len, anc, *, T, HQ, HKV, D, kv_dtype, max_kv_len, k_scale=None, v_scale=None,
-              splits=0, path=0) -> AttnDesc:
-    """Descriptor over per-layer lists: q/o bf16 [B,T,HQ,D]; k/v [B,HKV,s_cap,D]; scales fp16 [B,HKV,s_cap]."""
+              splits=0, path=0, window=None) -> AttnDesc:
+    """Descriptor over per-layer lists: q/o bf16 [B,T,HQ,D]; k/v [B,HKV,s_cap,D]; scales fp16 [B,HKV,s_cap].
+
+    window: per-layer sliding windows (0 = full attention), or None for all full-attention layers.
+    """
     n = len(q)
     if not (1 <= n <= MAX_LAYERS) or not (len(k) == len(v) == len(o) == n):
         raise ValueError("per-layer lists must have the same length in [1, 64]")
+    if window is not None and len(window) != n:
+        raise ValueError("window needs one entry per layer")
     B = q[0].shape[0]
     s_cap = k[0].shape[2]
     d = AttnDesc()
@@ -80,6 +93,8 @@ def attn_desc(q, k, v, o, kv_len, anc, *, T, HQ, HKV, D, kv_dtype, max_kv_len, k
     _cuda(kv_len, "kv_len", torch.int32, (B,))
     _cuda(anc, "anc", torch.int64, (B, T))
     d.kv_len, d.anc = kv_len.data_ptr(), anc.data_ptr()
+    for l in range(n):
+        d.window[l] = 0 if window is None else int(window[l])
     return d
 
 
@@ -189,6 +204,7 @@ class VerifyRound:
     w_biases: torch.Tensor = None
     splits: int = 0
     attn_path: int = 0
+    window: tuple = None
     outs: dict = field(default_factory=dict)
 
     def __post_init__(self):
@@ -201,7 +217,8 @@ class VerifyRound:
                          o=[torch.empty(B, T, self.HQ, self.D, dtype=torch.bfloat16, device=dev) for _ in range(n)])
         self.adesc = attn_desc(self.q, self.k, self.v, self.outs["o"], self.kv_len, self.outs["anc"], T=T, HQ=self.HQ,
                                HKV=self.HKV, D=self.D, kv_dtype=self.kv_dtype, max_kv_len=self.max_kv_len,
-                               k_scale=self.k_scale, v_scale=self.v_scale, splits=self.splits, path=self.attn_path)
+                               k_scale=self.k_scale, v_scale=self.v_scale, splits=self.splits, path=self.attn_path,
+                               window=self.window)
         self.kdesc = kv_desc(self.k, self.v, HKV=self.HKV, D=self.D, kv_dtype=self.kv_dtype, k_scale=self.k_scale,
                              v_scale=self.v_scale)
         self.attn_ws = torch.empty(max(attention_workspace_size(self.adesc), 256), dtype=torch.uint8, device=dev)

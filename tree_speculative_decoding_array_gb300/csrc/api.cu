@@ -40,4 +40,4 @@ int sm_count() {
 
 extern "C" const char* tsv_last_error(void) { return tsv::g_err; }
 
-extern "C" int tsv_version(void) { return 100; }
+extern "C" int tsv_version(void) { return 101; }

@@ -54,11 +54,33 @@ static AttnGeom attn_geom(const tsv_attn_desc* d) {
             const long long base = (long long)g.units * tc_mtiles(d);
             const long long slots = sm_count();
             const long long tiles = (d->max_kv_len + 63) / 64;
+            bool sliding = false;
+            for (int l = 0; l < d->n_layers; ++l) sliding = sliding || d->window[l] > 0;
             double best = 1e300;
             s = 1;
             for (int c = 1; c <= (cap_s > 1 ? cap_s : 1); ++c) {
-                const long long waves = (base * c + slots - 1) / slots;
-                const double t = (double)waves * (8.0 + (double)((tiles + c - 1) / c)) + (c > 1 ? 2.0 : 0.0);
+                double t;
+                if (!sliding) {
+                    const long long waves = (base * c + slots - 1) / slots;
+                    t = (double)waves * (8.0 + (double)((tiles + c - 1) / c)) + (c > 1 ? 2.0 : 0.0);
+                } else {
+                    // Sliding-window layers only keep the key ranges that meet their band; their other CTAs
+                    // return at once.  Estimate: total work over the SMs, but never below the longest CTA.
+                    const long long chunk = ((d->max_kv_len + c - 1) / c + 63) / 64 * 64;
+                    const long long per_layer = base / d->n_layers;  // (sequence, kv head, m-tile) items
+                    double work = 0.0, longest = 0.0;
+                    for (int l = 0; l < d->n_layers; ++l) {
+                        const long long w = d->window[l];
+                        const long long len = w > 0 ? (w + d->T - 1 < d->max_kv_len ? w + d->T - 1 : d->max_kv_len)
+                                                    : d->max_kv_len;
+                        const long long first = (d->max_kv_len - len) / chunk, last = (d->max_kv_len - 1) / chunk;
+                        const long long active = last - first + 1;
+                        const double tl = 8.0 + (double)(((len < chunk ? len : chunk) + 63) / 64 + (w > 0 ? 1 : 0));
+                        work += (double)per_layer * ((double)active * tl + 0.5 * (double)(c - active));
+                        longest = longest > tl ? longest : tl;
+                    }
+                    t = (work / (double)slots > longest ? work / (double)slots : longest) + (c > 1 ? 2.0 : 0.0);
+                }
                 if (t < best * 0.98) {
                     best = t;
                     s = c;
@@ -124,6 +146,7 @@ __global__ void __launch_bounds__(kAttThreads) attn_simt_kernel(const __grid_con
     float* v_s = k_s + kBK * KS;     // [kBK][D]
     float* p_s = v_s + kBK * D;      // [kRB][kBK]
     __shared__ uint64_t anc_s[kRB];
+    __shared__ int lo_s[kRB];  // sliding-window layers: smallest key position each row keeps
     __shared__ float m_s[kRB], l_s[kRB], alpha_s[kRB];
 
     const int unit = blockIdx.z;
@@ -140,8 +163,13 @@ __global__ void __launch_bounds__(kAttThreads) attn_simt_kernel(const __grid_con
         return;
     }
     const int S = kvl - T;
-    const int k_begin = s * chunk;
+    const int win = d.window[layer];
+    int k_begin = s * chunk;
     const int k_end = min(kvl, k_begin + chunk);
+    // Sliding-window layer: node i keeps keys c >= S + i - win + 1; key tiles below the first row's bound are
+    // skipped (whole tiles from the range start).
+    const int lo_first = win > 0 ? S + row0 / G - win + 1 : INT_MIN;
+    if (lo_first > k_begin) k_begin += ((lo_first - k_begin) / kBK) * kBK;
     const float qscale = 1.4426950408889634f * rsqrtf((float)D);  // log2(e) / sqrt(D)
 
     // Q rows (fp32, pre-scaled into the log2 domain) and their ancestor words
@@ -158,6 +186,7 @@ __global__ void __launch_bounds__(kAttThreads) attn_simt_kernel(const __grid_con
     if (threadIdx.x < kRB) {
         const int gr = row0 + threadIdx.x;
         anc_s[threadIdx.x] = gr < rows_unit ? d.anc[(size_t)b * T + gr / G] : 0ull;
+        lo_s[threadIdx.x] = (win > 0 && gr < rows_unit) ? S + gr / G - win + 1 : INT_MIN;
         m_s[threadIdx.x] = -INFINITY;
         l_s[threadIdx.x] = 0.f;
     }
@@ -212,7 +241,7 @@ __global__ void __launch_bounds__(kAttThreads) attn_simt_kernel(const __grid_con
                 s1 = fmaf(kk.x, bb.x, fmaf(kk.y, bb.y, fmaf(kk.z, bb.z, fmaf(kk.w, bb.w, s1))));
             }
             const int c = kt + j;
-            bool v0 = j < nk, v1 = j < nk;
+            bool v0 = j < nk && c >= lo_s[r0], v1 = j < nk && c >= lo_s[r0 + 8];
             if (c >= S) {
                 const int node = c - S;
                 v0 = v0 && ((anc_s[r0] >> node) & 1ull);
@@ -367,6 +396,8 @@ static tsv_status check_desc(const tsv_attn_desc* d) {
         return fail(TSV_EINVAL, "tree_verify_attention: max_kv_len=%d must be in [T, s_cap=%lld]", d->max_kv_len,
                     (long long)d->s_cap);
     if (d->splits < 0) return fail(TSV_EINVAL, "tree_verify_attention: splits=%d < 0", d->splits);
+    for (int l = 0; l < d->n_layers; ++l)
+        if (d->window[l] < 0) return fail(TSV_EINVAL, "tree_verify_attention: layer %d window=%d < 0", l, d->window[l]);
     if (d->path < TSV_ATTN_AUTO || d->path > TSV_ATTN_TCGEN05)
         return fail(TSV_EINVAL, "tree_verify_attention: path=%d", d->path);
     if (d->path == TSV_ATTN_TCGEN05 && !tc_supported(d))

@@ -59,6 +59,7 @@ struct TcParams {
     float* ws_o;
     float* ws_ml;
     int32_t* status;
+    int window[TSV_MAX_LAYERS];  // per layer sliding window, 0 = full attention
     int64_t s_cap;
     int B, T, HQ, HKV, G, R, mtiles, splits, chunk, max_kv_len, mma_bf16;
 };
@@ -181,10 +182,17 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
         return;
     }
     const int S = kvl - T;
-    const int k_begin = split * p.chunk;
-    const int k_end = min(kvl, k_begin + p.chunk);
-    const int ntiles = k_end > k_begin ? (k_end - k_begin + kTcBK - 1) / kTcBK : 0;
     const int row0 = mt * kTcRows;
+    const int k_end = min(kvl, split * p.chunk + p.chunk);
+    // Sliding-window layer: node i keeps keys c >= S + i - window + 1.  lo_first / lo_last are that bound for
+    // the first and last real row of this tile; key tiles below lo_first are skipped (64-key steps from the
+    // range start), tiles at or above lo_last need no band test.
+    const int win = p.window[layer];
+    const int lo_first = win > 0 ? S + row0 / p.G - win + 1 : INT_MIN;
+    const int lo_last = win > 0 ? S + (min(p.R, row0 + kTcRows) - 1) / p.G - win + 1 : INT_MIN;
+    int k_begin = split * p.chunk;
+    if (lo_first > k_begin) k_begin += ((lo_first - k_begin) / kTcBK) * kTcBK;
+    const int ntiles = k_end > k_begin ? (k_end - k_begin + kTcBK - 1) / kTcBK : 0;
 
     // A CTA of this launch already timed out: do not start (keeps a broken launch short).
     if (p.status != nullptr && *reinterpret_cast<volatile int32_t*>(p.status) == TSV_DEV_TIMEOUT) return;
@@ -382,6 +390,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
         const int node = row_ok ? gr / p.G : 0;
         const int head = kvh * p.G + (row_ok ? gr % p.G : 0);
         const uint64_t anc = row_ok ? p.anc[(size_t)b * T + node] : 0ull;
+        const int lo_row = win > 0 ? S + node - win + 1 : INT_MIN;  // sliding band of this row
         const bool bf = p.mma_bf16 != 0;
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         {  // Q row -> TMEM lane r, 16-bit pairs (rounded to fp16 when the MMA runs in fp16)
@@ -432,7 +441,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             // Scores in the log2 domain.  Tiles whose 64 keys are all history keys inside the range need no mask.
             float x[64];
             // (padding rows past the unit's G*T rows take it too: their Q is zero and their results are dropped)
-            if (c0 + kTcBK <= k_end && c0 + kTcBK <= S) {
+            if (c0 + kTcBK <= k_end && c0 + kTcBK <= S && c0 >= lo_last) {
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const float raw = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
@@ -442,7 +451,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
 #pragma unroll
                 for (int c = 0; c < 64; ++c) {
                     const int key = c0 + c;
-                    bool v = row_ok && key < k_end;
+                    bool v = row_ok && key < k_end && key >= lo_row;
                     if (key >= S) v = v && ((anc >> ((key - S) & 63)) & 1ull);
                     const float raw = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
                     x[c] = v ? raw * (I8 ? ksc[c] : qk_scale) : -INFINITY;
@@ -617,6 +626,7 @@ tsv_status launch_tc(const tsv_attn_desc* d, int splits, int chunk, float* ws_o,
         prm.ks[l] = reinterpret_cast<const uint16_t*>(d->k_scale[l]);
         prm.vs[l] = reinterpret_cast<const uint16_t*>(d->v_scale[l]);
     }
+    for (int l = 0; l < d->n_layers; ++l) prm.window[l] = d->window[l];
     prm.kv_len = d->kv_len;
     prm.anc = d->anc;
     prm.ws_o = ws_o;

@@ -83,3 +83,42 @@ extern "C" tsv_status tsv_tree_mask(const int32_t* parents, int32_t B, int32_t T
     dense_mask_kernel<<<grid, 256, 0, stream>>>(anc, B, T, mask_offset, dense_mask);
     return check_launch("tree_mask(dense)");
 }
+
+// ---------------------------------------------------------------------------
+// tsv_sliding_band_mask: the dense mask of a sliding-window layer (PR #1212,
+// the commit on caller masks and the sliding-window band): the caller's
+// additive mask intersected, by element-wise minimum, with the band of query
+// row q at position offset + q, which keeps columns offset + q - window < c
+// <= offset + q.  Applied only where the two can disagree (offset + T >
+// window), so shorter contexts keep exactly the caller's mask.
+// ---------------------------------------------------------------------------
+namespace tsv {
+
+__global__ void sliding_band_kernel(float* __restrict__ mask, int B, int T, int offset, int window) {
+    const int W = offset + T;
+    const size_t n = (size_t)B * T * W;
+    for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
+        const int c = (int)(e % W);
+        const int q = (int)((e / W) % T);
+        const int pos = offset + q;
+        if (c > pos || c <= pos - window) mask[e] = fminf(mask[e], -1e9f);
+    }
+}
+
+}  // namespace tsv
+
+extern "C" tsv_status tsv_sliding_band_mask(float* dense_mask, int32_t B, int32_t T, int32_t mask_offset,
+                                            int32_t window, cudaStream_t stream) {
+    using namespace tsv;
+    clear_error();
+    if (B < 0 || T < 0 || mask_offset < 0)
+        return fail(TSV_EINVAL, "sliding_band_mask: B=%d T=%d mask_offset=%d must be >= 0", B, T, mask_offset);
+    if (T > TSV_MAX_T) return fail(TSV_ECAPACITY, "sliding_band_mask: T=%d exceeds the maximum of %d nodes", T, TSV_MAX_T);
+    if (window < 1) return fail(TSV_EINVAL, "sliding_band_mask: window=%d must be >= 1", window);
+    if (B == 0 || T == 0 || (int64_t)mask_offset + T <= window) return TSV_OK;  // below the window: untouched
+    if (!dense_mask) return fail(TSV_EINVAL, "sliding_band_mask: dense_mask is null");
+    const size_t n = (size_t)B * T * (size_t)(mask_offset + T);
+    const int grid = (int)((n + 255) / 256 < (size_t)sm_count() * 8 ? (n + 255) / 256 : (size_t)sm_count() * 8);
+    sliding_band_kernel<<<grid, 256, 0, stream>>>(dense_mask, B, T, mask_offset, window);
+    return check_launch("sliding_band_mask");
+}
