@@ -137,15 +137,17 @@ def run_ours(args, rank, world, local_rank):
     if args.sliding:
         w, e = (int(x) for x in args.sliding.split(":"))
         cfg = configs.with_sliding_layers(cfg, w, e)
+    if args.append:
+        cfg = configs.scaled(cfg, name=f"{cfg.name}+append{args.append}", rot_dim=args.append)
     round_id = args.round if args.round is not None else ({1: 2}.get(args.config, 0))
     wl = Workload(cfg, device=dev, round_id=round_id, attn_path=args.attn_path)
     vr = wl.vr
     wl.save_tail()
     moved = any(p != list(range(len(p))) for p in wl.round["paths"])
     stream = torch.cuda.current_stream()
-    names = ["mask", "attn", "lm", "walk", "gather"]
+    names = ["mask"] + (["append"] if cfg.rot_dim > 0 else []) + ["attn", "lm", "walk", "gather"]
 
-    def reset():  # one launch: pristine tails of every cache and kv_len = S + T
+    def reset():  # one launch: pristine tails of every cache and kv_len (S + T; S when the round appends)
         wl.restore_tail()
 
     def step(evs=None):
@@ -199,7 +201,7 @@ def run_ours(args, rank, world, local_rank):
             left -= 8 if left >= 8 else (4 if left >= 4 else left)
             lm_groups += 1
         lm_launches = lm_groups + 1
-    launches = 1 + (1 + (tsv.attention_workspace_size(vr.adesc) > 0)) + lm_launches + 1 + 2
+    launches = 1 + (1 + (tsv.attention_workspace_size(vr.adesc) > 0)) + lm_launches + 1 + 2 + (2 if cfg.rot_dim > 0 else 0)
     return dict(cfg=cfg, ms=ms, per_kernel=per_kernel, clocks=clk.summary(), e2e=e2e, launches=launches,
                 round_id=round_id)
 
@@ -328,6 +330,9 @@ def main():
     ap.add_argument("--sliding", default=None,
                     help="W:E = a hybrid model where of every E layers the last is full attention and the others "
                          "slide over W positions")
+    ap.add_argument("--append", type=int, default=0, metavar="ROT_DIM",
+                    help="> 0: every round first appends its block (rotary width ROT_DIM, base 1e6; Int8 caches "
+                         "quantised on append), timed as its own stage")
     ap.add_argument("--layers", type=int, default=None,
                     help="attention layers (default: the workload's); fewer only for small profiler captures")
     args = ap.parse_args()
@@ -345,6 +350,8 @@ def main():
     if args.sliding:
         w, e = (int(x) for x in args.sliding.split(":"))
         cfg = configs.with_sliding_layers(cfg, w, e)
+    if args.append:
+        cfg = configs.scaled(cfg, name=f"{cfg.name}+append{args.append}", rot_dim=args.append)
     config = {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "layers": cfg.n_layers, "HQ": cfg.HQ, "HKV": cfg.HKV,
               "D": cfg.D, "S": cfg.S, "H": cfg.H, "V": cfg.V, "kv": configs.DTYPE_NAMES[cfg.kv_dtype],
               "lm_head": configs.DTYPE_NAMES[cfg.w_dtype], "topology": cfg.topology,
@@ -407,7 +414,7 @@ def main():
     }
     if args.sliding:
         config["sliding"] = {"window": int(args.sliding.split(":")[0]), "every": int(args.sliding.split(":")[1])}
-    if not args.no_cpu_baseline and not args.sliding:
+    if not args.no_cpu_baseline and not args.sliding and not args.append:
         try:
             o = run_oracle(args.config, r["round_id"])
             line["cpu_baseline"] = {"value": o["nodes_per_s"], "unit": "nodes/s", "cores": 1, "kind": "oracle",

@@ -275,6 +275,51 @@ typedef struct {
 tsv_status tsv_kv_gather_positions(const tsv_kv_desc* kv, int32_t* kv_len, const int32_t* path,
                                    const int32_t* path_len, int32_t T, int32_t* dev_status, cudaStream_t stream);
 
+/*
+ * tsv_tree_append - append the verify block to every layer's cache, each node
+ * at its own position, ahead of the attention call.
+ *   [1214] (as cited by mlxcel issue #1209, "branch the draft tree, and verify
+ *   it at its own positions"): node i is verified at position S_b + depth(i)
+ *   (the root, the last committed token, at S_b; a chain gets S_b + i); its K
+ *   and V rows still go to cache slot S_b + i, the topological block layout
+ *   tsv_tree_verify_attention and tsv_kv_gather_positions use.  Rotary
+ *   embedding (reading; the pages name only positions): the first rot_dim
+ *   features are rotated in pairs (j, j + rot_dim/2) - or (2j, 2j + 1) when
+ *   interleaved - by the angle pos * rope_base^(-2j / rot_dim); Q and K are
+ *   rotated, V is not.  Int8 caches ([1212] gather_positions commit: one scale
+ *   per token; a per-token scale maps every single-valued token to the same
+ *   code): scale = fp16(absmax / 127) with the division in fp32, code =
+ *   round-half-to-even(x / scale) in fp32, clamped to [-127, 127]; a token whose
+ *   scale is 0 stores zero codes.  fp16 / bf16 caches store the rotated fp32
+ *   values rounded to nearest even.  Angles are reduced in fp64, so positions
+ *   up to 2^31 keep fp32 accuracy.
+ *   kv_len: in, S_b per sequence; out, S_b + T.  depth: from tsv_tree_mask.
+ *   Device errors: TSV_DEV_BAD_KV_LEN when S_b + T > s_cap; a sequence whose
+ *   depth[b][0] != 0 (its mask call failed) is skipped.  Skipped sequences
+ *   keep their caches and kv_len.
+ */
+typedef struct {
+    int32_t n_layers;   /* 1 .. TSV_MAX_LAYERS */
+    int32_t B, T, HQ, HKV, D; /* HQ % HKV == 0; D in {64, 128, 256} */
+    int64_t s_cap;
+    int32_t kv_dtype;   /* TSV_F16, TSV_BF16 or TSV_I8_SCALED */
+    int32_t rot_dim;    /* even, 2 <= rot_dim <= D; features >= rot_dim are copied */
+    int32_t interleaved; /* 0: pairs (j, j + rot_dim/2); 1: pairs (2j, 2j + 1) */
+    int32_t reserved;
+    double rope_base;   /* > 0, e.g. 1e4 or 1e6 */
+    const void* q_in[TSV_MAX_LAYERS];  /* per layer: bf16 [B, T, HQ, D], not yet rotated */
+    void* q_out[TSV_MAX_LAYERS];       /* per layer: bf16 [B, T, HQ, D], out (may equal q_in) */
+    const void* k_new[TSV_MAX_LAYERS]; /* per layer: bf16 [B, T, HKV, D], not yet rotated */
+    const void* v_new[TSV_MAX_LAYERS]; /* per layer: bf16 [B, T, HKV, D] */
+    void* k[TSV_MAX_LAYERS];           /* per layer caches as in tsv_kv_desc */
+    void* v[TSV_MAX_LAYERS];
+    void* k_scale[TSV_MAX_LAYERS];
+    void* v_scale[TSV_MAX_LAYERS];
+    const int32_t* depth;              /* int32 [B, T] */
+} tsv_append_desc;
+
+tsv_status tsv_tree_append(const tsv_append_desc* d, int32_t* kv_len, int32_t* dev_status, cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -57,3 +57,14 @@ def kv_values(dtype: int, store, scale_bits=None) -> np.ndarray:
     if dtype == 2:
         return int8_scaled(store, scale_bits)
     raise ValueError(f"not a KV format: {dtype}")
+
+
+def round_bf16(x) -> np.ndarray:
+    """fp64 values rounded to the nearest bf16 value (8 significant bits, ties to even; normal range)."""
+    m, e = np.frexp(np.asarray(x, dtype=np.float64))
+    return np.ldexp(np.rint(np.ldexp(m, 8)), e - 8)
+
+
+def round_f16(x) -> np.ndarray:
+    """fp64 values rounded to the nearest fp16 value (numpy's correctly rounded conversion)."""
+    return np.asarray(x, dtype=np.float64).astype(np.float16).astype(np.float64)

@@ -39,6 +39,8 @@ class Config:
     plant_c: float = 0.25  # planting strength of the target direction in hidden
     min_gap: float = 1e-2  # required top-1/top-2 logit gap (fp64)
     window: tuple = ()     # per-layer sliding windows (0 = full attention); empty = every layer full
+    rot_dim: int = 0       # > 0: the round appends its block (rotary width rot_dim, base rope_base) before attention
+    rope_base: float = 1e6
     notes: str = ""
 
     @property

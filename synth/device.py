@@ -71,6 +71,16 @@ def alloc_q(cfg: Config, layer: int, device) -> torch.Tensor:
     return t
 
 
+def alloc_new_kv(cfg: Config, layer: int, device) -> dict:
+    """The block's new K and V rows [B, T, HKV, D] bf16 (inputs of the block append)."""
+    out = {}
+    for which, kind in (("k_new", st.KIND_KNEW), ("v_new", st.KIND_VNEW)):
+        t = torch.empty(cfg.B, cfg.T, cfg.HKV, cfg.D, dtype=torch.bfloat16, device=device)
+        fill(t, NORMAL_BF16, st.key(cfg, kind, layer), (1, 1, cfg.B * cfg.T * cfg.HKV, cfg.D), (0, 0, cfg.D))
+        out[which] = t
+    return out
+
+
 def alloc_head(cfg: Config, device) -> dict:
     V, H = cfg.V, cfg.H
     if cfg.w_dtype == Q4:

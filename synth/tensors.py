@@ -33,6 +33,7 @@ from .configs import BF16, F16, I8, Q4, Config
 
 KIND_Q, KIND_K, KIND_V, KIND_KS, KIND_VS, KIND_W, KIND_WQ, KIND_WS, KIND_WB, KIND_HN = range(1, 11)
 KIND_TREE, KIND_TOK = 11, 12
+KIND_KNEW, KIND_VNEW = 13, 14  # the block's K and V rows before the append (K not yet rotated)
 
 W_SIGMA = np.float32(0.02)
 KV_SCALE_LO, KV_SCALE_W = np.float32(0.005), np.float32(0.045)
@@ -80,6 +81,14 @@ def q_full(cfg: Config, layer: int) -> np.ndarray:
     n = cfg.B * cfg.T * cfg.HQ * cfg.D
     out = _gen_flat(key(cfg, KIND_Q, layer), n, BF16)
     return out.reshape(cfg.B, cfg.T, cfg.HQ, cfg.D)
+
+
+def new_kv_rows(cfg: Config, which: str, layer: int, b: int, node: int) -> np.ndarray:
+    """bf16 bits of the new K or V rows [b, node, :, :] handed to the block append -> uint16[HKV, D]."""
+    kind = KIND_KNEW if which == "k" else KIND_VNEW
+    base = ((b * cfg.T + node) * cfg.HKV + np.arange(cfg.HKV, dtype=np.int64)) * cfg.D
+    idx = base[:, None] + np.arange(cfg.D, dtype=np.int64)[None, :]
+    return bits_for_index(key(cfg, kind, layer), idx, BF16)
 
 
 def kv_rows(cfg: Config, which: str, layer: int, b: int, kvh: int, c0: int, c1: int) -> np.ndarray:

@@ -31,13 +31,20 @@ class Workload:
         self.s_cap = s_cap or cfg.NKV
         self.caches = [sd.alloc_cache(cfg, l, self.s_cap, device) for l in range(L)]
         self.q = [sd.alloc_q(cfg, l, device) for l in range(L)]
+        # cfg.rot_dim > 0: every round appends its block first (Q rotated from q_in into q, K/V rows into [S, S+T))
+        self.append = cfg.rot_dim > 0
+        self.q_in = self.new_kv = None
+        if self.append:
+            self.q_in = self.q
+            self.q = [torch.empty_like(t) for t in self.q_in]
+            self.new_kv = [sd.alloc_new_kv(cfg, l, device) for l in range(L)]
         self.head = sd.alloc_head(cfg, device)
         self.round = trees.make_round(cfg, round_id)
         r = self.round
         self.parents = torch.from_numpy(r["parents"]).to(device)
         self.tokens = torch.from_numpy(r["tokens"]).to(device)
         self.hidden = bits_to_bf16(r["hidden"], device)
-        self.kv_len = torch.full((cfg.B,), cfg.NKV, dtype=torch.int32, device=device)
+        self.kv_len = torch.full((cfg.B,), cfg.S if self.append else cfg.NKV, dtype=torch.int32, device=device)
         i8 = cfg.kv_dtype == I8
         self.vr = VerifyRound(
             T=cfg.T, HQ=cfg.HQ, HKV=cfg.HKV, D=cfg.D, V=cfg.V, kv_dtype=cfg.kv_dtype, w_dtype=cfg.w_dtype,
@@ -47,7 +54,10 @@ class Workload:
             k_scale=[c["ks"] for c in self.caches] if i8 else None,
             v_scale=[c["vs"] for c in self.caches] if i8 else None,
             w_scales=self.head["scales"], w_biases=self.head["biases"], splits=splits, attn_path=attn_path,
-            window=tuple(cfg.layer_window(l) for l in range(L)) if cfg.window else None)
+            window=tuple(cfg.layer_window(l) for l in range(L)) if cfg.window else None,
+            q_in=self.q_in, k_new=[x["k_new"] for x in self.new_kv] if self.append else None,
+            v_new=[x["v_new"] for x in self.new_kv] if self.append else None, rot_dim=cfg.rot_dim,
+            rope_base=cfg.rope_base)
         self._tail = None
 
     def set_round(self, round_id: int):
@@ -61,12 +71,13 @@ class Workload:
     def save_tail(self):
         """Keep a pristine copy of the verify block [S, S+T) of every cache and of kv_len (the gather rewrites both).
 
-        ``restore_tail`` then puts them back with one batched copy launch.
+        ``restore_tail`` then puts them back with one batched copy launch.  A round that appends its block keeps
+        only kv_len (= S): the append rewrites the block rows every round.
         """
         S, T = self.cfg.S, self.cfg.T
         rows = []
         self._saved = []
-        for c in self.caches:
+        for c in ([] if self.append else self.caches):  # an appending round rewrites the block itself
             for name, t in c.items():
                 tail = t[:, :, S:S + T]
                 saved = tail.contiguous().clone()

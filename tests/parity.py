@@ -11,6 +11,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
+from oracle import append as oap
 from oracle import attention as oa
 from oracle import gather as og
 from oracle import lm_head as ol
@@ -38,25 +39,51 @@ def oracle_mask(parents: np.ndarray):
     return anc, depth
 
 
-def kv_values(cfg, layer, b, kvh):
+def stored(cfg, x):
+    """The value a cache of cfg's format keeps for fp64 row values x [n, D] (oracle's own rounding)."""
+    if cfg.kv_dtype == configs.I8:
+        out = []
+        for row in x:
+            codes, sbits = oap.quantize_token(row)
+            out.append(codes.astype(np.float64) * float(np.uint16(sbits).view(np.float16)))
+        return np.stack(out)
+    return osd.round_f16(x) if cfg.kv_dtype == configs.F16 else osd.round_bf16(x)
+
+
+def appended_rows(cfg, layer, b, kvh, parents_b):
+    """K and V block rows [S, S+T) as an appending round stores them (rotated K, then the cache's format)."""
+    pos = oap.node_positions(parents_b, cfg.S)
+    kn = osd.bf16(np.stack([tensors.new_kv_rows(cfg, "k", layer, b, i)[kvh] for i in range(cfg.T)]))
+    vn = osd.bf16(np.stack([tensors.new_kv_rows(cfg, "v", layer, b, i)[kvh] for i in range(cfg.T)]))
+    k_rot = np.stack([oap.rope(kn[i], pos[i], cfg.rope_base, cfg.rot_dim) for i in range(cfg.T)])
+    return stored(cfg, k_rot), stored(cfg, vn)
+
+
+def kv_values(cfg, layer, b, kvh, parents_b=None):
     """fp64 K and V of one (layer, sequence, kv head) over the logical S + T rows."""
     out = []
     for w in ("k", "v"):
         store = tensors.kv_rows(cfg, w, layer, b, kvh, 0, cfg.NKV)
         sc = tensors.kv_scales(cfg, w, layer, b, kvh, 0, cfg.NKV) if cfg.kv_dtype == configs.I8 else None
         out.append(osd.kv_values(cfg.kv_dtype, store, sc))
+    if cfg.rot_dim > 0:  # the round appended its own block over rows [S, S + T)
+        kb, vb = appended_rows(cfg, layer, b, kvh, parents_b)
+        out[0][cfg.S:cfg.NKV], out[1][cfg.S:cfg.NKV] = kb, vb
     return out
 
 
 def oracle_attention_rows(cfg, layer, b, kvh, nodes, parents_b):
     """O rows for every (node in nodes, head of the kv group) -> dict[(i, h)] = fp64 [D]."""
-    K, V = kv_values(cfg, layer, b, kvh)
+    K, V = kv_values(cfg, layer, b, kvh, parents_b)
     G = cfg.G
     heads = [kvh * G + g for g in range(G)]
     res = {}
     w = cfg.layer_window(layer)
+    pos = oap.node_positions(parents_b, cfg.S)
     for i in nodes:
         q = osd.bf16(tensors.q_rows(cfg, layer, b, i, heads))
+        if cfg.rot_dim > 0:  # the attention reads Q rotated to the node's position, stored as bf16
+            q = osd.round_bf16(oap.rope(q, pos[i], cfg.rope_base, cfg.rot_dim))
         vis = ot.ancestors(parents_b, i)
         cols = ot.visible_keys(parents_b, i, cfg.S, w)
         for gi, h in enumerate(heads):
@@ -84,6 +111,30 @@ def oracle_logits_at(cfg, hidden_bits_row, vocab_rows):
     wr = head_rows_fn(cfg)
     W = np.concatenate([wr(int(v), int(v) + 1) for v in vocab_rows])
     return W @ osd.bf16(hidden_bits_row)
+
+
+def _cache_rows(cfg, c, which, b, kvh, r0, r1):
+    """fp64 values of GPU cache rows [r0, r1) of one (sequence, kv head)."""
+    t = c[which][b, kvh, r0:r1].cpu()
+    if cfg.kv_dtype == configs.I8:
+        sc = c["ks" if which == "k" else "vs"][b, kvh, r0:r1].cpu().view(torch.int16).numpy().view(np.uint16)
+        return osd.int8_scaled(t.numpy(), sc)
+    bits = t.view(torch.int16).numpy().view(np.uint16)
+    return osd.f16(bits) if cfg.kv_dtype == configs.F16 else osd.bf16(bits)
+
+
+def _appended_gather_ok(cfg, c, layer, b, kvh, parents_b, path) -> bool:
+    S, T = cfg.S, cfg.T
+    kb, vb = appended_rows(cfg, layer, b, kvh, parents_b)
+    ok = True
+    for which, exp_rows, exact in (("k", kb, False), ("v", vb, True)):
+        exp, _ = og.gather_within_tail(exp_rows, 0, path)
+        got = _cache_rows(cfg, c, which, b, kvh, S, S + T)
+        if exact:
+            ok &= bool(np.array_equal(got, exp))
+        else:
+            ok &= bool(np.max(np.abs(got - exp)) <= 1e-2 * max(float(np.max(np.abs(exp))), 1e-30))
+    return ok
 
 
 # ----------------------------------------------------------------------------- comparison of a round
@@ -178,6 +229,9 @@ def check_round(wl, out, layers=(0,), attn_rows="all", lm="auto", kv_heads=None,
             path = r["paths"][b]
             gather_ok &= int(kvl[b]) == S + len(path)
             for kvh in kv_heads:
+                if cfg.rot_dim > 0:  # appended rows: V stored exactly, rotated K within one rounding step
+                    gather_ok &= _appended_gather_ok(cfg, c, layer, b, kvh, parents[b].tolist(), path)
+                    continue
                 for w, key in (("k", "k"), ("v", "v")):
                     orig = tensors.kv_rows(cfg, w, layer, b, kvh, S, S + T)
                     exp, _ = og.gather_within_tail(orig, 0, path)

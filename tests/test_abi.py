@@ -38,7 +38,7 @@ def test_version_and_error_string():
 
 @pytest.mark.skipif(shutil.which("gcc") is None, reason="gcc not available")
 def test_struct_layouts_match_header(tmp_path):
-    fields = {"tsv_attn_desc": _abi.AttnDesc, "tsv_kv_desc": _abi.KvDesc}
+    fields = {"tsv_attn_desc": _abi.AttnDesc, "tsv_kv_desc": _abi.KvDesc, "tsv_append_desc": _abi.AppendDesc}
     lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "tsv.h"', "int main(void){"]
     for cname, py in fields.items():
         lines.append(f'printf("{cname} %zu\\n", sizeof({cname}));')
@@ -91,5 +91,13 @@ def test_host_validation_refuses_without_launching():
     st = lib.tsv_lm_head_argmax(C.c_void_p(16), 1, 256, 10, 1, C.c_void_p(16), None, None, C.c_void_p(16), None,
                                 C.c_void_p(16), 0, None)
     assert st == _abi.ECAPACITY  # workspace too small
+    a = _abi.AppendDesc()
+    a.n_layers, a.B, a.T, a.HQ, a.HKV, a.D, a.s_cap, a.kv_dtype, a.rot_dim, a.rope_base = 1, 1, 4, 8, 2, 64, 16, 0, 63, 1e4
+    st = lib.tsv_tree_append(C.byref(a), C.c_void_p(16), None, None)
+    assert st == _abi.EINVAL and b"rot_dim" in lib.tsv_last_error()  # odd rotary width
+    a.rot_dim, a.rope_base = 64, 0.0
+    assert lib.tsv_tree_append(C.byref(a), C.c_void_p(16), None, None) == _abi.EINVAL
+    a.rope_base, a.D = 1e4, 96
+    assert lib.tsv_tree_append(C.byref(a), C.c_void_p(16), None, None) == _abi.EUNSUPPORTED
     assert lib.tsv_lm_head_workspace_size(3, 256, 1000, 1) >= 24
     assert lib.tsv_lm_head_workspace_size(16, 512, 1000, 3) >= 16 * 8 + 16 * 512 * 2  # fp16 copy of hidden

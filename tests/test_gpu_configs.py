@@ -153,3 +153,17 @@ def test_sliding_hybrid_full_size(gpu_lib, idx, window, every):
     assert rep["ok"], rep
     del wl, out
     _free()
+
+
+@pytest.mark.parametrize("idx,rot_dim", [(1, 256), (2, 64)])
+def test_round_that_appends_its_block_full_size(gpu_lib, idx, rot_dim):
+    """A round that first appends its block (rotary positions S + depth, Int8 quantised on append for the
+    specinfer workload), then verifies it: every stage against the oracle of the appended cache."""
+    cfg = configs.scaled(configs.CONFIGS[idx], name=configs.CONFIGS[idx].name + f"+append{rot_dim}", rot_dim=rot_dim)
+    wl = Workload(cfg)
+    assert wl.kv_len.tolist() == [cfg.S] * cfg.B
+    out = _run(wl)
+    rep = check_round(wl, out, layers=[0, 7], attn_rows="all" if cfg.T <= 16 else 4, kv_heads=[0, 3], lm="planted")
+    assert rep["ok"], rep
+    del wl, out
+    _free()

@@ -44,6 +44,16 @@ class KvDesc(C.Structure):
     ]
 
 
+class AppendDesc(C.Structure):
+    _fields_ = [
+        ("n_layers", _i32), ("B", _i32), ("T", _i32), ("HQ", _i32), ("HKV", _i32), ("D", _i32), ("s_cap", _i64),
+        ("kv_dtype", _i32), ("rot_dim", _i32), ("interleaved", _i32), ("reserved", _i32), ("rope_base", C.c_double),
+        ("q_in", _vp * MAX_LAYERS), ("q_out", _vp * MAX_LAYERS), ("k_new", _vp * MAX_LAYERS),
+        ("v_new", _vp * MAX_LAYERS), ("k", _vp * MAX_LAYERS), ("v", _vp * MAX_LAYERS),
+        ("k_scale", _vp * MAX_LAYERS), ("v_scale", _vp * MAX_LAYERS), ("depth", _vp),
+    ]
+
+
 SIGNATURES = {
     "tsv_last_error": (C.c_char_p, []),
     "tsv_version": (C.c_int, []),
@@ -56,6 +66,7 @@ SIGNATURES = {
     "tsv_lm_head_argmax_noalloc": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "tsv_tree_accept_walk": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "tsv_kv_gather_positions": (C.c_int, [C.POINTER(KvDesc), _vp, _vp, _vp, _i32, _vp, _vp]),
+    "tsv_tree_append": (C.c_int, [C.POINTER(AppendDesc), _vp, _vp, _vp]),
 }
 
 _lib = None

@@ -13,7 +13,7 @@ from dataclasses import dataclass, field
 import torch
 
 from . import _abi
-from ._abi import BF16, F16, I8_SCALED, MAX_LAYERS, Q4_G64, AttnDesc, KvDesc, check, load
+from ._abi import BF16, F16, I8_SCALED, MAX_LAYERS, Q4_G64, AppendDesc, AttnDesc, KvDesc, check, load
 
 KV_TORCH_DTYPE = {F16: torch.float16, BF16: torch.bfloat16, I8_SCALED: torch.int8}
 
@@ -107,6 +107,44 @@ def tree_verify_attention(desc: AttnDesc, workspace=None, dev_status=None, strea
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     check(lib.tsv_tree_verify_attention(C.byref(desc), _p(workspace), ws_bytes, _p(dev_status), _stream(stream)),
           "tree_verify_attention")
+
+
+# ----------------------------------------------------------------------------- block append (rotary + Int8)
+def append_desc(q_in, q_out, k_new, v_new, k, v, depth, *, T, HQ, HKV, D, kv_dtype, rot_dim, rope_base,
+                interleaved=False, k_scale=None, v_scale=None) -> AppendDesc:
+    """Descriptor over per-layer lists: q_in/q_out bf16 [B,T,HQ,D]; k_new/v_new bf16 [B,T,HKV,D]; caches as
+    for attn_desc."""
+    n = len(q_in)
+    if not (1 <= n <= MAX_LAYERS) or not (len(q_out) == len(k_new) == len(v_new) == len(k) == len(v) == n):
+        raise ValueError("per-layer lists must have the same length in [1, 64]")
+    B = q_in[0].shape[0]
+    s_cap = k[0].shape[2]
+    d = AppendDesc()
+    d.n_layers, d.B, d.T, d.HQ, d.HKV, d.D, d.s_cap = n, B, T, HQ, HKV, D, s_cap
+    d.kv_dtype, d.rot_dim, d.interleaved, d.rope_base = kv_dtype, int(rot_dim), int(bool(interleaved)), float(rope_base)
+    kvt = KV_TORCH_DTYPE[kv_dtype]
+    for l in range(n):
+        _cuda(q_in[l], "q_in", torch.bfloat16, (B, T, HQ, D))
+        _cuda(q_out[l], "q_out", torch.bfloat16, (B, T, HQ, D))
+        _cuda(k_new[l], "k_new", torch.bfloat16, (B, T, HKV, D))
+        _cuda(v_new[l], "v_new", torch.bfloat16, (B, T, HKV, D))
+        _cuda(k[l], "k", kvt, (B, HKV, s_cap, D))
+        _cuda(v[l], "v", kvt, (B, HKV, s_cap, D))
+        d.q_in[l], d.q_out[l] = q_in[l].data_ptr(), q_out[l].data_ptr()
+        d.k_new[l], d.v_new[l], d.k[l], d.v[l] = k_new[l].data_ptr(), v_new[l].data_ptr(), k[l].data_ptr(), v[l].data_ptr()
+        if kv_dtype == I8_SCALED:
+            _cuda(k_scale[l], "k_scale", torch.float16, (B, HKV, s_cap))
+            _cuda(v_scale[l], "v_scale", torch.float16, (B, HKV, s_cap))
+            d.k_scale[l], d.v_scale[l] = k_scale[l].data_ptr(), v_scale[l].data_ptr()
+    _cuda(depth, "depth", torch.int32, (B, T))
+    d.depth = depth.data_ptr()
+    return d
+
+
+def tree_append(desc: AppendDesc, kv_len, dev_status=None, stream=None):
+    """Append the block at the nodes' positions; kv_len int32 [B]: S_b in, S_b + T out."""
+    _cuda(kv_len, "kv_len", torch.int32, (desc.B,))
+    check(load().tsv_tree_append(C.byref(desc), _p(kv_len), _p(dev_status), _stream(stream)), "tree_append")
 
 
 # ----------------------------------------------------------------------------- a3 LM head
@@ -205,6 +243,11 @@ class VerifyRound:
     splits: int = 0
     attn_path: int = 0
     window: tuple = None
+    q_in: list = None      # block append (optional): pre-rotation Q, new K and V rows per layer
+    k_new: list = None
+    v_new: list = None
+    rot_dim: int = 0
+    rope_base: float = 1e6
     outs: dict = field(default_factory=dict)
 
     def __post_init__(self):
@@ -221,15 +264,23 @@ class VerifyRound:
                                window=self.window)
         self.kdesc = kv_desc(self.k, self.v, HKV=self.HKV, D=self.D, kv_dtype=self.kv_dtype, k_scale=self.k_scale,
                              v_scale=self.v_scale)
+        self.apdesc = None
+        if self.q_in is not None:  # the round appends its block: Q rotated from q_in into q, K/V rows into the caches
+            self.apdesc = append_desc(self.q_in, self.q, self.k_new, self.v_new, self.k, self.v, self.outs["depth"], T=T,
+                                      HQ=self.HQ, HKV=self.HKV, D=self.D, kv_dtype=self.kv_dtype, rot_dim=self.rot_dim,
+                                      rope_base=self.rope_base, k_scale=self.k_scale, v_scale=self.v_scale)
         self.attn_ws = torch.empty(max(attention_workspace_size(self.adesc), 256), dtype=torch.uint8, device=dev)
         self.lm_ws = torch.empty(max(lm_head_workspace_size(B * T, self.hidden.shape[1], self.V, self.w_dtype), 256),
                                  dtype=torch.uint8, device=dev)
 
-    def run(self, stream=None, stages=("mask", "attn", "lm", "walk", "gather")):
+    def run(self, stream=None, stages=("mask", "append", "attn", "lm", "walk", "gather")):
+        """Issue the round's calls in order; "append" runs only when the round was built with append inputs."""
         o = self.outs
         B, T = self.parents.shape
         if "mask" in stages:
             tree_mask(self.parents, o["anc"], o["depth"], dev_status=o["status"], stream=stream)
+        if "append" in stages and self.apdesc is not None:
+            tree_append(self.apdesc, self.kv_len, dev_status=o["status"], stream=stream)
         if "attn" in stages:
             tree_verify_attention(self.adesc, self.attn_ws, dev_status=o["status"], stream=stream)
         if "lm" in stages:
