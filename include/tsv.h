@@ -278,8 +278,9 @@ tsv_status tsv_kv_gather_positions(const tsv_kv_desc* kv, int32_t* kv_len, const
 /*
  * tsv_tree_append - append the verify block to every layer's cache, each node
  * at its own position, ahead of the attention call.
- *   [1214] (as cited by mlxcel issue #1209, "branch the draft tree, and verify
- *   it at its own positions"): node i is verified at position S_b + depth(i)
+ *   [1185], the closing comment's list of follow-ups: the tree path verifies
+ *   the tree at its own positions (the title of the PR that added tree
+ *   drafting there).  Node i is verified at position S_b + depth(i)
  *   (the root, the last committed token, at S_b; a chain gets S_b + i); its K
  *   and V rows still go to cache slot S_b + i, the topological block layout
  *   tsv_tree_verify_attention and tsv_kv_gather_positions use.  Rotary

@@ -2,8 +2,8 @@
 
 Definitions followed:
 
-* Positions - mlxcel PR #1214 ("branch the draft tree, and verify it at its own positions", as cited by
-  issue #1209): a tree node is verified at its own position, not at its slot in the flattened block.  Reading:
+* Positions - mlxcel issue #1185, the closing comment's follow-up list: the tree path verifies the tree at its
+  own positions, not at its nodes' slots in the flattened block.  Reading:
   node i sits at position S + depth(i) (the root, the last committed token, at S); for a chain depth(i) = i, the
   chain verify's positions.
 * Rotary embedding - the pages name it only through "positions"; the plainest reading is the standard rotary

@@ -1,8 +1,8 @@
 // tsv_tree_append: the verify block appended to every layer's cache, each
 // node at its own position.
 //
-// mlxcel PR #1214 (cited by issue #1209: "branch the draft tree, and verify
-// it at its own positions"): node i of the block is verified at position
+// mlxcel issue #1185, the closing comment's follow-up list: the tree path
+// verifies the tree at its own positions.  Node i of the block is verified at position
 // S + depth(i), while its K/V rows keep the topological slot S + i.  Q and
 // the new K rows are rotated (rotary embedding of the first rot_dim
 // features); V is not.  Int8 caches (PR #1212, gather_positions commit: one
