@@ -139,6 +139,9 @@ def run_ours(args, rank, world, local_rank):
         cfg = configs.with_sliding_layers(cfg, w, e)
     if args.append:
         cfg = configs.scaled(cfg, name=f"{cfg.name}+append{args.append}", rot_dim=args.append)
+    if args.sampled:
+        t, k, p = args.sampled.split(":")
+        cfg = configs.scaled(cfg, name=f"{cfg.name}+sampled{args.sampled}", sample=(float(t), int(k), float(p)))
     round_id = args.round if args.round is not None else ({1: 2}.get(args.config, 0))
     wl = Workload(cfg, device=dev, round_id=round_id, attn_path=args.attn_path)
     vr = wl.vr
@@ -187,13 +190,16 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.synchronize()
     got_len = vr.outs["path_len"].cpu().tolist()
     want_len = [len(p) for p in wl.round["paths"]]
-    assert got_len == want_len, (got_len, want_len)
+    if cfg.sample:  # the walk follows each node's draw, not the planted argmax path
+        assert all(1 <= n <= cfg.T for n in got_len), got_len
+    else:
+        assert got_len == want_len, (got_len, want_len)
 
     # e2e through the public API with host buffers: per step H2D of the round inputs, D2H of the results
     e2e = run_e2e(args, wl, stream) if rank == 0 else None
 
     # launches of our kernels per step
-    if cfg.rows > 8:  # tensor-core LM head: (fp16 copy of hidden) + kernel + unpack
+    if cfg.rows > 8:  # tensor-core LM head: (fp16 copy of hidden) + kernel + unpack (sampled: + the sampler)
         lm_launches = 1 + (cfg.w_dtype != configs.BF16) + 1
     else:  # CUDA-core GEMV: one launch per group of up to 8 rows + unpack
         lm_groups, left = 0, cfg.rows
@@ -201,6 +207,15 @@ def run_ours(args, rank, world, local_rank):
             left -= 8 if left >= 8 else (4 if left >= 4 else left)
             lm_groups += 1
         lm_launches = lm_groups + 1
+    if cfg.sample:  # no unpack; top-k passes (one per 4096-entry chunk level) and the draw
+        n, passes = cfg.V, 0
+        while True:
+            passes += 1
+            ch = (n + 4095) // 4096
+            if ch == 1:
+                break
+            n = ch * min(int(cfg.sample[1]), cfg.V)
+        lm_launches += passes + 1 - 1
     launches = 1 + (1 + (tsv.attention_workspace_size(vr.adesc) > 0)) + lm_launches + 1 + 2 + (2 if cfg.rot_dim > 0 else 0)
     return dict(cfg=cfg, ms=ms, per_kernel=per_kernel, clocks=clk.summary(), e2e=e2e, launches=launches,
                 round_id=round_id)
@@ -333,6 +348,9 @@ def main():
     ap.add_argument("--append", type=int, default=0, metavar="ROT_DIM",
                     help="> 0: every round first appends its block (rotary width ROT_DIM, base 1e6; Int8 caches "
                          "quantised on append), timed as its own stage")
+    ap.add_argument("--sampled", default=None, metavar="T:K:P",
+                    help="sampled verification: the LM stage writes every logit and draws each node's token at "
+                         "temperature T from the top-K, top-P nucleus (e.g. 1:20:0.95)")
     ap.add_argument("--layers", type=int, default=None,
                     help="attention layers (default: the workload's); fewer only for small profiler captures")
     args = ap.parse_args()
@@ -352,6 +370,9 @@ def main():
         cfg = configs.with_sliding_layers(cfg, w, e)
     if args.append:
         cfg = configs.scaled(cfg, name=f"{cfg.name}+append{args.append}", rot_dim=args.append)
+    if args.sampled:
+        t, k, p = args.sampled.split(":")
+        cfg = configs.scaled(cfg, name=f"{cfg.name}+sampled{args.sampled}", sample=(float(t), int(k), float(p)))
     config = {"workload": cfg.name, "B": cfg.B, "T": cfg.T, "layers": cfg.n_layers, "HQ": cfg.HQ, "HKV": cfg.HKV,
               "D": cfg.D, "S": cfg.S, "H": cfg.H, "V": cfg.V, "kv": configs.DTYPE_NAMES[cfg.kv_dtype],
               "lm_head": configs.DTYPE_NAMES[cfg.w_dtype], "topology": cfg.topology,
@@ -414,7 +435,7 @@ def main():
     }
     if args.sliding:
         config["sliding"] = {"window": int(args.sliding.split(":")[0]), "every": int(args.sliding.split(":")[1])}
-    if not args.no_cpu_baseline and not args.sliding and not args.append:
+    if not args.no_cpu_baseline and not args.sliding and not args.append and not args.sampled:
         try:
             o = run_oracle(args.config, r["round_id"])
             line["cpu_baseline"] = {"value": o["nodes_per_s"], "unit": "nodes/s", "cores": 1, "kind": "oracle",

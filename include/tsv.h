@@ -203,6 +203,40 @@ tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32_t H, int32
                               float* maxlogit, void* workspace, size_t ws_bytes, cudaStream_t stream);
 
 /*
+ * tsv_lm_head_logits - the same projection, writing every logit instead of the
+ * argmax: logits float [rows, V] (fp32 accumulation, same kernels and
+ * workspace as tsv_lm_head_argmax).  The input of sampled verification
+ * (tsv_sample_nucleus): Splash issue #728, "What it does" - sampled requests
+ * draw from the target's nucleus-filtered distribution at every node.
+ */
+tsv_status tsv_lm_head_logits(const void* hidden, int32_t rows, int32_t H, int32_t V, int32_t w_dtype,
+                              const void* W, const void* scales, const void* biases, float* logits,
+                              void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * tsv_sample_nucleus - each node's draw for sampled (temperature > 0)
+ * verification.  Splash issue #728, "What it does": every node draws from
+ * the nucleus-filtered distribution with its own uniform, which keeps the
+ * chain verify's output distribution; the walk (tsv_tree_accept_walk, with
+ * these tokens in place of the argmax) then follows the child whose draft
+ * token equals the draw.  Filter order (reading; the page names the three
+ * knobs): logits / temperature, the top_k largest (ties to the lower index),
+ * softmax over them, the shortest descending prefix whose mass reaches top_p,
+ * renormalised; the token is the first whose cumulative mass exceeds
+ * uniforms[row] * (kept mass).
+ *   logits   float [rows, V] (tsv_lm_head_logits); uniforms float [rows] in
+ *            [0, 1), one per node, drawn by the caller; tokens int32 [rows], out.
+ *   1 <= top_k <= 64 (TSV_EUNSUPPORTED above: the top-k selection is exact
+ *   and bounded), temperature > 0, 0 < top_p <= 1, rows <= 65535.
+ *   Arithmetic: softmax weights and prefix sums in fp32.
+ */
+size_t tsv_sample_workspace_size(int32_t rows, int32_t V, int32_t top_k);
+
+tsv_status tsv_sample_nucleus(const float* logits, int32_t rows, int32_t V, float temperature, int32_t top_k,
+                              float top_p, const float* uniforms, int32_t* tokens, void* workspace, size_t ws_bytes,
+                              cudaStream_t stream);
+
+/*
  * tsv_lm_head_argmax_noalloc - tsv_lm_head_argmax without a workspace argument.
  *   The pages have no counterpart: this entry point exists only in this
  *   library, for callers that cannot allocate device memory themselves -

@@ -55,3 +55,9 @@ def argmax_streamed(weight_rows, h, V: int):
             else:
                 second[r] = max(second[r], ctop[r])
     return arg, best, best - second
+
+
+def logits_streamed(weight_rows, h, V: int) -> np.ndarray:
+    """All fp64 logits [R, V], the head produced chunk by chunk by ``weight_rows(r0, r1)``."""
+    h = np.atleast_2d(np.asarray(h, dtype=np.float64))
+    return np.concatenate([h @ weight_rows(r0, min(V, r0 + CHUNK_ROWS)).T for r0 in range(0, V, CHUNK_ROWS)], axis=1)

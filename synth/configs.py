@@ -41,6 +41,7 @@ class Config:
     window: tuple = ()     # per-layer sliding windows (0 = full attention); empty = every layer full
     rot_dim: int = 0       # > 0: the round appends its block (rotary width rot_dim, base rope_base) before attention
     rope_base: float = 1e6
+    sample: tuple = ()     # (temperature, top_k, top_p): sampled verification; empty = greedy
     notes: str = ""
 
     @property

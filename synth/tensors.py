@@ -34,6 +34,7 @@ from .configs import BF16, F16, I8, Q4, Config
 KIND_Q, KIND_K, KIND_V, KIND_KS, KIND_VS, KIND_W, KIND_WQ, KIND_WS, KIND_WB, KIND_HN = range(1, 11)
 KIND_TREE, KIND_TOK = 11, 12
 KIND_KNEW, KIND_VNEW = 13, 14  # the block's K and V rows before the append (K not yet rotated)
+KIND_U = 15  # per-node uniforms of sampled verification
 
 W_SIGMA = np.float32(0.02)
 KV_SCALE_LO, KV_SCALE_W = np.float32(0.005), np.float32(0.045)
@@ -81,6 +82,12 @@ def q_full(cfg: Config, layer: int) -> np.ndarray:
     n = cfg.B * cfg.T * cfg.HQ * cfg.D
     out = _gen_flat(key(cfg, KIND_Q, layer), n, BF16)
     return out.reshape(cfg.B, cfg.T, cfg.HQ, cfg.D)
+
+
+def node_uniforms(cfg: Config, round_id: int) -> np.ndarray:
+    """fp32 uniforms in [0, 1), one per node of the round ([B * T]), for sampled verification."""
+    idx = np.arange(cfg.B * cfg.T, dtype=np.int64) + np.int64(round_id) * (cfg.B * cfg.T)
+    return rng.uniform_f32(_draws(key(cfg, KIND_U), idx), 0.0, 1.0)
 
 
 def new_kv_rows(cfg: Config, which: str, layer: int, b: int, node: int) -> np.ndarray:

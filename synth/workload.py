@@ -45,6 +45,10 @@ class Workload:
         self.tokens = torch.from_numpy(r["tokens"]).to(device)
         self.hidden = bits_to_bf16(r["hidden"], device)
         self.kv_len = torch.full((cfg.B,), cfg.S if self.append else cfg.NKV, dtype=torch.int32, device=device)
+        self.uniforms = None
+        if cfg.sample:  # sampled verification: one uniform per node and round
+            from . import tensors as st
+            self.uniforms = torch.from_numpy(st.node_uniforms(cfg, round_id)).to(device)
         i8 = cfg.kv_dtype == I8
         self.vr = VerifyRound(
             T=cfg.T, HQ=cfg.HQ, HKV=cfg.HKV, D=cfg.D, V=cfg.V, kv_dtype=cfg.kv_dtype, w_dtype=cfg.w_dtype,
@@ -57,7 +61,7 @@ class Workload:
             window=tuple(cfg.layer_window(l) for l in range(L)) if cfg.window else None,
             q_in=self.q_in, k_new=[x["k_new"] for x in self.new_kv] if self.append else None,
             v_new=[x["v_new"] for x in self.new_kv] if self.append else None, rot_dim=cfg.rot_dim,
-            rope_base=cfg.rope_base)
+            rope_base=cfg.rope_base, sample=tuple(cfg.sample) if cfg.sample else None, uniforms=self.uniforms)
         self._tail = None
 
     def set_round(self, round_id: int):
@@ -67,6 +71,9 @@ class Workload:
         self.parents.copy_(torch.from_numpy(r["parents"]))
         self.tokens.copy_(torch.from_numpy(r["tokens"]))
         self.hidden.copy_(bits_to_bf16(r["hidden"], "cpu"))
+        if self.uniforms is not None:
+            from . import tensors as st
+            self.uniforms.copy_(torch.from_numpy(st.node_uniforms(self.cfg, round_id)))
 
     def save_tail(self):
         """Keep a pristine copy of the verify block [S, S+T) of every cache and of kv_len (the gather rewrites both).

@@ -167,3 +167,44 @@ def test_round_that_appends_its_block_full_size(gpu_lib, idx, rot_dim):
     assert rep["ok"], rep
     del wl, out
     _free()
+
+
+@pytest.mark.parametrize("idx", [1, 2])
+def test_sampled_round_full_size(gpu_lib, idx):
+    """Sampled verification at full vocabulary: each node's draw (temperature 1, top-k 20, top-p 0.95, its own
+    uniform) against the oracle's draw from its own fp64 logits; the walk on those draws.  The GPU logits differ
+    from the oracle's by fp32 accumulation (and the 4-bit head's fp16 dequantisation), so a draw may take any
+    value the oracle draws within 2e-3 of the node's uniform or of top_p."""
+    from oracle import lm_head as ol
+    from oracle import sampling as osm
+    from oracle import storage as osd
+    from oracle import tree as ot
+    from synth import tensors
+
+    from .parity import head_rows_fn
+
+    base = configs.CONFIGS[idx]
+    cfg = configs.scaled(base, name=base.name + "+sampled", sample=(1.0, 20, 0.95))
+    wl = Workload(cfg)
+    out = _run(wl)
+    r = wl.round
+    T = cfg.T
+    lg = ol.logits_streamed(head_rows_fn(cfg), osd.bf16(r["hidden"]), cfg.V)
+    u = tensors.node_uniforms(cfg, 0).astype(np.float64)
+    got = out["argmax"].cpu().numpy()
+    g_path = out["path"].cpu().numpy()
+    g_len = out["path_len"].cpu().numpy()
+    eps = 2e-3
+    for b in range(cfg.B):
+        exact = []
+        for i in range(T):
+            row = b * T + i
+            cands = {osm.draw(lg[row], 1.0, 20, pp, uu) for pp in (0.95 - eps, 0.95, 0.95 + eps)
+                     for uu in (max(0.0, u[row] - eps), u[row], min(1 - 1e-12, u[row] + eps))}
+            assert int(got[row]) in cands, (b, i, int(got[row]), cands)
+            exact.append(osm.draw(lg[row], 1.0, 20, 0.95, u[row]) if len(cands) == 1 else None)
+        if all(e is not None for e in exact):
+            path, em = ot.accept_walk(exact, r["tokens"][b], r["parents"][b])
+            assert g_len[b] == len(path) and g_path[b, :len(path)].tolist() == path
+    del wl, out
+    _free()

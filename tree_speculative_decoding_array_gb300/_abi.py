@@ -63,6 +63,9 @@ SIGNATURES = {
     "tsv_tree_verify_attention": (C.c_int, [C.POINTER(AttnDesc), _vp, _sz, _vp, _vp]),
     "tsv_lm_head_workspace_size": (_sz, [_i32, _i32, _i32, _i32]),
     "tsv_lm_head_argmax": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "tsv_lm_head_logits": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "tsv_sample_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "tsv_sample_nucleus": (C.c_int, [_vp, _i32, _i32, C.c_float, _i32, C.c_float, _vp, _vp, _vp, _sz, _vp]),
     "tsv_lm_head_argmax_noalloc": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "tsv_tree_accept_walk": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "tsv_kv_gather_positions": (C.c_int, [C.POINTER(KvDesc), _vp, _vp, _vp, _i32, _vp, _vp]),

@@ -174,6 +174,35 @@ def lm_head_argmax(hidden, W, argmax, *, w_dtype, V, scales=None, biases=None, m
                                  _p(maxlogit), _p(workspace), ws_bytes, _stream(stream)), "lm_head_argmax")
 
 
+def lm_head_logits(hidden, W, logits, *, w_dtype, V, scales=None, biases=None, workspace=None, stream=None):
+    """Every logit: hidden bf16 [rows, H] -> logits fp32 [rows, V]."""
+    lib = load()
+    rows, H = hidden.shape
+    _cuda(logits, "logits", torch.float32, (rows, V))
+    if workspace is None:
+        workspace = torch.empty(max(lm_head_workspace_size(rows, H, V, w_dtype), 256), dtype=torch.uint8,
+                                device=hidden.device)
+    check(lib.tsv_lm_head_logits(_p(hidden), rows, H, V, w_dtype, _p(W), _p(scales), _p(biases), _p(logits),
+                                 _p(workspace), workspace.numel(), _stream(stream)), "lm_head_logits")
+
+
+def sample_workspace_size(rows: int, V: int, top_k: int) -> int:
+    return int(load().tsv_sample_workspace_size(rows, V, top_k))
+
+
+def sample_nucleus(logits, uniforms, tokens, *, temperature, top_k, top_p, workspace=None, stream=None):
+    """Each row's draw from its nucleus-filtered distribution: logits fp32 [rows, V], uniforms fp32 [rows]."""
+    lib = load()
+    rows, V = logits.shape
+    _cuda(uniforms, "uniforms", torch.float32, (rows,))
+    _cuda(tokens, "tokens", torch.int32, (rows,))
+    if workspace is None:
+        workspace = torch.empty(max(sample_workspace_size(rows, V, top_k), 256), dtype=torch.uint8,
+                                device=logits.device)
+    check(lib.tsv_sample_nucleus(_p(logits), rows, V, float(temperature), int(top_k), float(top_p), _p(uniforms),
+                                 _p(tokens), _p(workspace), workspace.numel(), _stream(stream)), "sample_nucleus")
+
+
 # ----------------------------------------------------------------------------- a4 walk
 def tree_accept_walk(argmax, tokens, parents, path, path_len, emitted, dev_status=None, stream=None):
     lib = load()
@@ -248,6 +277,8 @@ class VerifyRound:
     v_new: list = None
     rot_dim: int = 0
     rope_base: float = 1e6
+    sample: tuple = None   # sampled verification (optional): (temperature, top_k, top_p)
+    uniforms: torch.Tensor = None  # fp32 [B * T], one per node
     outs: dict = field(default_factory=dict)
 
     def __post_init__(self):
@@ -272,6 +303,10 @@ class VerifyRound:
         self.attn_ws = torch.empty(max(attention_workspace_size(self.adesc), 256), dtype=torch.uint8, device=dev)
         self.lm_ws = torch.empty(max(lm_head_workspace_size(B * T, self.hidden.shape[1], self.V, self.w_dtype), 256),
                                  dtype=torch.uint8, device=dev)
+        if self.sample is not None:  # the LM stage writes every logit and draws each node's token
+            self.outs["logits"] = torch.empty(B * T, self.V, dtype=torch.float32, device=dev)
+            self.sample_ws = torch.empty(max(sample_workspace_size(B * T, self.V, int(self.sample[1])), 256),
+                                         dtype=torch.uint8, device=dev)
 
     def run(self, stream=None, stages=("mask", "append", "attn", "lm", "walk", "gather")):
         """Issue the round's calls in order; "append" runs only when the round was built with append inputs."""
@@ -283,9 +318,15 @@ class VerifyRound:
             tree_append(self.apdesc, self.kv_len, dev_status=o["status"], stream=stream)
         if "attn" in stages:
             tree_verify_attention(self.adesc, self.attn_ws, dev_status=o["status"], stream=stream)
-        if "lm" in stages:
+        if "lm" in stages and self.sample is None:
             lm_head_argmax(self.hidden, self.W, o["argmax"], w_dtype=self.w_dtype, V=self.V, scales=self.w_scales,
                            biases=self.w_biases, maxlogit=o["maxlogit"], workspace=self.lm_ws, stream=stream)
+        elif "lm" in stages:  # sampled verification: o["argmax"] receives each node's draw, the walk's input
+            t, k, p = self.sample
+            lm_head_logits(self.hidden, self.W, o["logits"], w_dtype=self.w_dtype, V=self.V, scales=self.w_scales,
+                           biases=self.w_biases, workspace=self.lm_ws, stream=stream)
+            sample_nucleus(o["logits"], self.uniforms, o["argmax"], temperature=t, top_k=k, top_p=p,
+                           workspace=self.sample_ws, stream=stream)
         if "walk" in stages:
             tree_accept_walk(o["argmax"].view(B, T), self.tokens, self.parents, o["path"], o["path_len"], o["emitted"],
                              dev_status=o["status"], stream=stream)

@@ -63,11 +63,25 @@ __device__ __forceinline__ void merge_best(const unsigned long long (&mine)[R], 
     if (threadIdx.x < R && r0 + (int)threadIdx.x < rows) atomicMax(&best[r0 + threadIdx.x], s_best[threadIdx.x]);
 }
 
+// Every logit to logits[row][v] (sampled verification): lane r writes hidden row r0 + r of vocabulary rows v
+// (a0) and v + 1 (a1, when has1); warp_sum left the sums in every lane.
+template <int R>
+__device__ __forceinline__ void store_logits(float* logits, const float (&a0)[R], const float (&a1)[R], bool has1,
+                                             int v, int V, int r0, int rows, int lane) {
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        if (lane == r && r0 + r < rows) {
+            logits[(size_t)(r0 + r) * V + v] = a0[r];
+            if (has1) logits[(size_t)(r0 + r) * V + v + 1] = a1[r];
+        }
+}
+
 // fp16 / bf16 weights [V, H]; hidden rows r0 .. r0 + R - 1.  H % 256 == 0.
 template <int R, bool BF16W>
 __global__ void __launch_bounds__(kLmThreads) lm_gemv16_kernel(const uint16_t* __restrict__ hidden, int rows, int H,
                                                                int V, const uint16_t* __restrict__ W,
-                                                               unsigned long long* __restrict__ best, int r0) {
+                                                               unsigned long long* __restrict__ best, int r0,
+                                                               float* __restrict__ logits) {
     extern __shared__ uint4 smem[];
     __shared__ unsigned long long s_best[8];
     uint4* hs = smem;  // [R][H/8]
@@ -124,6 +138,7 @@ __global__ void __launch_bounds__(kLmThreads) lm_gemv16_kernel(const uint16_t* _
         }
         warp_sum<R>(a0);
         warp_sum<R>(a1);
+        if (logits) store_logits<R>(logits, a0, a1, has1, v0, V, r0, rows, lane);
         if (lane == 0) {
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -148,7 +163,8 @@ __global__ void __launch_bounds__(kLmThreads) lm_gemv_q4_kernel(const uint16_t* 
                                                                 int V, const uint8_t* __restrict__ Wq,
                                                                 const uint16_t* __restrict__ scales,
                                                                 const uint16_t* __restrict__ biases,
-                                                                unsigned long long* __restrict__ best, int r0) {
+                                                                unsigned long long* __restrict__ best, int r0,
+                                                                float* __restrict__ logits) {
     extern __shared__ uint4 smem[];
     __shared__ unsigned long long s_best[8];
     const int nvec = H >> 5;  // 32-code vectors per row
@@ -208,6 +224,7 @@ __global__ void __launch_bounds__(kLmThreads) lm_gemv_q4_kernel(const uint16_t* 
             }
         }
         warp_sum<R>(acc);
+        if (logits) store_logits<R>(logits, acc, acc, false, v, V, r0, rows, lane);
         if (lane == 0)
 #pragma unroll
             for (int r = 0; r < R; ++r) {
@@ -229,20 +246,24 @@ __global__ void lm_unpack_kernel(const unsigned long long* __restrict__ best, in
 
 template <int R>
 static void launch_group(int grid, cudaStream_t st, const uint16_t* hidden, int rows, int H, int V, int w_dtype,
-                         const void* W, const void* scales, const void* biases, unsigned long long* best, int r0) {
+                         const void* W, const void* scales, const void* biases, unsigned long long* best, int r0,
+                         float* logits) {
     if (w_dtype == TSV_Q4_G64) {
         const size_t sm = (size_t)R * (H >> 3) * 16 + (size_t)R * (H >> 5) * 4;
         cudaFuncSetAttribute(lm_gemv_q4_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
         lm_gemv_q4_kernel<R><<<grid, kLmThreads, sm, st>>>(hidden, rows, H, V, (const uint8_t*)W,
-                                                           (const uint16_t*)scales, (const uint16_t*)biases, best, r0);
+                                                           (const uint16_t*)scales, (const uint16_t*)biases, best, r0,
+                                                           logits);
     } else {
         const size_t sm = (size_t)R * (H >> 3) * 16;
         if (w_dtype == TSV_BF16) {
             cudaFuncSetAttribute(lm_gemv16_kernel<R, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-            lm_gemv16_kernel<R, true><<<grid, kLmThreads, sm, st>>>(hidden, rows, H, V, (const uint16_t*)W, best, r0);
+            lm_gemv16_kernel<R, true><<<grid, kLmThreads, sm, st>>>(hidden, rows, H, V, (const uint16_t*)W, best, r0,
+                                                                    logits);
         } else {
             cudaFuncSetAttribute(lm_gemv16_kernel<R, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-            lm_gemv16_kernel<R, false><<<grid, kLmThreads, sm, st>>>(hidden, rows, H, V, (const uint16_t*)W, best, r0);
+            lm_gemv16_kernel<R, false><<<grid, kLmThreads, sm, st>>>(hidden, rows, H, V, (const uint16_t*)W, best, r0,
+                                                                     logits);
         }
     }
 }
@@ -254,7 +275,7 @@ namespace tsv {
 size_t lm_tc_extra_bytes(int rows, int H, int w_dtype);
 bool lm_tc_applies(int rows, int H, int V, int w_dtype);
 tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype, const void* W, const void* scales,
-                        const void* biases, unsigned long long* best, void* extra, cudaStream_t stream);
+                        const void* biases, unsigned long long* best, float* logits, void* extra, cudaStream_t stream);
 static size_t best_bytes(int rows) { return ((size_t)rows * sizeof(unsigned long long) + 255) & ~(size_t)255; }
 }  // namespace tsv
 
@@ -266,52 +287,76 @@ extern "C" size_t tsv_lm_head_workspace_size(int32_t rows, int32_t H, int32_t V,
     return n;
 }
 
-extern "C" tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32_t H, int32_t V, int32_t w_dtype,
-                                         const void* W, const void* scales, const void* biases, int32_t* argmax,
-                                         float* maxlogit, void* workspace, size_t ws_bytes, cudaStream_t stream) {
-    using namespace tsv;
-    clear_error();
-    if (rows < 1 || V < 1 || H < 64) return fail(TSV_EINVAL, "lm_head_argmax: rows=%d V=%d H=%d", rows, V, H);
-    if (!hidden || !W || !argmax || !workspace) return fail(TSV_EINVAL, "lm_head_argmax: null pointer argument");
+namespace tsv {
+
+// Shared body of tsv_lm_head_argmax (argmax != NULL) and tsv_lm_head_logits (logits != NULL).
+static tsv_status lm_head_run(const char* name, const void* hidden, int32_t rows, int32_t H, int32_t V,
+                              int32_t w_dtype, const void* W, const void* scales, const void* biases, int32_t* argmax,
+                              float* maxlogit, float* logits, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    if (rows < 1 || V < 1 || H < 64) return fail(TSV_EINVAL, "%s: rows=%d V=%d H=%d", name, rows, V, H);
+    if (!hidden || !W || !(argmax || logits) || !workspace) return fail(TSV_EINVAL, "%s: null pointer argument", name);
     if (w_dtype != TSV_F16 && w_dtype != TSV_BF16 && w_dtype != TSV_Q4_G64)
-        return fail(TSV_EUNSUPPORTED, "lm_head_argmax: weight format %d (fp16, bf16 or 4-bit group-64 only)", w_dtype);
+        return fail(TSV_EUNSUPPORTED, "%s: weight format %d (fp16, bf16 or 4-bit group-64 only)", name, w_dtype);
     if (w_dtype == TSV_Q4_G64) {
-        if (H % 64) return fail(TSV_EINVAL, "lm_head_argmax: H=%d not a multiple of the 64-wide group", H);
-        if (!scales || !biases) return fail(TSV_EINVAL, "lm_head_argmax: 4-bit head without scales/biases");
+        if (H % 64) return fail(TSV_EINVAL, "%s: H=%d not a multiple of the 64-wide group", name, H);
+        if (!scales || !biases) return fail(TSV_EINVAL, "%s: 4-bit head without scales/biases", name);
     } else if (H % 256) {
-        return fail(TSV_EINVAL, "lm_head_argmax: H=%d not a multiple of 256", H);
+        return fail(TSV_EINVAL, "%s: H=%d not a multiple of 256", name, H);
     }
-    if ((size_t)H * 17 > 200 * 1024) return fail(TSV_ECAPACITY, "lm_head_argmax: H=%d above the supported 12,000", H);
-    if (((uintptr_t)hidden | (uintptr_t)W) & 15) return fail(TSV_EINVAL, "lm_head_argmax: hidden/W not 16-byte aligned");
+    if ((size_t)H * 17 > 200 * 1024) return fail(TSV_ECAPACITY, "%s: H=%d above the supported 12,000", name, H);
+    if (((uintptr_t)hidden | (uintptr_t)W) & 15) return fail(TSV_EINVAL, "%s: hidden/W not 16-byte aligned", name);
     if (ws_bytes < best_bytes(rows))
-        return fail(TSV_ECAPACITY, "lm_head_argmax: workspace %zu < %zu bytes", ws_bytes, best_bytes(rows));
+        return fail(TSV_ECAPACITY, "%s: workspace %zu < %zu bytes", name, ws_bytes, best_bytes(rows));
     unsigned long long* best = (unsigned long long*)workspace;
     if (cudaMemsetAsync(best, 0, (size_t)rows * sizeof(unsigned long long), stream) != cudaSuccess)
-        return check_launch("lm_head_argmax(memset)");
+        return check_launch(name);
     // More than one 8-row pass: the tensor-core kernel, when the workspace also holds what it needs.
     const bool sb_aligned = w_dtype != TSV_Q4_G64 || ((((uintptr_t)scales | (uintptr_t)biases) & 15) == 0);
     if (lm_tc_applies(rows, H, V, w_dtype) && sb_aligned &&
         ws_bytes >= best_bytes(rows) + lm_tc_extra_bytes(rows, H, w_dtype)) {
-        tsv_status st = launch_lm_tc(hidden, rows, H, V, w_dtype, W, scales, biases, best,
+        tsv_status st = launch_lm_tc(hidden, rows, H, V, w_dtype, W, scales, biases, best, logits,
                                      (char*)workspace + best_bytes(rows), stream);
-        if (st != TSV_OK) return st;
+        if (st != TSV_OK || !argmax) return st;
         lm_unpack_kernel<<<(rows + 127) / 128, 128, 0, stream>>>(best, rows, argmax, maxlogit);
-        return check_launch("lm_head_argmax(unpack)");
+        return check_launch(name);
     }
     const int grid = sm_count() * 4;
     const uint16_t* hb = (const uint16_t*)hidden;
     for (int r0 = 0; r0 < rows;) {
         const int left = rows - r0;
-        if (left >= 8) { launch_group<8>(grid, stream, hb, rows, H, V, w_dtype, W, scales, biases, best, r0); r0 += 8; }
-        else if (left >= 4) { launch_group<4>(grid, stream, hb, rows, H, V, w_dtype, W, scales, biases, best, r0); r0 += 4; }
-        else if (left == 3) { launch_group<3>(grid, stream, hb, rows, H, V, w_dtype, W, scales, biases, best, r0); r0 += 3; }
-        else if (left == 2) { launch_group<2>(grid, stream, hb, rows, H, V, w_dtype, W, scales, biases, best, r0); r0 += 2; }
-        else { launch_group<1>(grid, stream, hb, rows, H, V, w_dtype, W, scales, biases, best, r0); r0 += 1; }
-        tsv_status st = check_launch("lm_head_argmax");
+        if (left >= 8) { launch_group<8>(grid, stream, hb, rows, H, V, w_dtype, W, scales, biases, best, r0, logits); r0 += 8; }
+        else if (left >= 4) { launch_group<4>(grid, stream, hb, rows, H, V, w_dtype, W, scales, biases, best, r0, logits); r0 += 4; }
+        else if (left == 3) { launch_group<3>(grid, stream, hb, rows, H, V, w_dtype, W, scales, biases, best, r0, logits); r0 += 3; }
+        else if (left == 2) { launch_group<2>(grid, stream, hb, rows, H, V, w_dtype, W, scales, biases, best, r0, logits); r0 += 2; }
+        else { launch_group<1>(grid, stream, hb, rows, H, V, w_dtype, W, scales, biases, best, r0, logits); r0 += 1; }
+        tsv_status st = check_launch(name);
         if (st != TSV_OK) return st;
     }
+    if (!argmax) return TSV_OK;
     lm_unpack_kernel<<<(rows + 127) / 128, 128, 0, stream>>>(best, rows, argmax, maxlogit);
-    return check_launch("lm_head_argmax(unpack)");
+    return check_launch(name);
+}
+
+}  // namespace tsv
+
+extern "C" tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32_t H, int32_t V, int32_t w_dtype,
+                                         const void* W, const void* scales, const void* biases, int32_t* argmax,
+                                         float* maxlogit, void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    using namespace tsv;
+    clear_error();
+    if (!argmax) return fail(TSV_EINVAL, "lm_head_argmax: null pointer argument");
+    return lm_head_run("lm_head_argmax", hidden, rows, H, V, w_dtype, W, scales, biases, argmax, maxlogit, nullptr,
+                       workspace, ws_bytes, stream);
+}
+
+extern "C" tsv_status tsv_lm_head_logits(const void* hidden, int32_t rows, int32_t H, int32_t V, int32_t w_dtype,
+                                         const void* W, const void* scales, const void* biases, float* logits,
+                                         void* workspace, size_t ws_bytes, cudaStream_t stream) {
+    using namespace tsv;
+    clear_error();
+    if (!logits) return fail(TSV_EINVAL, "lm_head_logits: null pointer argument");
+    return lm_head_run("lm_head_logits", hidden, rows, H, V, w_dtype, W, scales, biases, nullptr, nullptr, logits,
+                       workspace, ws_bytes, stream);
 }
 
 // ---------------------------------------------------------------------------

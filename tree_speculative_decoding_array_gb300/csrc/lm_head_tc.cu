@@ -49,9 +49,10 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 }
 
 // Argmax of one accumulator tile over this warp's 32 vocabulary rows, for each of the nrows hidden rows
-// (TMEM columns starting at taddr).  v = this lane's vocabulary row; rows >= V never win.
+// (TMEM columns starting at taddr).  v = this lane's vocabulary row; rows >= V never win.  With logits != NULL
+// every logit is also written to logits[row0 + column][v] (sampled verification).
 __device__ __forceinline__ void lm_epilogue_tile(uint32_t taddr, int nrows, int v, int V,
-                                                 unsigned long long* s_best, int lane) {
+                                                 unsigned long long* s_best, int lane, float* logits, int row0) {
     const uint32_t v0 = (uint32_t)(v - lane);
     for (int c0 = 0; c0 < nrows; c0 += 32) {
         uint32_t d[32];
@@ -60,6 +61,7 @@ __device__ __forceinline__ void lm_epilogue_tile(uint32_t taddr, int nrows, int 
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
             if (c0 + k < nrows) {  // uniform across the warp
+                if (logits && v < V) logits[(size_t)(row0 + c0 + k) * V + v] = __uint_as_float(d[k]);
                 const uint32_t o = v < V ? orderable(__uint_as_float(d[k])) : 0u;
                 const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, o);
                 const uint32_t who = __ballot_sync(0xFFFFFFFFu, o == mx);
@@ -87,6 +89,7 @@ struct LmTcParams {
     CUtensorMap wmap;
     CUtensorMap hmap;
     unsigned long long* best;
+    float* logits;  // NULL, or [rows][V] fp32 written by the epilogue
     int rows, H, V, NP, nchunks, vtiles, mma_bf16, stages, stage_bytes;
 };
 
@@ -195,7 +198,8 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
             const int buf = it & 1;
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, 1024))) break;
             tc::tc_fence_after();
-            lm_epilogue_tile(tmem + lane_base + buf * 256, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane);
+            lm_epilogue_tile(tmem + lane_base + buf * 256, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane,
+                             p.logits, chunk * p.NP);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
@@ -229,6 +233,7 @@ struct LmQ4Params {
     CUtensorMap bmap;  // biases, same
     CUtensorMap hmap;  // fp16 hidden copy in converter feature order, UINT16 [rows][H], box {64, NP}, swizzled
     unsigned long long* best;
+    float* logits;     // NULL, or [rows][V] fp32 written by the epilogue
     int rows, H, V, NP, DC, NA, HS, nchunks, vtiles;
 };
 
@@ -455,7 +460,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
             const int buf = it & 1;
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, 1024))) break;
             tc::tc_fence_after();
-            lm_epilogue_tile(tmem + lane_base + buf * p.DC, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane);
+            lm_epilogue_tile(tmem + lane_base + buf * p.DC, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane,
+                             p.logits, chunk * p.NP);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
@@ -539,7 +545,8 @@ bool lm_tc_applies(int rows, int H, int V, int w_dtype) {
 }
 
 static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const void* W, const void* scales,
-                               const void* biases, unsigned long long* best, void* extra, cudaStream_t stream) {
+                               const void* biases, unsigned long long* best, float* logits, void* extra,
+                               cudaStream_t stream) {
     static thread_local LmQ4Params prm;
     const int nchunks = (rows + kQ4MaxNP - 1) / kQ4MaxNP;
     int NP = (rows + nchunks - 1) / nchunks;
@@ -566,6 +573,7 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
                      64, (uint32_t)NP, true);
     if (!ok) return fail(TSV_ECUDA, "lm_head_argmax: tensor map encoding failed");
     prm.best = best;
+    prm.logits = logits;
     prm.rows = rows;
     prm.H = H;
     prm.V = V;
@@ -583,8 +591,8 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
 }
 
 tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype, const void* W, const void* scales,
-                        const void* biases, unsigned long long* best, void* extra, cudaStream_t stream) {
-    if (w_dtype == TSV_Q4_G64) return launch_lm_q4(hidden, rows, H, V, W, scales, biases, best, extra, stream);
+                        const void* biases, unsigned long long* best, float* logits, void* extra, cudaStream_t stream) {
+    if (w_dtype == TSV_Q4_G64) return launch_lm_q4(hidden, rows, H, V, W, scales, biases, best, logits, extra, stream);
     static thread_local LmTcParams prm;
     const int nchunks = (rows + 255) / 256;
     int NP = (rows + nchunks - 1) / nchunks;
@@ -603,6 +611,7 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
                      (uint32_t)NP, true);
     if (!ok) return fail(TSV_ECUDA, "lm_head_argmax: tensor map encoding failed");
     prm.best = best;
+    prm.logits = logits;
     prm.rows = rows;
     prm.H = H;
     prm.V = V;
