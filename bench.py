@@ -148,7 +148,9 @@ def run_ours(args, rank, world, local_rank):
     wl.save_tail()
     moved = any(p != list(range(len(p))) for p in wl.round["paths"])
     stream = torch.cuda.current_stream()
-    names = ["mask"] + (["append"] if cfg.rot_dim > 0 else []) + ["attn", "lm", "walk", "gather"]
+    names = (["build"] if args.build_tree else []) + ["mask"] + (["append"] if cfg.rot_dim > 0 else []) + \
+        ["attn", "lm", "walk", "gather"]
+    build = make_build_stage(cfg, args.build_tree, dev) if args.build_tree else None
 
     def reset():  # one launch: pristine tails of every cache and kv_len (S + T; S when the round appends)
         wl.restore_tail()
@@ -158,7 +160,10 @@ def run_ours(args, rank, world, local_rank):
         for i, n in enumerate(names):
             if evs is not None:
                 evs[i][0].record(stream)
-            vr.run(stages=(n,))
+            if n == "build":
+                build()
+            else:
+                vr.run(stages=(n,))
             if evs is not None:
                 evs[i][1].record(stream)
 
@@ -217,8 +222,58 @@ def run_ours(args, rank, world, local_rank):
             n = ch * min(int(cfg.sample[1]), cfg.V)
         lm_launches += passes + 1 - 1
     launches = 1 + (1 + (tsv.attention_workspace_size(vr.adesc) > 0)) + lm_launches + 1 + 2 + (2 if cfg.rot_dim > 0 else 0)
+    if args.build_tree:  # draft children: top-k passes + output; selection: one
+        n, passes = cfg.V, 0
+        while True:
+            passes += 1
+            ch = (n + 4095) // 4096
+            if ch == 1:
+                break
+            n = ch * args.build_tree
+        launches += passes + 1 + 1
     return dict(cfg=cfg, ms=ms, per_kernel=per_kernel, clocks=clk.summary(), e2e=e2e, launches=launches,
                 round_id=round_id)
+
+
+def make_build_stage(cfg, k, dev):
+    """Tree construction on synthetic drafter output: every node of the round's B trees is expanded (drafter
+    logits [B*T, V], N(0, 1) bf16 values widened to fp32), its top-k children become candidates, and the best-first
+    selection picks T of the 1 + T*k candidates per sequence.  The verify stages keep the planted trees (the round
+    stays checkable); this stage is timed beside them."""
+    import torch
+
+    import tree_speculative_decoding_array_gb300 as tsv
+    from synth import device as sd
+    from synth import tensors as st
+
+    B, T, V = cfg.B, cfg.T, cfg.V
+    lg16 = torch.empty(B * T, V, dtype=torch.bfloat16, device=dev)
+    sd.fill(lg16, sd.NORMAL_BF16, st.key(cfg, st.KIND_DRAFT), (1, 1, B * T, V), (0, 0, V))
+    logits = lg16.float()
+    del lg16
+    toks = torch.empty(B * T, k, dtype=torch.int32, device=dev)
+    lps = torch.empty(B * T, k, dtype=torch.float32, device=dev)
+    ws = torch.empty(max(int(tsv.load().tsv_draft_children_workspace_size(B * T, V, k)), 256), dtype=torch.uint8,
+                     device=dev)
+    N = 1 + T * k
+    par = torch.empty(B, N, dtype=torch.int32)
+    par[:, 0] = -1
+    for m in range(T):  # children of the m-th expanded candidate (0 = the root, then candidates 1, 2, ...)
+        par[:, 1 + m * k:1 + (m + 1) * k] = m
+    par = par.to(dev)
+    ctok = torch.zeros(B, N, dtype=torch.int32, device=dev)
+    clp = torch.zeros(B, N, dtype=torch.float32, device=dev)
+    outs = [torch.empty(B, T, dtype=torch.int32, device=dev) for _ in range(3)]
+    sizes = torch.empty(B, dtype=torch.int32, device=dev)
+
+    def build():
+        tsv.draft_children(logits, toks, lps, top_k=k, workspace=ws)
+        # candidates 1 + m*k + j of sequence b are child j of its node m (a strided view: no extra copy kernel
+        # of ours runs; torch's copy is the only non-tsv launch of the stage)
+        clp[:, 1:].copy_(lps.view(B, T * k))
+        ctok[:, 1:].copy_(toks.view(B, T * k))
+        tsv.tree_select(par, ctok, clp, *outs, sizes, depth_max=cfg.depth_max or T)
+    return build
 
 
 def run_e2e(args, wl, stream):
@@ -351,6 +406,9 @@ def main():
     ap.add_argument("--sampled", default=None, metavar="T:K:P",
                     help="sampled verification: the LM stage writes every logit and draws each node's token at "
                          "temperature T from the top-K, top-P nucleus (e.g. 1:20:0.95)")
+    ap.add_argument("--build-tree", type=int, default=0, metavar="K",
+                    help="> 0: time a tree-construction stage first: the drafter's top-K children of every node "
+                         "(drafter logits [B*T, V]) and the best-first selection of T nodes from 1 + T*K candidates")
     ap.add_argument("--layers", type=int, default=None,
                     help="attention layers (default: the workload's); fewer only for small profiler captures")
     args = ap.parse_args()
@@ -435,7 +493,7 @@ def main():
     }
     if args.sliding:
         config["sliding"] = {"window": int(args.sliding.split(":")[0]), "every": int(args.sliding.split(":")[1])}
-    if not args.no_cpu_baseline and not args.sliding and not args.append and not args.sampled:
+    if not args.no_cpu_baseline and not args.sliding and not args.append and not args.sampled and not args.build_tree:
         try:
             o = run_oracle(args.config, r["round_id"])
             line["cpu_baseline"] = {"value": o["nodes_per_s"], "unit": "nodes/s", "cores": 1, "kind": "oracle",

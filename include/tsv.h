@@ -77,6 +77,7 @@ typedef enum {
 #define TSV_DEV_TIMEOUT 5     /* a bounded wait inside a kernel expired (a library bug; outputs unspecified) */
 
 #define TSV_MAX_T 64
+#define TSV_MAX_CANDIDATES 1024 /* candidate-tree nodes per sequence for tsv_tree_select */
 #define TSV_MAX_LAYERS 64
 
 /* Reason for the last non-TSV_OK status returned on this thread ("" if none). */
@@ -123,6 +124,41 @@ tsv_status tsv_tree_mask(const int32_t* parents, int32_t B, int32_t T, uint64_t*
  */
 tsv_status tsv_sliding_band_mask(float* dense_mask, int32_t B, int32_t T, int32_t mask_offset, int32_t window,
                                  cudaStream_t stream);
+
+/*
+ * Building the draft tree from the drafter's confidence (two calls).
+ *   [1204] "What this needs", the fourth decision: EAGLE-2 branches by the
+ *   drafter's confidence, which needs the drafter's logits; [1212], the
+ *   draft_tree commit: the runner-up at an uncertain step is the alternative
+ *   worth a verify position; [728] "What it does": the chain plus likely
+ *   alternatives from the draft's top-k selector.
+ *
+ * tsv_draft_children - for every expanded node (row of drafter logits
+ *   [rows, V] fp32), its top_k tokens (ties to the lower index) and their
+ *   log-probabilities log_softmax(logits)[token]: child_tokens int32 and
+ *   child_logp float, [rows, top_k], largest first.  1 <= top_k <= min(64, V).
+ * tsv_tree_select - the verified tree from a candidate tree (reading: the
+ *   root plus the T - 1 candidates of highest cumulative log-probability,
+ *   summed in fp32 from the root down, depth <= depth_max, ties to the earlier
+ *   candidate - what best-first expansion by path probability selects).
+ *   cand_parents int32 [B, N] (topological: [b][0] = -1, 0 <= [b][i] < i),
+ *   cand_tokens int32 [B, N], cand_logp float [B, N] (log-probability of the
+ *   candidate given its parent, <= 0; the root's is ignored).  N <= 1024.
+ *   Out: parents, tokens, cand_index int32 [B, T] in selection order (descending
+ *   score, so topological; the root first), sizes int32 [B] = nodes chosen
+ *   (< T when fewer candidates qualify; the rest of the row is -1).
+ *   Device errors: TSV_DEV_BAD_ROOT / TSV_DEV_BAD_PARENT for a candidate tree
+ *   that is not topological (that sequence's outputs are -1, size 0) or whose
+ *   chosen node's parent was not chosen (a log-probability above 0).
+ */
+size_t tsv_draft_children_workspace_size(int32_t rows, int32_t V, int32_t top_k);
+
+tsv_status tsv_draft_children(const float* draft_logits, int32_t rows, int32_t V, int32_t top_k, int32_t* child_tokens,
+                              float* child_logp, void* workspace, size_t ws_bytes, cudaStream_t stream);
+
+tsv_status tsv_tree_select(const int32_t* cand_parents, const int32_t* cand_tokens, const float* cand_logp, int32_t B,
+                           int32_t N, int32_t T, int32_t depth_max, int32_t* parents, int32_t* tokens,
+                           int32_t* cand_index, int32_t* sizes, int32_t* dev_status, cudaStream_t stream);
 
 /*
  * Tree-masked GQA attention of the verify block, for n_layers layers at once.

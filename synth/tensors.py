@@ -35,6 +35,7 @@ KIND_Q, KIND_K, KIND_V, KIND_KS, KIND_VS, KIND_W, KIND_WQ, KIND_WS, KIND_WB, KIN
 KIND_TREE, KIND_TOK = 11, 12
 KIND_KNEW, KIND_VNEW = 13, 14  # the block's K and V rows before the append (K not yet rotated)
 KIND_U = 15  # per-node uniforms of sampled verification
+KIND_DRAFT = 16  # synthetic drafter logits (tree construction)
 
 W_SIGMA = np.float32(0.02)
 KV_SCALE_LO, KV_SCALE_W = np.float32(0.005), np.float32(0.045)

@@ -16,6 +16,7 @@ F16, BF16, I8_SCALED, Q4_G64 = range(4)
 DEV_OK, DEV_BAD_ROOT, DEV_BAD_PARENT, DEV_BAD_PATH, DEV_BAD_KV_LEN, DEV_TIMEOUT = range(6)
 ATTN_AUTO, ATTN_SIMT, ATTN_TCGEN05 = range(3)
 MAX_T = 64
+MAX_CANDIDATES = 1024
 MAX_LAYERS = 64
 NOALLOC_MAX_ROWS = 4096
 
@@ -59,6 +60,9 @@ SIGNATURES = {
     "tsv_version": (C.c_int, []),
     "tsv_tree_mask": (C.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp]),
     "tsv_sliding_band_mask": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp]),
+    "tsv_draft_children_workspace_size": (_sz, [_i32, _i32, _i32]),
+    "tsv_draft_children": (C.c_int, [_vp, _i32, _i32, _i32, _vp, _vp, _vp, _sz, _vp]),
+    "tsv_tree_select": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "tsv_attention_workspace_size": (_sz, [C.POINTER(AttnDesc)]),
     "tsv_tree_verify_attention": (C.c_int, [C.POINTER(AttnDesc), _vp, _sz, _vp, _vp]),
     "tsv_lm_head_workspace_size": (_sz, [_i32, _i32, _i32, _i32]),

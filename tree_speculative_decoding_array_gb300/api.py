@@ -62,6 +62,36 @@ def sliding_band_mask(dense_mask, mask_offset, window, stream=None):
           "sliding_band_mask")
 
 
+def draft_children(draft_logits, child_tokens, child_logp, *, top_k, workspace=None, stream=None):
+    """Top-k children of every expanded node: draft_logits fp32 [rows, V] -> tokens int32, logp fp32 [rows, k]."""
+    lib = load()
+    rows, V = draft_logits.shape
+    _cuda(draft_logits, "draft_logits", torch.float32, (rows, V))
+    _cuda(child_tokens, "child_tokens", torch.int32, (rows, top_k))
+    _cuda(child_logp, "child_logp", torch.float32, (rows, top_k))
+    if workspace is None:
+        workspace = torch.empty(max(int(lib.tsv_draft_children_workspace_size(rows, V, top_k)), 256),
+                                dtype=torch.uint8, device=draft_logits.device)
+    check(lib.tsv_draft_children(_p(draft_logits), rows, V, int(top_k), _p(child_tokens), _p(child_logp),
+                                 _p(workspace), workspace.numel(), _stream(stream)), "draft_children")
+
+
+def tree_select(cand_parents, cand_tokens, cand_logp, parents, tokens, cand_index, sizes, *, depth_max,
+                dev_status=None, stream=None):
+    """Verified tree [B, T] from a candidate tree [B, N] by cumulative drafter log-probability."""
+    B, N = cand_parents.shape
+    T = parents.shape[1]
+    for t, name, dt, shape in ((cand_parents, "cand_parents", torch.int32, (B, N)),
+                               (cand_tokens, "cand_tokens", torch.int32, (B, N)),
+                               (cand_logp, "cand_logp", torch.float32, (B, N)), (parents, "parents", torch.int32, (B, T)),
+                               (tokens, "tokens", torch.int32, (B, T)), (cand_index, "cand_index", torch.int32, (B, T)),
+                               (sizes, "sizes", torch.int32, (B,))):
+        _cuda(t, name, dt, shape)
+    check(load().tsv_tree_select(_p(cand_parents), _p(cand_tokens), _p(cand_logp), B, N, T, int(depth_max),
+                                 _p(parents), _p(tokens), _p(cand_index), _p(sizes), _p(dev_status), _stream(stream)),
+          "tree_select")
+
+
 # ----------------------------------------------------------------------------- a2 attention
 def attn_desc(q, k, v, o, kv_len, anc, *, T, HQ, HKV, D, kv_dtype, max_kv_len, k_scale=None, v_scale=None,
               splits=0, path=0, window=None) -> AttnDesc:

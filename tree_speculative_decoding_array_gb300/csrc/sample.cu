@@ -41,10 +41,14 @@ __device__ __forceinline__ void cx(unsigned long long& a, unsigned long long& b)
 // input is the row's fp32 logits [n]; else packed keys [n] from an earlier pass.  Each warp sorts its lanes'
 // 8 keys, takes its own top K by K rounds of a warp maximum (the winning lane pops its head), and warp 0 merges
 // the 16 warps' sorted lists the same way.
+// With lse_part != NULL (the first pass over logits) each CTA also writes its chunk's (max, sum of exp(x - max))
+// to lse_part[row][chunk], for log-probabilities.
 template <bool FROM_LOGITS>
 __global__ void __launch_bounds__(kSortThreads) topk_chunk_kernel(const void* __restrict__ in, int n, int K,
-                                                                  unsigned long long* __restrict__ out) {
+                                                                  unsigned long long* __restrict__ out,
+                                                                  float2* __restrict__ lse_part) {
     __shared__ unsigned long long wtop[kSortThreads / 32][kMaxTopK];
+    __shared__ float2 wlse[kSortThreads / 32];
     const int row = blockIdx.y, ch = blockIdx.x;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const size_t base = (size_t)row * n;
@@ -58,6 +62,33 @@ __global__ void __launch_bounds__(kSortThreads) topk_chunk_kernel(const void* __
             else key = reinterpret_cast<const unsigned long long*>(in)[base + e];
         }
         a[j] = key;
+    }
+    if (FROM_LOGITS && lse_part) {  // this chunk's (max, sum exp(x - max)); padding keys (0) are not logits
+        float m = -INFINITY, sum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (a[j] != 0ull) m = fmaxf(m, unorderable((uint32_t)(a[j] >> 32)));
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+            if (a[j] != 0ull && m != -INFINITY) sum += expf(unorderable((uint32_t)(a[j] >> 32)) - m);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o), s2 = __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+            const float mm = fmaxf(m, m2);
+            sum = (m == -INFINITY ? 0.f : sum * expf(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * expf(m2 - mm));
+            m = mm;
+        }
+        if (lane == 0) wlse[warp] = make_float2(m, sum);
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            float M = -INFINITY, S = 0.f;
+            for (int w = 0; w < kSortThreads / 32; ++w) {
+                const float mm = fmaxf(M, wlse[w].x);
+                S = (M == -INFINITY ? 0.f : S * expf(M - mm)) + (wlse[w].x == -INFINITY ? 0.f : wlse[w].y * expf(wlse[w].x - mm));
+                M = mm;
+            }
+            lse_part[(size_t)row * gridDim.x + ch] = make_float2(M, S);
+        }
     }
     // sorting network for 8 keys, descending
     cx(a[0], a[1]); cx(a[2], a[3]); cx(a[4], a[5]); cx(a[6], a[7]);
@@ -158,13 +189,14 @@ extern "C" tsv_status tsv_sample_nucleus(const float* logits, int32_t rows, int3
     unsigned long long* buf[2] = {(unsigned long long*)workspace, (unsigned long long*)((char*)workspace + need / 2)};
     int cur = 0;
     int nch = chunks_of(V);
-    topk_chunk_kernel<true><<<dim3(nch, rows), kSortThreads, 0, stream>>>(logits, V, K, buf[cur]);
+    topk_chunk_kernel<true><<<dim3(nch, rows), kSortThreads, 0, stream>>>(logits, V, K, buf[cur], nullptr);
     tsv_status st = check_launch("sample_nucleus(top-k)");
     if (st != TSV_OK) return st;
     long long n = (long long)nch * K;  // survivors per row
     while (nch > 1) {
         nch = chunks_of(n);
-        topk_chunk_kernel<false><<<dim3(nch, rows), kSortThreads, 0, stream>>>(buf[cur], (int)n, K, buf[cur ^ 1]);
+        topk_chunk_kernel<false><<<dim3(nch, rows), kSortThreads, 0, stream>>>(buf[cur], (int)n, K, buf[cur ^ 1],
+                                                                              nullptr);
         st = check_launch("sample_nucleus(top-k merge)");
         if (st != TSV_OK) return st;
         cur ^= 1;
@@ -173,4 +205,83 @@ extern "C" tsv_status tsv_sample_nucleus(const float* logits, int32_t rows, int3
     nucleus_draw_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(buf[cur], rows, K, 1.f / temperature, top_p, uniforms,
                                                             tokens);
     return check_launch("sample_nucleus(draw)");
+}
+
+// ---------------------------------------------------------------------------
+// tsv_draft_children: the drafter's candidate children of every expanded
+// node - its top_k tokens and their log-probabilities log_softmax(logits) -
+// the confidence signal the draft tree branches on (mlxcel issue #1204, "What
+// this needs", the fourth decision: EAGLE-2 branches by drafter confidence).
+// ---------------------------------------------------------------------------
+namespace tsv {
+
+// One warp per row: log(sum exp(x)) from the chunks' (max, sum) partials, then the row's K children.
+__global__ void draft_children_kernel(const unsigned long long* __restrict__ top, const float2* __restrict__ lse_part,
+                                      int nch, int rows, int K, int32_t* __restrict__ tokens, float* __restrict__ logp) {
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (row >= rows) return;
+    float m = -INFINITY, sum = 0.f;
+    for (int c = lane; c < nch; c += 32) {
+        const float2 p = lse_part[(size_t)row * nch + c];
+        const float mm = fmaxf(m, p.x);
+        sum = (m == -INFINITY ? 0.f : sum * expf(m - mm)) + (p.x == -INFINITY ? 0.f : p.y * expf(p.x - mm));
+        m = mm;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xFFFFFFFFu, m, o), s2 = __shfl_xor_sync(0xFFFFFFFFu, sum, o);
+        const float mm = fmaxf(m, m2);
+        sum = (m == -INFINITY ? 0.f : sum * expf(m - mm)) + (m2 == -INFINITY ? 0.f : s2 * expf(m2 - mm));
+        m = mm;
+    }
+    const float lse = m + logf(sum);
+    for (int j = lane; j < K; j += 32) {
+        const unsigned long long key = top[(size_t)row * K + j];
+        tokens[(size_t)row * K + j] = (int32_t)(0xFFFFFFFFu - (uint32_t)(key & 0xFFFFFFFFull));
+        logp[(size_t)row * K + j] = unorderable((uint32_t)(key >> 32)) - lse;
+    }
+}
+
+}  // namespace tsv
+
+extern "C" size_t tsv_draft_children_workspace_size(int32_t rows, int32_t V, int32_t top_k) {
+    const size_t base = tsv_sample_workspace_size(rows, V, top_k);
+    return base ? base + (((size_t)rows * tsv::chunks_of(V) * sizeof(float2) + 255) & ~(size_t)255) : 0;
+}
+
+extern "C" tsv_status tsv_draft_children(const float* draft_logits, int32_t rows, int32_t V, int32_t top_k,
+                                         int32_t* child_tokens, float* child_logp, void* workspace, size_t ws_bytes,
+                                         cudaStream_t stream) {
+    using namespace tsv;
+    clear_error();
+    if (rows < 1 || rows > 65535 || V < 1) return fail(TSV_EINVAL, "draft_children: rows=%d (1..65535) V=%d", rows, V);
+    if (top_k < 1 || top_k > kMaxTopK || top_k > V)
+        return fail(TSV_EUNSUPPORTED, "draft_children: top_k=%d outside [1, min(%d, V)]", top_k, kMaxTopK);
+    if (!draft_logits || !child_tokens || !child_logp || !workspace)
+        return fail(TSV_EINVAL, "draft_children: null pointer argument");
+    const size_t need = tsv_draft_children_workspace_size(rows, V, top_k);
+    if (ws_bytes < need) return fail(TSV_ECAPACITY, "draft_children: workspace %zu < %zu bytes", ws_bytes, need);
+    const size_t half = tsv_sample_workspace_size(rows, V, top_k) / 2;
+    unsigned long long* buf[2] = {(unsigned long long*)workspace, (unsigned long long*)((char*)workspace + half)};
+    float2* lse_part = (float2*)((char*)workspace + 2 * half);
+    const int K = top_k;
+    const int nch0 = chunks_of(V);
+    int cur = 0, nch = nch0;
+    topk_chunk_kernel<true><<<dim3(nch, rows), kSortThreads, 0, stream>>>(draft_logits, V, K, buf[cur], lse_part);
+    tsv_status st = check_launch("draft_children(top-k)");
+    if (st != TSV_OK) return st;
+    long long n = (long long)nch * K;
+    while (nch > 1) {
+        nch = chunks_of(n);
+        topk_chunk_kernel<false><<<dim3(nch, rows), kSortThreads, 0, stream>>>(buf[cur], (int)n, K, buf[cur ^ 1],
+                                                                              nullptr);
+        st = check_launch("draft_children(top-k merge)");
+        if (st != TSV_OK) return st;
+        cur ^= 1;
+        n = (long long)nch * K;
+    }
+    draft_children_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(buf[cur], lse_part, nch0, rows, K, child_tokens,
+                                                              child_logp);
+    return check_launch("draft_children");
 }
