@@ -34,6 +34,7 @@ struct AttnGeom {
 // Defined in attention_tc.cu.
 bool tc_supported(const tsv_attn_desc* d);
 int tc_mtiles(const tsv_attn_desc* d);
+bool tc_wide(const tsv_attn_desc* d);
 tsv_status launch_tc(const tsv_attn_desc* d, int splits, int chunk, float* ws_o, float* ws_ml, int32_t* status,
                      cudaStream_t stream);
 
@@ -44,7 +45,8 @@ static AttnGeom attn_geom(const tsv_attn_desc* d) {
     g.rgs = (g.rows_unit + kRB - 1) / kRB;
     g.path = (d->path == TSV_ATTN_TCGEN05 || (d->path == TSV_ATTN_AUTO && tc_supported(d))) ? TSV_ATTN_TCGEN05
                                                                                            : TSV_ATTN_SIMT;
-    const int key_tile = g.path == TSV_ATTN_TCGEN05 ? 64 : kBK;
+    // key tiles: 128 for the tcgen05 128-key kernel, 64 for its 64-key kernels, kBK for the CUDA cores
+    const int key_tile = g.path == TSV_ATTN_TCGEN05 ? (tc_wide(d) ? 128 : 64) : kBK;
     int s = d->splits;
     if (s <= 0) {
         const int cap_s = (d->max_kv_len + 255) / 256 < 64 ? (d->max_kv_len + 255) / 256 : 64;

@@ -570,6 +570,381 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
     }
 }
 
+// ------------------------------------------------------------------ 16-bit caches: 128-key score tiles
+// Q K^T over 128 keys per MMA (N = 128): an MMA occupies the tensor pipe for about 100 cycles whatever N <= 128
+// is, so 128-key tiles halve the Q K^T issue cost per key of the 64-key design above.  P V still runs over
+// 64-key halves (V stages of 64 keys, P written half by half, so P V of the first half starts while the
+// second is being written).  TMEM: Q [0, 128), S [128, 256) (one buffer: the softmax frees it right after
+// reading it), O [256, 512).  Shared memory: K stages [2 x 64 KB] at 0 (layout [64-dim block][128 keys][128 B]),
+// V stages [2 x 32 KB] at 128 KB, P [2 halves x 16 KB] at 192 KB, barriers at 224 KB.
+constexpr int kWK = 128;
+constexpr uint32_t kWKTile = kWK * kTcD * 2;  // 64 KiB
+constexpr int kWSmem = 1024 + 229376 + 512;
+
+__global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_constant__ TcParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sK = sm;
+    uint8_t* sV = sm + 131072;
+    uint8_t* sP = sm + 196608;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 229376);
+    uint64_t* kfull = bars + 0;   // [2] 128-key K tile landed
+    uint64_t* kempty = bars + 2;  // [2] Q K^T done with it
+    uint64_t* vfull = bars + 4;   // [2] 64-key V half landed
+    uint64_t* vempty = bars + 6;  // [2] P V done with it
+    uint64_t* s_full = bars + 8;
+    uint64_t* s_free = bars + 9;
+    uint64_t* p_full = bars + 10;  // [2] P half written (4 softmax warps)
+    uint64_t* p_free = bars + 12;  // [2] P V done with the P half
+    uint64_t* o_done = bars + 14;
+    uint64_t* q_full = bars + 15;
+    uint64_t* drain = bars + 16;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 18);
+    constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int item = blockIdx.x;
+    const int mt = item % p.mtiles;
+    item /= p.mtiles;
+    const int split = item % p.splits;
+    const int unit = item / p.splits;
+    const int kvh = unit % p.HKV;
+    const int b = (unit / p.HKV) % p.B;
+    const int layer = unit / (p.HKV * p.B);
+    const int T = p.T;
+    const int kvl = p.kv_len[b];
+    if (kvl < T || kvl > p.max_kv_len || (int64_t)kvl > p.s_cap) {
+        if (split == 0 && mt == 0 && kvh == 0 && layer == 0 && threadIdx.x == 0)
+            dev_fail(p.status, TSV_DEV_BAD_KV_LEN, b, kvl);
+        return;
+    }
+    const int S = kvl - T;
+    const int row0 = mt * kTcRows;
+    const int k_end = min(kvl, split * p.chunk + p.chunk);
+    const int win = p.window[layer];
+    const int lo_first = win > 0 ? S + row0 / p.G - win + 1 : INT_MIN;
+    const int lo_last = win > 0 ? S + (min(p.R, row0 + kTcRows) - 1) / p.G - win + 1 : INT_MIN;
+    int k_begin = split * p.chunk;
+    if (lo_first > k_begin) k_begin += ((lo_first - k_begin) / kWK) * kWK;
+    const int ntiles = k_end > k_begin ? (k_end - k_begin + kWK - 1) / kWK : 0;  // 128-key tiles
+    const int nhalves = 2 * ntiles;
+
+    if (p.status != nullptr && *reinterpret_cast<volatile int32_t*>(p.status) == TSV_DEV_TIMEOUT) return;
+    if (ntiles == 0) {
+        if (threadIdx.x < kTcRows && row0 + (int)threadIdx.x < p.R) {
+            const size_t slot = ((size_t)unit * p.splits + split) * p.R + row0 + threadIdx.x;
+            p.ws_ml[2 * slot] = -INFINITY;
+            p.ws_ml[2 * slot + 1] = 0.f;
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&kfull[s], 1);
+            tc::mbar_init(&kempty[s], 1);
+            tc::mbar_init(&vfull[s], 1);
+            tc::mbar_init(&vempty[s], 1);
+            tc::mbar_init(&p_full[s], 4);
+            tc::mbar_init(&p_free[s], 1);
+        }
+        tc::mbar_init(s_full, 1);
+        tc::mbar_init(s_free, 4);
+        tc::mbar_init(o_done, 1);
+        tc::mbar_init(q_full, 4);
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 5) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4 || warp == 6) {
+        // ------------------------------------------------------------ TMA producers: warp 4 K tiles, warp 6 V halves
+        if (lane == 0) {
+            const bool isK = warp == 4;
+            const CUtensorMap* m = isK ? &p.kmap[layer] : &p.vmap[layer];
+            uint64_t* fullb = isK ? kfull : vfull;
+            uint64_t* emptyb = isK ? kempty : vempty;
+            tc::tma_prefetch_desc(m);
+            const int rowbase = (int)(((int64_t)b * p.HKV + kvh) * p.s_cap + k_begin);
+            const int n = isK ? ntiles : nhalves;
+            int issued = 0;
+            for (int j = 0; j < n; ++j) {
+                const int st = j & 1;
+                if (j >= 2 && !tc::mbar_wait(&emptyb[st], ((j >> 1) - 1) & 1, abort_flag, 256)) break;
+                if (isK) {  // 128 keys: two 64-row boxes per 64-dim block
+                    tc::mbar_expect_tx(&fullb[st], kWKTile);
+                    uint8_t* dst = sK + st * kWKTile;
+#pragma unroll
+                    for (int db = 0; db < 4; ++db) {
+                        tc::tma_load_2d(dst + db * 16384, m, &fullb[st], db * 64, rowbase + j * kWK);
+                        tc::tma_load_2d(dst + db * 16384 + 8192, m, &fullb[st], db * 64, rowbase + j * kWK + 64);
+                    }
+                } else {
+                    tc::mbar_expect_tx(&fullb[st], kTileBytes);
+                    uint8_t* dst = sV + st * kTileBytes;
+#pragma unroll
+                    for (int db = 0; db < 4; ++db) tc::tma_load_2d(dst + db * 8192, m, &fullb[st], db * 64, rowbase + j * kTcBK);
+                }
+                issued = j + 1;
+            }
+            if (*abort_flag)
+                for (int j = max(0, issued - 2); j < issued; ++j) drain_wait(&fullb[j & 1], (j >> 1) & 1);
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issuer (event loop, P V first)
+        if (lane == 0) {
+            const bool bf = p.mma_bf16 != 0;
+            const uint32_t id_qk = tc::idesc_f16(bf, false, false, kTcRows, kWK);
+            const uint32_t id_pv = tc::idesc_f16(bf, false, true, kTcRows, kTcD);
+            const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), aP = tc::smem_u32(sP);
+            bool ok = tc::mbar_wait_spin(q_full, 0, abort_flag);
+            if (ok) tc::tc_fence_after();
+            int sj = 0, pq = 0;  // next Q K^T tile, next P V half
+            uint32_t idle = 0;
+            uint64_t t_idle = 0;
+            while (ok && pq < nhalves) {
+                bool prog = false;
+                if (pq < 2 * sj) {
+                    const int h = pq & 1, j = pq >> 1, st = pq & 1;
+                    bool ready = tc::mbar_test(&p_full[h], j & 1);
+                    if (ready) ready = tc::mbar_test(&vfull[st], (pq >> 1) & 1);
+                    if (ready) {
+                        tc::tc_fence_after();
+                        const uint32_t vbase = aV + st * kTileBytes, pbase = aP + h * 16384;
+#pragma unroll
+                        for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                            const uint64_t da = tc::sdesc_sw128(pbase + kk * 32, 16, 1024);
+                            const uint64_t db = tc::sdesc_sw128(vbase + kk * 2048, 8192, 1024);
+                            tc::mma_f16(tmem + kColO, da, db, id_pv, (pq > 0 || kk > 0) ? 1u : 0u);
+                        }
+                        tc::mma_commit(&p_free[h]);
+                        tc::mma_commit(&vempty[st]);
+                        ++pq;
+                        prog = true;
+                    }
+                }
+                if (sj < ntiles) {
+                    const int st = sj & 1;
+                    bool ready = tc::mbar_test(&kfull[st], (sj >> 1) & 1);
+                    if (ready && sj >= 1) ready = tc::mbar_test(s_free, (sj - 1) & 1);
+                    if (ready) {
+                        tc::tc_fence_after();
+                        const uint32_t kbase = aK + st * kWKTile;
+#pragma unroll
+                        for (int kk = 0; kk < kTcD / 16; ++kk) {
+                            const uint64_t db = tc::sdesc_sw128(kbase + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                            tc::mma_f16_ts(tmem + kColS, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
+                        }
+                        tc::mma_commit(s_full);
+                        tc::mma_commit(&kempty[st]);
+                        ++sj;
+                        prog = true;
+                    }
+                }
+                if (prog) {
+                    idle = 0;
+                } else if ((++idle & 63) == 1) {
+                    const uint64_t now = tc::globaltimer();
+                    if (idle == 1) t_idle = now;
+                    if (*abort_flag || now - t_idle > tc::kWaitNs) {
+                        *abort_flag = 1;
+                        ok = false;
+                    }
+                }
+            }
+            if (ok) {
+                tc::mma_commit(o_done);
+            } else {
+                tc::mma_commit(drain);
+                drain_wait(drain, 0);
+            }
+        }
+    } else if (warp < 4) {
+        // ------------------------------------------------------------ softmax warpgroup
+        const int r = threadIdx.x;
+        const int gr = row0 + r;
+        const bool row_ok = gr < p.R;
+        const int node = row_ok ? gr / p.G : 0;
+        const int head = kvh * p.G + (row_ok ? gr % p.G : 0);
+        const uint64_t anc = row_ok ? p.anc[(size_t)b * T + node] : 0ull;
+        const int lo_row = win > 0 ? S + node - win + 1 : INT_MIN;
+        const bool bf = p.mma_bf16 != 0;
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        {  // Q row -> TMEM lane r, 16-bit pairs (rounded to fp16 when the MMA runs in fp16)
+            const uint4* src = reinterpret_cast<const uint4*>(p.q[layer] + ((size_t)(b * T + node) * p.HQ + head) * kTcD);
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                uint4 v[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) v[i] = row_ok ? src[half * 16 + i] : make_uint4(0, 0, 0, 0);
+#pragma unroll
+                for (int c2 = 0; c2 < 2; ++c2) {
+                    uint32_t w[32];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        uint4 x = v[c2 * 8 + i];
+                        if (!bf) x = bf16x8_to_f16x8(x);
+                        w[4 * i] = x.x;
+                        w[4 * i + 1] = x.y;
+                        w[4 * i + 2] = x.z;
+                        w[4 * i + 3] = x.w;
+                    }
+                    tc::tmem_st32(tmem + lane_base + kColQ + (half * 2 + c2) * 32, w);
+                }
+            }
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(q_full);
+        }
+        const float qk_scale = 1.4426950408889634f * 0.0625f;  // log2(e) / sqrt(256)
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(s_full, j & 1, abort_flag))) { ok = false; break; }
+            tc::tc_fence_after();
+            float x[128];
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4) {
+                uint32_t sv[32];
+                tc::tmem_ld32(tmem + lane_base + kColS + q4 * 32, sv);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[q4 * 32 + c] = __uint_as_float(sv[c]);
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(s_free);
+
+            const int c0 = k_begin + j * kWK;
+            if (c0 + kWK <= k_end && c0 + kWK <= S && c0 >= lo_last) {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) x[c] *= qk_scale;
+            } else {
+#pragma unroll
+                for (int c = 0; c < 128; ++c) {
+                    const int key = c0 + c;
+                    bool v = row_ok && key < k_end && key >= lo_row;
+                    if (key >= S) v = v && ((anc >> ((key - S) & 63)) & 1ull);
+                    x[c] = v ? x[c] * qk_scale : -INFINITY;
+                }
+            }
+            float mt_ = x[0];
+#pragma unroll
+            for (int c = 1; c < 128; ++c) mt_ = fmaxf(mt_, x[c]);
+            float alpha = 1.f;
+            bool resc = false;
+            if (mt_ > m_ref + 8.f) {
+                alpha = tc::ex2_approx(m_ref - mt_);
+                m_ref = mt_;
+                resc = true;
+            }
+            const float msub = m_ref == -INFINITY ? 0.f : m_ref;
+            if (j >= 1) {  // P V of the previous tile (both halves) done: P reusable, O stable for the rescale
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&p_free[1], (j - 1) & 1, abort_flag))) { ok = false; break; }
+                tc::tc_fence_after();
+                if (__any_sync(0xFFFFFFFFu, resc)) {
+#pragma unroll 1
+                    for (int ch = 0; ch < 8; ++ch) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
+                        tc::tmem_wait_ld();
+#pragma unroll
+                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                        tc::tmem_st32(tmem + lane_base + kColO + ch * 32, o);
+                    }
+                    tc::tmem_wait_st();
+                }
+            }
+            float ps = 0.f;
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int ch0 = c0 + h * kTcBK;
+                if (ch0 + kTcBK > k_end) {  // zero V rows past the key range in this half's stage (not our bytes)
+                    const int q = 2 * j + h, st = q & 1;
+                    if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (q >> 1) & 1, abort_flag))) { ok = false; break; }
+                    const int nk = max(0, k_end - ch0);
+                    uint8_t* vb = sV + st * kTileBytes;
+                    for (int e = r; e < (kTcBK - nk) * 32; e += kTcRows) {
+                        const int row = nk + e / 32, chunk = e % 32;
+                        *reinterpret_cast<uint4*>(vb + (chunk >> 3) * 8192 + row * 128 + (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
+                    }
+                }
+                uint32_t pk[32];
+                float sm2 = 0.f;
+#pragma unroll
+                for (int c = 0; c < 64; c += 2) {
+                    const float p0 = tc::ex2_approx(x[h * 64 + c] - msub);
+                    const float p1 = tc::ex2_approx(x[h * 64 + c + 1] - msub);
+                    sm2 += p0 + p1;
+                    pk[c >> 1] = pack2(p0, p1, bf);
+                }
+                ps += sm2;
+                uint8_t* ph = sP + h * 16384;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch)
+                    *reinterpret_cast<uint4*>(ph + r * 128 + ((ch ^ (r & 7)) << 4)) =
+                        make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
+                tc::fence_proxy_async_smem();
+                tc::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) tc::mbar_arrive(&p_full[h]);
+            }
+            if (!ok) break;
+            l = l * alpha + ps;
+        }
+        if (ok && __all_sync(0xFFFFFFFFu, tc::mbar_wait(o_done, 0, abort_flag))) {
+            tc::tc_fence_after();
+            const size_t slot = ((size_t)unit * p.splits + split) * p.R + gr;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int ch = 0; ch < 8; ++ch) {
+                uint32_t o[32];
+                tc::tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
+                tc::tmem_wait_ld();
+                if (!row_ok) continue;
+                if (p.splits == 1) {
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o[layer]) +
+                                                          ((size_t)(b * T + node) * p.HQ + head) * kTcD + ch * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack2(__uint_as_float(o[8 * k + 2 * e]) * inv, __uint_as_float(o[8 * k + 2 * e + 1]) * inv, true);
+                        dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * kTcD + ch * 32);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                             __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+                }
+            }
+            if (row_ok && p.splits > 1) {
+                p.ws_ml[2 * slot] = m_ref;
+                p.ws_ml[2 * slot + 1] = l;
+            }
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) dev_fail(p.status, TSV_DEV_TIMEOUT, b, blockIdx.x);
+    if (warp == 5) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -613,6 +988,10 @@ bool tc_supported(const tsv_attn_desc* d) {
 
 int tc_mtiles(const tsv_attn_desc* d) { return ((d->HQ / d->HKV) * d->T + kTcRows - 1) / kTcRows; }
 
+// The 128-key kernel for 16-bit caches when a unit has more than one 128-row tile of query rows: there the
+// halved Q K^T issue cost wins; with a single, mostly empty row tile the deeper 64-key pipeline is faster.
+bool tc_wide(const tsv_attn_desc* d) { return d->kv_dtype != TSV_I8_SCALED && tc_mtiles(d) >= 2; }
+
 tsv_status launch_tc(const tsv_attn_desc* d, int splits, int chunk, float* ws_o, float* ws_ml, int32_t* status,
                      cudaStream_t stream) {
     static thread_local TcParams prm;
@@ -649,6 +1028,9 @@ tsv_status launch_tc(const tsv_attn_desc* d, int splits, int chunk, float* ws_o,
     if (i8) {
         cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
         attn_tc_kernel<true><<<(unsigned)items, kTcThreadsI8, kTcSmem, stream>>>(prm);
+    } else if (tc_wide(d)) {
+        cudaFuncSetAttribute(attn_tcw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
+        attn_tcw_kernel<<<(unsigned)items, kTcThreads16, kWSmem, stream>>>(prm);
     } else {
         cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
         attn_tc_kernel<false><<<(unsigned)items, kTcThreads16, kTcSmem, stream>>>(prm);
