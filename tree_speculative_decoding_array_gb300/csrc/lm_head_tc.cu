@@ -51,6 +51,7 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
 // Argmax of one accumulator tile over this warp's 32 vocabulary rows, for each of the nrows hidden rows
 // (TMEM columns starting at taddr).  v = this lane's vocabulary row; rows >= V never win.  With logits != NULL
 // every logit is also written to logits[row0 + column][v] (sampled verification).
+template <bool LOGITS>
 __device__ __forceinline__ void lm_epilogue_tile(uint32_t taddr, int nrows, int v, int V,
                                                  unsigned long long* s_best, int lane, float* logits, int row0) {
     const uint32_t v0 = (uint32_t)(v - lane);
@@ -61,7 +62,7 @@ __device__ __forceinline__ void lm_epilogue_tile(uint32_t taddr, int nrows, int 
 #pragma unroll
         for (int k = 0; k < 32; ++k) {
             if (c0 + k < nrows) {  // uniform across the warp
-                if (logits && v < V) logits[(size_t)(row0 + c0 + k) * V + v] = __uint_as_float(d[k]);
+                if (LOGITS && v < V) logits[(size_t)(row0 + c0 + k) * V + v] = __uint_as_float(d[k]);
                 const uint32_t o = v < V ? orderable(__uint_as_float(d[k])) : 0u;
                 const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, o);
                 const uint32_t who = __ballot_sync(0xFFFFFFFFu, o == mx);
@@ -94,6 +95,7 @@ struct LmTcParams {
 };
 
 // Shared memory: [TMA ring: stages x (W block 16 KB | hidden block NP x 128 B)] ... [bests | barriers]
+template <bool LOGITS>
 __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_constant__ LmTcParams p) {
     const int S = p.stages;
     extern __shared__ uint8_t smem_raw[];
@@ -198,7 +200,7 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
             const int buf = it & 1;
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, 1024))) break;
             tc::tc_fence_after();
-            lm_epilogue_tile(tmem + lane_base + buf * 256, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane,
+            lm_epilogue_tile<LOGITS>(tmem + lane_base + buf * 256, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane,
                              p.logits, chunk * p.NP);
             tc::tc_fence_before();
             __syncwarp();
@@ -255,6 +257,7 @@ __device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
 
 // Shared memory: [W ring: 3 x 36 KB] [hidden ring: HS x NP*128 B] ... [bests | barriers].
 // TMEM: accumulators [0, DC) and [DC, 2 DC); A slots of 32 columns (one k-block) from 2 DC.
+template <bool LOGITS>
 __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_constant__ LmQ4Params p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
@@ -460,7 +463,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
             const int buf = it & 1;
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, 1024))) break;
             tc::tc_fence_after();
-            lm_epilogue_tile(tmem + lane_base + buf * p.DC, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane,
+            lm_epilogue_tile<LOGITS>(tmem + lane_base + buf * p.DC, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane,
                              p.logits, chunk * p.NP);
             tc::tc_fence_before();
             __syncwarp();
@@ -585,8 +588,13 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
     prm.vtiles = (V + kLmM - 1) / kLmM;
     const int sms = sm_count();
     const int groups = sms / nchunks > 0 ? sms / nchunks : 1;
-    cudaFuncSetAttribute(lm_q4_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
-    lm_q4_kernel<<<groups * nchunks, kQ4Threads, kLmSmem, stream>>>(prm);
+    if (logits) {
+        cudaFuncSetAttribute(lm_q4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+        lm_q4_kernel<true><<<groups * nchunks, kQ4Threads, kLmSmem, stream>>>(prm);
+    } else {
+        cudaFuncSetAttribute(lm_q4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+        lm_q4_kernel<false><<<groups * nchunks, kQ4Threads, kLmSmem, stream>>>(prm);
+    }
     return check_launch("lm_head_argmax(tcgen05, 4-bit)");
 }
 
@@ -625,8 +633,13 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
     if (prm.stages < 2) return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the pipeline");
     const int sms = sm_count();
     const int groups = sms / nchunks > 0 ? sms / nchunks : 1;
-    cudaFuncSetAttribute(lm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
-    lm_tc_kernel<<<groups * nchunks, kLmThreads16, kLmSmem, stream>>>(prm);
+    if (logits) {
+        cudaFuncSetAttribute(lm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+        lm_tc_kernel<true><<<groups * nchunks, kLmThreads16, kLmSmem, stream>>>(prm);
+    } else {
+        cudaFuncSetAttribute(lm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+        lm_tc_kernel<false><<<groups * nchunks, kLmThreads16, kLmSmem, stream>>>(prm);
+    }
     return check_launch("lm_head_argmax(tcgen05)");
 }
 
