@@ -78,7 +78,7 @@ __device__ __forceinline__ void store_logits(float* logits, const float (&a0)[R]
 
 // fp16 / bf16 weights [V, H]; hidden rows r0 .. r0 + R - 1.  H % 256 == 0.
 template <int R, bool BF16W>
-__global__ void __launch_bounds__(kLmThreads) lm_gemv16_kernel(const uint16_t* __restrict__ hidden, int rows, int H,
+__global__ void __launch_bounds__(kLmThreads, R <= 4 ? 3 : 2) lm_gemv16_kernel(const uint16_t* __restrict__ hidden, int rows, int H,
                                                                int V, const uint16_t* __restrict__ W,
                                                                unsigned long long* __restrict__ best, int r0,
                                                                float* __restrict__ logits) {
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kLmThreads) lm_gemv16_kernel(const uint16_t* _
 //   sum_k (s q_k + b) h_k = s * sum_k q_k h_k + b * sum_k h_k
 // with the per-half-group sums of h precomputed once in shared memory.
 template <int R>
-__global__ void __launch_bounds__(kLmThreads) lm_gemv_q4_kernel(const uint16_t* __restrict__ hidden, int rows, int H,
+__global__ void __launch_bounds__(kLmThreads, R <= 4 ? 3 : 2) lm_gemv_q4_kernel(const uint16_t* __restrict__ hidden, int rows, int H,
                                                                 int V, const uint8_t* __restrict__ Wq,
                                                                 const uint16_t* __restrict__ scales,
                                                                 const uint16_t* __restrict__ biases,
@@ -245,9 +245,12 @@ __global__ void lm_unpack_kernel(const unsigned long long* __restrict__ best, in
 }
 
 template <int R>
-static void launch_group(int grid, cudaStream_t st, const uint16_t* hidden, int rows, int H, int V, int w_dtype,
-                         const void* W, const void* scales, const void* biases, unsigned long long* best, int r0,
-                         float* logits) {
+static void launch_group(int grid_unused, cudaStream_t st, const uint16_t* hidden, int rows, int H, int V,
+                         int w_dtype, const void* W, const void* scales, const void* biases, unsigned long long* best,
+                         int r0, float* logits) {
+    (void)grid_unused;
+    // one wave: the resident CTAs per SM the launch bounds allow (3 up to 4 rows, 2 for 8)
+    const int grid = sm_count() * (R <= 4 ? 3 : 2);
     if (w_dtype == TSV_Q4_G64) {
         const size_t sm = (size_t)R * (H >> 3) * 16 + (size_t)R * (H >> 5) * 4;
         cudaFuncSetAttribute(lm_gemv_q4_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
