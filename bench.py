@@ -176,15 +176,31 @@ def run_ours(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
+    if args.graph:
+        # The round captured once as a CUDA graph and replayed: the same launches on the same buffers, without
+        # the host issuing each one.  Per-stage times come from the eager rounds timed below it.
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step()
+        for _ in range(args.warmup):
+            graph.replay()
+        torch.cuda.synchronize()
     with ClockSampler(torch.cuda.current_device()) as clk:
         t0.record(stream)
         for s in range(args.steps):
-            step(ev[s])
+            if args.graph:
+                graph.replay()
+            else:
+                step(ev[s])
         t1.record(stream)
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     ms = t0.elapsed_time(t1)
+    if args.graph:  # per-stage times: eager rounds with events
+        for s in range(args.steps):
+            step(ev[s])
+        torch.cuda.synchronize()
     per_kernel = {n: statistics.mean(ev[s][i][0].elapsed_time(ev[s][i][1]) for s in range(args.steps))
                   for i, n in enumerate(names)}
     if world > 1:
@@ -409,6 +425,9 @@ def main():
     ap.add_argument("--build-tree", type=int, default=0, metavar="K",
                     help="> 0: time a tree-construction stage first: the drafter's top-K children of every node "
                          "(drafter logits [B*T, V]) and the best-first selection of T nodes from 1 + T*K candidates")
+    ap.add_argument("--eager", dest="graph", action="store_false",
+                    help="issue every call of every timed round from the host instead of replaying the round as a "
+                         "captured CUDA graph (the default; per-stage times are always taken on eager rounds)")
     ap.add_argument("--layers", type=int, default=None,
                     help="attention layers (default: the workload's); fewer only for small profiler captures")
     args = ap.parse_args()
@@ -435,7 +454,7 @@ def main():
               "D": cfg.D, "S": cfg.S, "H": cfg.H, "V": cfg.V, "kv": configs.DTYPE_NAMES[cfg.kv_dtype],
               "lm_head": configs.DTYPE_NAMES[cfg.w_dtype], "topology": cfg.topology,
               "l2": f"inputs larger than L2 ({cfg.algorithmic_bytes() / 1e9:.2f} GB read per round), no flush",
-              "parallelism": f"replicas x{args.gpus}"}
+              "parallelism": f"replicas x{args.gpus}", "launch": "cuda graph" if args.graph else "eager"}
     round_id = args.round if args.round is not None else ({1: 2}.get(args.config, 0))
 
     if args.impl == "reference":
