@@ -226,7 +226,7 @@ constexpr int kQ4WStages = 3;
 constexpr int kQ4WStage = 2 * 16384 + 2 * 2048;       // codes [128 rows x 256 B] as two swizzled boxes, scales, biases
 constexpr int kQ4HOff = kQ4WStages * kQ4WStage;       // hidden ring after the W ring
 constexpr int kQ4MaxHStages = 16;
-constexpr int kQ4MaxASlots = 14;
+constexpr int kQ4MaxAGroups = 8;
 constexpr int kQ4MaxNP = 128;
 
 struct LmQ4Params {
@@ -237,6 +237,7 @@ struct LmQ4Params {
     unsigned long long* best;
     float* logits;     // NULL, or [rows][V] fp32 written by the epilogue
     int rows, H, V, NP, DC, NA, HS, nchunks, vtiles;
+    int GK;            // k-blocks per A-slot group and per hidden stage (1, 2 or 4): one wait and one commit each
 };
 
 // One 32-bit word of codes (features 8j..8j+7, feature 8j+i in bits 4i..4i+3) -> four fp16 pairs
@@ -256,7 +257,9 @@ __device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
 }
 
 // Shared memory: [W ring: 3 x 36 KB] [hidden ring: HS x NP*128 B] ... [bests | barriers].
-// TMEM: accumulators [0, DC) and [DC, 2 DC); A slots of 32 columns (one k-block) from 2 DC.
+// TMEM: accumulators [0, DC) and [DC, 2 DC); from 2 DC, NA groups of GK A slots of 32 columns (one k-block
+// each).  Hidden stages hold GK k-blocks too, so the MMA thread waits, fences and commits once per GK k-blocks
+// (each M=128 MMA occupies the tensor pipe ~100 cycles at these N; per-k-block barrier traffic would double it).
 template <bool LOGITS>
 __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_constant__ LmQ4Params p) {
     extern __shared__ uint8_t smem_raw[];
@@ -270,8 +273,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
     uint64_t* wempty = bars + 3;      // [3] every converter warp is done with the stage
     uint64_t* hfull = bars + 6;       // [16] hidden block landed
     uint64_t* hempty = bars + 22;     // [16] MMAs done with the hidden block
-    uint64_t* afull = bars + 38;      // [14] A slot written (4 converter warps)
-    uint64_t* aempty = bars + 52;     // [14] MMAs done with the A slot
+    uint64_t* afull = bars + 38;      // [8] A-slot group written (the converter warps that contribute to it)
+    uint64_t* aempty = bars + 52;     // [8] MMAs done with the A-slot group
     uint64_t* acc_full = bars + 66;   // [2]
     uint64_t* acc_empty = bars + 68;  // [2]
     uint64_t* drain = bars + 70;
@@ -284,7 +287,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
     const int groups = gridDim.x / p.nchunks;
     const int KB = p.H / kLmKB;
     const int NSt = KB / kQ4KBPerStage;  // W stages per vocabulary tile
-    const int NA = p.NA, HS = p.HS;
+    const int NA = p.NA, HS = p.HS, GK = p.GK;  // A-slot groups, hidden stages, k-blocks per group
     const int nrows = min(p.NP, p.rows - chunk * p.NP);
     if (group >= p.vtiles || nrows <= 0) return;
 
@@ -298,7 +301,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
             tc::mbar_init(&hempty[s], 1);
         }
         for (int s = 0; s < NA; ++s) {
-            tc::mbar_init(&afull[s], 4);
+            tc::mbar_init(&afull[s], GK >= 2 ? 8 : 4);  // one k-block per group: only one converter set writes it
             tc::mbar_init(&aempty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -351,16 +354,17 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
         }
     } else if (warp == 14) {
         if (lane == 0) {
-            // -------------------------------------------------------- hidden blocks, one per k-block
+            // -------------------------------------------------------- hidden blocks, GK k-blocks per stage
             tc::tma_prefetch_desc(&p.hmap);
             int g = 0, issued = 0;
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups) {
-                for (int kb = 0; kb < KB; ++kb, ++g) {
+                for (int kb = 0; kb < KB; kb += GK, ++g) {
                     const int s = g % HS;
                     if (g >= HS && !tc::mbar_wait(&hempty[s], ((g / HS) - 1) & 1, abort_flag, 512)) { ok = false; break; }
-                    tc::mbar_expect_tx(&hfull[s], h_bytes);
-                    tc::tma_load_2d(hring + s * h_bytes, &p.hmap, &hfull[s], kb * kLmKB, chunk * p.NP);
+                    tc::mbar_expect_tx(&hfull[s], h_bytes * GK);
+                    for (int u = 0; u < GK; ++u)
+                        tc::tma_load_2d(hring + (s * GK + u) * h_bytes, &p.hmap, &hfull[s], (kb + u) * kLmKB, chunk * p.NP);
                     issued = g + 1;
                 }
             }
@@ -379,16 +383,18 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                 const int buf = it & 1;
                 if (it >= 2 && !tc::mbar_wait_spin(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = 0; kb < KB; kb += GK) {  // one group of GK k-blocks: one wait each, one commit each
                     if (!tc::mbar_wait_spin(&afull[as], aph, abort_flag)) { ok = false; break; }
                     if (!tc::mbar_wait_spin(&hfull[hs], hph, abort_flag)) { ok = false; break; }
                     tc::tc_fence_after();
-                    const uint32_t a = tmem + a_col + (uint32_t)as * 32;
-                    const uint32_t b = hbase + (uint32_t)hs * h_bytes;
+                    for (int u = 0; u < GK; ++u) {
+                        const uint32_t a = tmem + a_col + (uint32_t)(as * GK + u) * 32;
+                        const uint32_t b = hbase + (uint32_t)(hs * GK + u) * h_bytes;
 #pragma unroll
-                    for (int kk = 0; kk < kLmKB / 16; ++kk)
-                        tc::mma_f16_ts(tmem + buf * p.DC, a + kk * 8, tc::sdesc_sw128(b + kk * 32, 16, 1024), idesc,
-                                       (kb > 0 || kk > 0) ? 1u : 0u);
+                        for (int kk = 0; kk < kLmKB / 16; ++kk)
+                            tc::mma_f16_ts(tmem + buf * p.DC, a + kk * 8, tc::sdesc_sw128(b + kk * 32, 16, 1024), idesc,
+                                           (kb + u > 0 || kk > 0) ? 1u : 0u);
+                    }
                     tc::mma_commit(&aempty[as]);
                     tc::mma_commit(&hempty[hs]);
                     if (++as == NA) { as = 0; aph ^= 1u; }
@@ -420,13 +426,15 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                 const uint4 bi8 = *reinterpret_cast<const uint4*>(st + 34816 + r * 16);
                 for (int kk = 0; kk < kQ4KBPerStage; ++kk, ++g) {
                     if ((g & 1) != par) continue;
-                    const int as = g % NA;
-                    if (g >= NA &&
-                        !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&aempty[as], ((g / NA) - 1) & 1, abort_flag, 256))) {
+                    // A-slot group of k-block g; this set writes the k-blocks of its parity in the group
+                    const int gg = g / GK, as = gg % NA, gi = g % GK;
+                    const bool first = GK == 1 || gi == par, last = GK == 1 || gi == GK - 2 + par;
+                    if (first && gg >= NA &&
+                        !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&aempty[as], ((gg / NA) - 1) & 1, abort_flag, 256))) {
                         ok = false;
                         break;
                     }
-                    tc::tc_fence_after();
+                    if (first) tc::tc_fence_after();
                     const uint32_t sw = u4_word(sc8, kk >> 1), bw = u4_word(bi8, kk >> 1);
                     const float sf = (kk & 1) ? bf16_hi(sw) : bf16_lo(sw);
                     const float bf = (kk & 1) ? bf16_hi(bw) : bf16_lo(bw);
@@ -445,11 +453,13 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                     q4_word(hi.y, s2, b2, k1024, out + 20);
                     q4_word(hi.z, s2, b2, k1024, out + 24);
                     q4_word(hi.w, s2, b2, k1024, out + 28);
-                    tc::tmem_st32(tmem + lane_base + a_col + (uint32_t)as * 32, out);
-                    tc::tmem_wait_st();
-                    tc::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&afull[as]);
+                    tc::tmem_st32(tmem + lane_base + a_col + (uint32_t)(as * GK + gi) * 32, out);
+                    if (last) {
+                        tc::tmem_wait_st();
+                        tc::tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) tc::mbar_arrive(&afull[as]);
+                    }
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&wempty[s]);
@@ -555,11 +565,17 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
     int NP = (rows + nchunks - 1) / nchunks;
     NP = ((NP + 15) / 16) * 16;
     const int DC = ((NP + 31) / 32) * 32;
-    int NA = (512 - 2 * DC) / 32;
-    NA = (NA > kQ4MaxASlots ? kQ4MaxASlots : NA) & ~1;  // even: a slot is always refilled by the same converter set
-    int HS = (kLmUsable - kQ4HOff) / (NP * 128);
-    HS = HS > kQ4MaxHStages ? kQ4MaxHStages : HS;
-    if (NA < 2 || HS < 2) return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the 4-bit pipeline");
+    // k-blocks per group: the largest of 4, 2, 1 that leaves at least 2 hidden stages and 2 A-slot groups
+    int GK = 4, NA = 0, HS = 0;
+    for (; GK >= 1; GK >>= 1) {
+        NA = (512 - 2 * DC) / (32 * GK);
+        NA = NA > kQ4MaxAGroups ? kQ4MaxAGroups : NA;
+        if (GK == 1) NA &= ~1;  // even: with one k-block per group a slot is always refilled by the same converter set
+        HS = (kLmUsable - kQ4HOff) / (NP * 128 * GK);
+        HS = HS > kQ4MaxHStages ? kQ4MaxHStages : HS;
+        if (NA >= 2 && HS >= 2) break;
+    }
+    if (GK < 1) return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the 4-bit pipeline");
 
     const size_t n8 = (size_t)rows * H / 8;
     hidden_to_f16_q4order_kernel<<<sm_count() * 4, 256, 0, stream>>>((const uint4*)hidden, (uint4*)extra, n8);
@@ -584,6 +600,7 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
     prm.DC = DC;
     prm.NA = NA;
     prm.HS = HS;
+    prm.GK = GK;
     prm.nchunks = nchunks;
     prm.vtiles = (V + kLmM - 1) / kLmM;
     const int sms = sm_count();
