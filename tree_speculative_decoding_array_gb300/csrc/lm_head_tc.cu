@@ -384,8 +384,9 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                 if (it >= 2 && !tc::mbar_wait_spin(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
                 for (int kb = 0; kb < KB; kb += GK) {  // one group of GK k-blocks: one wait each, one commit each
-                    if (!tc::mbar_wait_spin(&afull[as], aph, abort_flag)) { ok = false; break; }
-                    if (!tc::mbar_wait_spin(&hfull[hs], hph, abort_flag)) { ok = false; break; }
+                    // short sleeps between polls: this thread shares its SM sub-partition with two converter warps
+                    if (!tc::mbar_wait(&afull[as], aph, abort_flag, 64)) { ok = false; break; }
+                    if (!tc::mbar_wait(&hfull[hs], hph, abort_flag, 64)) { ok = false; break; }
                     tc::tc_fence_after();
                     for (int u = 0; u < GK; ++u) {
                         const uint32_t a = tmem + a_col + (uint32_t)(as * GK + u) * 32;
