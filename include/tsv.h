@@ -83,6 +83,17 @@ typedef enum {
 /* Reason for the last non-TSV_OK status returned on this thread ("" if none). */
 const char* tsv_last_error(void);
 
+/*
+ * tsv_selftest_bounded_wait - checks the failure path every tensor-core
+ * kernel relies on (no page counterpart: a property of this implementation).
+ * One CTA waits on a barrier that nothing completes; the library's bounded
+ * wait gives up after 1 s, raises the CTA's abort flag (which ends the other
+ * warps' waits) and records TSV_DEV_TIMEOUT in dev_status (words 1..2: the
+ * flag, the warp).  The device stays usable.  dev_status: int32[4], device
+ * memory, zeroed by the caller.
+ */
+tsv_status tsv_selftest_bounded_wait(int32_t* dev_status, cudaStream_t stream);
+
 /* ABI version of this library (major * 100 + minor). */
 int tsv_version(void);
 

@@ -409,3 +409,51 @@ def test_gather_bad_path(gpu_lib):
     torch.cuda.synchronize()
     assert st.tolist()[:2] == [gpu_lib.DEV_BAD_PATH, 0]
     assert kv_len.tolist() == [8, 6]  # bad sequence untouched, good one advanced
+
+
+# ----------------------------------------------------------------------------- limits and failure paths
+def test_attention_maximum_layer_count(gpu_lib):
+    """All TSV_MAX_LAYERS layers in one launch, on both kernels."""
+    for path in (1, 2):
+        rng = np.random.default_rng(64 + path)
+        run_attn_case(gpu_lib, rng, B=1, T=3, HQ=6, HKV=2, D=256, S_list=[70], kv_dtype=1, splits=0, layers=64,
+                      path=path)
+
+
+def test_empty_batch_is_a_no_op(gpu_lib):
+    T, HQ, HKV, D = 3, 4, 2, 64
+    e32 = lambda *s: torch.zeros(*s, dtype=torch.int32, device=DEV)
+    par, anc, depth = e32(0, T), torch.zeros(0, T, dtype=torch.int64, device=DEV), e32(0, T)
+    gpu_lib.tree_mask(par, anc, depth)
+    q = [torch.zeros(0, T, HQ, D, dtype=torch.bfloat16, device=DEV)]
+    k = [torch.zeros(0, HKV, 8, D, dtype=torch.float16, device=DEV)]
+    desc = gpu_lib.attn_desc(q, k, [k[0].clone()], [q[0].clone()], e32(0), anc, T=T, HQ=HQ, HKV=HKV, D=D,
+                             kv_dtype=0, max_kv_len=8)
+    gpu_lib.tree_verify_attention(desc, torch.empty(256, dtype=torch.uint8, device=DEV))
+    gpu_lib.tree_accept_walk(e32(0, T), e32(0, T), par, e32(0, T), e32(0), e32(0, T))
+    gpu_lib.kv_gather_positions(gpu_lib.kv_desc(k, [k[0].clone()], HKV=HKV, D=D, kv_dtype=0), e32(0), e32(0, T),
+                                e32(0), T)
+    kn = [torch.zeros(0, T, HKV, D, dtype=torch.bfloat16, device=DEV)]
+    ad = gpu_lib.append_desc(q, q, kn, kn, k, [k[0].clone()], depth, T=T, HQ=HQ, HKV=HKV, D=D, kv_dtype=0,
+                             rot_dim=D, rope_base=1e4)
+    gpu_lib.tree_append(ad, e32(0))
+    torch.cuda.synchronize()
+    with pytest.raises(gpu_lib.TsvError, match="TSV_EINVAL"):  # the LM head needs at least one row
+        gpu_lib.lm_head_argmax(torch.zeros(0, 256, dtype=torch.bfloat16, device=DEV),
+                               torch.zeros(10, 256, dtype=torch.bfloat16, device=DEV), e32(0), w_dtype=1, V=10)
+
+
+def test_bounded_wait_times_out_and_device_stays_usable(gpu_lib):
+    """A wait that nothing completes ends after its limit with TSV_DEV_TIMEOUT; the context keeps working."""
+    import ctypes as C
+    lib = gpu_lib.load()
+    st = status()
+    assert lib.tsv_selftest_bounded_wait(C.c_void_p(st.data_ptr()), C.c_void_p(torch.cuda.current_stream().cuda_stream)) == 0
+    torch.cuda.synchronize()
+    assert st.tolist()[0] == gpu_lib.DEV_TIMEOUT and st.tolist()[1] == 1
+    par = i32(np.array([[-1, 0, 1]], dtype=np.int32))
+    anc = torch.zeros(1, 3, dtype=torch.int64, device=DEV)
+    depth = torch.zeros(1, 3, dtype=torch.int32, device=DEV)
+    gpu_lib.tree_mask(par, anc, depth)
+    torch.cuda.synchronize()
+    assert depth.tolist() == [[0, 1, 2]]

@@ -58,6 +58,7 @@ class AppendDesc(C.Structure):
 SIGNATURES = {
     "tsv_last_error": (C.c_char_p, []),
     "tsv_version": (C.c_int, []),
+    "tsv_selftest_bounded_wait": (C.c_int, [_vp, _vp]),
     "tsv_tree_mask": (C.c_int, [_vp, _i32, _i32, _vp, _vp, _vp, _i32, _vp, _vp]),
     "tsv_sliding_band_mask": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp]),
     "tsv_draft_children_workspace_size": (_sz, [_i32, _i32, _i32]),

@@ -405,6 +405,7 @@ static tsv_status check_desc(const tsv_attn_desc* d) {
     if (d->path == TSV_ATTN_TCGEN05 && !tc_supported(d))
         return fail(TSV_EUNSUPPORTED, "tree_verify_attention: the tcgen05 kernel needs D == 256 and an fp16 or bf16 "
                                       "cache of fewer than 2^31 rows");
+    if (d->B == 0) return TSV_OK;  // an empty batch: no pointer is read
     if (!d->kv_len || !d->anc) return fail(TSV_EINVAL, "tree_verify_attention: kv_len and anc must be non-null");
     const int G = d->HQ / d->HKV;
     if ((long long)d->n_layers * d->B * d->HKV > 65535 || ((long long)G * d->T + kRB - 1) / kRB > 65535)

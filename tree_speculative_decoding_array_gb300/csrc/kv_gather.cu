@@ -117,7 +117,9 @@ extern "C" tsv_status tsv_kv_gather_positions(const tsv_kv_desc* kv, int32_t* kv
                                               cudaStream_t stream) {
     using namespace tsv;
     clear_error();
-    if (!kv || !kv_len || !path || !path_len) return fail(TSV_EINVAL, "kv_gather_positions: null pointer argument");
+    if (!kv) return fail(TSV_EINVAL, "kv_gather_positions: null descriptor");
+    if (kv->B == 0 && T >= 1 && T <= TSV_MAX_T) return TSV_OK;  // an empty batch: nothing to read or write
+    if (!kv_len || !path || !path_len) return fail(TSV_EINVAL, "kv_gather_positions: null pointer argument");
     if (T < 1 || T > TSV_MAX_T) return fail(TSV_ECAPACITY, "kv_gather_positions: T=%d outside [1, %d]", T, TSV_MAX_T);
     if (kv->n_layers < 1 || kv->n_layers > TSV_MAX_LAYERS)
         return fail(TSV_ECAPACITY, "kv_gather_positions: n_layers=%d outside [1, %d]", kv->n_layers, TSV_MAX_LAYERS);

@@ -213,6 +213,7 @@ static tsv_status check_append(const tsv_append_desc* d, const int32_t* kv_len) 
         return fail(TSV_EINVAL, "tree_append: rope_base=%g must be positive and finite", d->rope_base);
     if (d->s_cap < d->T) return fail(TSV_EINVAL, "tree_append: s_cap=%lld < T", (long long)d->s_cap);
     if ((long long)d->B * d->T > 0x7FFFFFFFLL) return fail(TSV_ECAPACITY, "tree_append: grid too large");
+    if (d->B == 0) return TSV_OK;  // an empty batch: no pointer is read
     if (!d->depth || !kv_len) return fail(TSV_EINVAL, "tree_append: depth and kv_len must be non-null");
     for (int l = 0; l < d->n_layers; ++l) {
         if (!d->q_in[l] || !d->q_out[l] || !d->k_new[l] || !d->v_new[l] || !d->k[l] || !d->v[l])
