@@ -22,8 +22,8 @@
 //
 // 4-bit heads (lm_q4_kernel): the dequantised weights never touch shared
 // memory.  Warp 4 streams the raw codes of 8 k-blocks plus their scales and
-// biases per stage, warp 14 the hidden blocks, through separate rings;
-// 8 converter warps (6-13) evaluate w = scale * q + bias in fp16 with one
+// biases per stage, warp 22 the hidden blocks, through separate rings;
+// 16 converter warps (6-21) evaluate w = scale * q + bias in fp16 with one
 // rounding (q exact via the 1024 + q bit trick) and store the A operand
 // straight into TMEM slots with tcgen05.st; warp 5 issues MMAs whose A
 // operand is read from TMEM.  The converter emits a code word's 8 features in
@@ -219,8 +219,10 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
 }
 
 // ------------------------------------------------------------------ 4-bit heads
-constexpr int kQ4Conv = 256;                          // 8 converter warps (two sets of the four TMEM lane quarters)
-constexpr int kQ4Threads = kLmEpi + 64 + kQ4Conv + 32;  // + warp 14: hidden-block producer
+constexpr int kQ4Sets = 4;                            // converter sets; a set = 4 warps, one per TMEM lane quarter
+constexpr int kQ4Conv = kQ4Sets * 128;                // converter warps 6 .. 6 + 4 * kQ4Sets - 1
+constexpr int kQ4HWarp = 6 + kQ4Conv / 32;            // the hidden-block producer's warp
+constexpr int kQ4Threads = kLmEpi + 64 + kQ4Conv + 32;
 constexpr int kQ4KBPerStage = 8;                      // k-blocks of 64 features per W stage
 constexpr int kQ4WStages = 3;
 constexpr int kQ4WStage = 2 * 16384 + 2 * 2048;       // codes [128 rows x 256 B] as two swizzled boxes, scales, biases
@@ -301,7 +303,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
             tc::mbar_init(&hempty[s], 1);
         }
         for (int s = 0; s < NA; ++s) {
-            tc::mbar_init(&afull[s], GK >= 2 ? 8 : 4);  // one k-block per group: only one converter set writes it
+            tc::mbar_init(&afull[s], 4 * GK);  // one set (4 warps) converts each k-block of the group
             tc::mbar_init(&aempty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                 for (int q = max(0, issued - kQ4WStages); q < issued; ++q)
                     lm_drain_wait(&wfull[q % kQ4WStages], (q / kQ4WStages) & 1);
         }
-    } else if (warp == 14) {
+    } else if (warp == kQ4HWarp) {
         if (lane == 0) {
             // -------------------------------------------------------- hidden blocks, GK k-blocks per stage
             tc::tma_prefetch_desc(&p.hmap);
@@ -407,8 +409,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
             lm_drain_wait(drain, 0);
         }
     } else if (warp >= 6) {
-        // ------------------------------------------------------------ converters (warps 6-13): codes -> fp16 A slots
-        // Set `par` converts the k-blocks g with g % 2 == par; its four warps cover the four TMEM lane quarters.
+        // ------------------------------------------------------------ converters: codes -> fp16 A slots in TMEM
+        // Set `par` converts the k-blocks g with g % kQ4Sets == par; its four warps cover the four lane quarters.
         const int par = (warp - 6) >> 2, quad = warp & 3;
         const int r = quad * 32 + lane;  // vocabulary row within the tile = TMEM lane
         const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
@@ -426,16 +428,15 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                 const uint4 sc8 = *reinterpret_cast<const uint4*>(st + 32768 + r * 16);
                 const uint4 bi8 = *reinterpret_cast<const uint4*>(st + 34816 + r * 16);
                 for (int kk = 0; kk < kQ4KBPerStage; ++kk, ++g) {
-                    if ((g & 1) != par) continue;
-                    // A-slot group of k-block g; this set writes the k-blocks of its parity in the group
+                    if ((g % kQ4Sets) != par) continue;
+                    // A-slot group of k-block g; a set converts at most one k-block of any group (GK <= kQ4Sets)
                     const int gg = g / GK, as = gg % NA, gi = g % GK;
-                    const bool first = GK == 1 || gi == par, last = GK == 1 || gi == GK - 2 + par;
-                    if (first && gg >= NA &&
+                    if (gg >= NA &&
                         !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&aempty[as], ((gg / NA) - 1) & 1, abort_flag, 256))) {
                         ok = false;
                         break;
                     }
-                    if (first) tc::tc_fence_after();
+                    tc::tc_fence_after();
                     const uint32_t sw = u4_word(sc8, kk >> 1), bw = u4_word(bi8, kk >> 1);
                     const float sf = (kk & 1) ? bf16_hi(sw) : bf16_lo(sw);
                     const float bf = (kk & 1) ? bf16_hi(bw) : bf16_lo(bw);
@@ -455,12 +456,10 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                     q4_word(hi.z, s2, b2, k1024, out + 24);
                     q4_word(hi.w, s2, b2, k1024, out + 28);
                     tc::tmem_st32(tmem + lane_base + a_col + (uint32_t)(as * GK + gi) * 32, out);
-                    if (last) {
-                        tc::tmem_wait_st();
-                        tc::tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) tc::mbar_arrive(&afull[as]);
-                    }
+                    tc::tmem_wait_st();
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) tc::mbar_arrive(&afull[as]);
                 }
                 __syncwarp();
                 if (lane == 0) tc::mbar_arrive(&wempty[s]);
@@ -571,7 +570,9 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
     for (; GK >= 1; GK >>= 1) {
         NA = (512 - 2 * DC) / (32 * GK);
         NA = NA > kQ4MaxAGroups ? kQ4MaxAGroups : NA;
-        if (GK == 1) NA &= ~1;  // even: with one k-block per group a slot is always refilled by the same converter set
+        // a slot group must always be refilled by the same converter sets (its previous use then completed
+        // before they wait again): NA a multiple of kQ4Sets / GK
+        NA -= NA % (kQ4Sets / GK);
         HS = (kLmUsable - kQ4HOff) / (NP * 128 * GK);
         HS = HS > kQ4MaxHStages ? kQ4MaxHStages : HS;
         if (NA >= 2 && HS >= 2) break;
