@@ -13,20 +13,24 @@
 //              Stores Q into TMEM, reads S from TMEM, applies the
 //              scale and the ancestor bits, runs the online softmax (fp32,
 //              log2 domain, lazy rescale of O when the max grows by > 2^8),
-//              writes P as 16-bit into shared memory, finally reads O.
+//              writes P as 16-bit pairs back over its S tile in TMEM,
+//              finally reads O.
 //   warp 4, 6  TMA producers (4: K, 6: V; one lane each): tiles of 64 keys x
 //              256, 128-byte swizzled, each in its own 3-stage ring (a K
 //              stage frees after Q K^T, a V stage after P V).
 //   warp 5     allocates TMEM (512 columns: Q 128 as 16-bit pairs, S 2 x 64,
 //              O 256) and issues the MMAs from an event loop:
 //              S = Q K^T (M=128, N=64, K=256, A read from TMEM) and
-//              O += P V (M=128, N=256, K=64, V read MN-major).
+//              O += P V (M=128, N=256, K=64, A = P read from TMEM, V read
+//              MN-major).  An S buffer is reused once the P V of the P
+//              written over it is done, so the softmax of tile j + 1 never
+//              waits for the P V of tile j (except to rescale O).
 // Int8 caches (Int8 codes with fp16 per-token scales) use 352 threads: warps
 // 6-9 are a converter group and warp 10 the V producer.  TMA brings the raw
-// int8 tiles into 2-stage staging rings; the converter writes the codes as
-// fp16 (exact) into 2-stage operand rings and the tile's scales into shared
-// memory; the softmax warpgroup multiplies S column c by k_scale[c] and folds
-// v_scale[c] into P.
+// int8 tiles (128-byte swizzled halves) into 2-stage staging rings; the
+// converter writes the codes as fp16 (exact) into 2-stage operand rings and
+// the tile's scales (fetched a tile ahead) into shared memory; the softmax
+// warpgroup multiplies S column c by k_scale[c] and folds v_scale[c] into P.
 // Warp-collective roles take every wait decision warp-uniformly (__all_sync),
 // so that tcgen05.ld / __syncwarp never see a partial warp.
 // Every mbarrier wait is bounded in time: on expiry the CTA raises a shared
@@ -43,7 +47,7 @@ constexpr int kTcRows = 128;
 constexpr int kTcBK = 64;
 constexpr int kTcD = 256;
 constexpr int kTcThreads16 = 224;  // + warp 6: V producer
-constexpr int kTcThreadsI8 = 352;  // + warps 6-9: converters, warp 10: V producer
+constexpr int kTcThreadsI8 = 480;  // + warps 6-9: K converters, 10-13: V converters, warp 14: V producer
 constexpr int kTcSmem = 1024 + 215040 + 512;
 constexpr uint32_t kTileBytes = kTcBK * kTcD * 2;  // one K (or V) tile: 32 KiB
 
@@ -106,24 +110,34 @@ __device__ __forceinline__ void i8x16_to_f16x16(uint4 in, uint32_t (&out)[8]) {
     }
 }
 
-// Raw int8 tile [64 keys x 256] (row-major) -> fp16 operand tile in the
-// 128-byte-swizzled layout (4 blocks of [64 keys x 64]); keys >= nk become 0.
+// Raw int8 tile [64 keys x 256] as TMA lands it: two 128-byte-swizzled halves [2][64 keys][128 B] (16-byte
+// chunk c of key k's half h at h * 8192 + k * 128 + ((c ^ (k & 7)) << 4)) -> fp16 operand tile in the
+// 128-byte-swizzled layout (4 blocks of [64 keys x 64]); keys >= nk become 0.  A quarter-warp takes one chunk
+// column of 8 consecutive keys, so its 16-byte loads and stores each hit 8 distinct bank groups.
 __device__ __forceinline__ void convert_i8_tile(const uint8_t* raw, uint8_t* dst, int nk, int ct) {
-#pragma unroll 2
+    const int key = ct & 63, k7 = key & 7;  // chunk q of the 256-byte row: 2 s + (ct >> 6)
+    uint4 in[8];  // all eight 16-byte loads in flight before the first conversion
+#pragma unroll
     for (int s = 0; s < 8; ++s) {
-        const int id = s * 128 + ct;
-        const int key = id >> 4, c = id & 15;
-        const uint4 v = key < nk ? *reinterpret_cast<const uint4*>(raw + key * 256 + c * 16) : make_uint4(0, 0, 0, 0);
+        const int q = 2 * s + (ct >> 6);
+        in[s] = key < nk ? *reinterpret_cast<const uint4*>(raw + (q >> 3) * 8192 + key * 128 + (((q & 7) ^ k7) << 4))
+                         : make_uint4(0, 0, 0, 0);
+    }
+    uint8_t* row = dst + key * 128;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const int q = 2 * s + (ct >> 6);
         uint32_t w[8];
-        i8x16_to_f16x16(v, w);
+        i8x16_to_f16x16(in[s], w);
         if (key >= nk) {
 #pragma unroll
             for (int e = 0; e < 8; ++e) w[e] = 0;
         }
-        const int kb = c >> 2, cc0 = (c & 3) * 2;
-        uint8_t* row = dst + kb * 8192 + key * 128;
-        *reinterpret_cast<uint4*>(row + ((cc0 ^ (key & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
-        *reinterpret_cast<uint4*>(row + (((cc0 + 1) ^ (key & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+        // features 16 q .. 16 q + 15: fp16 block q >> 2, 16-byte chunks (q & 3) * 2 and the next
+        const int cc0 = (q & 3) * 2;
+        uint8_t* rb = row + (q >> 2) * 8192;
+        *reinterpret_cast<uint4*>(rb + ((cc0 ^ k7) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(rb + (((cc0 + 1) ^ k7) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
     }
 }
 
@@ -133,25 +147,23 @@ template <bool I8>
 __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    // Q lives in TMEM.  16-bit caches: K stages [3 x 32K] at 0, V stages [3 x 32K] at 96K.
+    // Q, S and P live in TMEM.  16-bit caches: K stages [3 x 32K] at 0, V stages [3 x 32K] at 96K.
     // Int8 caches: fp16 K tiles [2 x 32K] at 0, fp16 V tiles [2 x 32K] at 64K, raw K stages [2 x 16K] at 128K,
-    // raw V stages [2 x 16K] at 160K.  P [128 x 64] 16-bit at 192K.
+    // raw V stages [2 x 16K] at 160K.
     constexpr int NS = I8 ? 2 : kNS;  // stages of the TMA rings
     uint8_t* sK = sm;
     uint8_t* sV = sm + (I8 ? 65536 : 98304);
     uint8_t* sRawK = sm + 131072;
     uint8_t* sRawV = sm + 163840;
-    uint8_t* sP = sm + 196608;
     float* sScale = reinterpret_cast<float*>(sm + 212992);  // Int8: [4 slots][64 K scales x log2(e)/16 | 64 V scales]
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 215040);
     uint64_t* kfull = bars + 0;      // [3] K tile (16-bit) / raw K tile (Int8) landed
     uint64_t* kempty = bars + 3;     // [3] stage free again: after Q K^T (16-bit) / after conversion (Int8)
     uint64_t* vfull = bars + 6;      // [3] V tile / raw V tile landed
     uint64_t* vempty = bars + 9;     // [3] stage free again: after P V (16-bit) / after conversion (Int8)
-    uint64_t* s_full = bars + 12;    // [2]
-    uint64_t* s_free = bars + 14;    // [2]
-    uint64_t* p_full = bars + 16;
-    uint64_t* p_free = bars + 17;
+    uint64_t* s_full = bars + 12;    // [2] S tile b written by Q K^T
+    uint64_t* sp_free = bars + 14;   // [2] P V of the P held in S buffer b done: buffer b and O free again
+    uint64_t* p_full = bars + 16;    // [2] P written over S buffer b
     uint64_t* o_done = bars + 18;
     uint64_t* q_full = bars + 19;
     uint64_t* drain = bars + 20;
@@ -162,7 +174,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
     uint64_t* sc_full = bars + 29;   // Int8: [4] scale slot written
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 34);
-    // TMEM columns: Q [0, 128) as 16-bit pairs, S [128, 192) and [192, 256), O [256, 512).
+    // TMEM columns: Q [0, 128) as 16-bit pairs, S [128, 192) and [192, 256) (P, 16-bit pairs, over the first 32
+    // columns of its S tile once the softmax has read it), O [256, 512).
     constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -215,15 +228,14 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
         }
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&s_full[s], 1);
-            tc::mbar_init(&s_free[s], 4);
+            tc::mbar_init(&sp_free[s], 1);
+            tc::mbar_init(&p_full[s], 4);
             tc::mbar_init(&kc_full[s], 4);
             tc::mbar_init(&kc_empty[s], 1);
             tc::mbar_init(&vc_full[s], 4);
             tc::mbar_init(&vc_empty[s], 1);
         }
         for (int s = 0; s < 4; ++s) tc::mbar_init(&sc_full[s], 4);
-        tc::mbar_init(p_full, 4);
-        tc::mbar_init(p_free, 1);
         tc::mbar_init(o_done, 1);
         tc::mbar_init(q_full, 4);
         tc::mbar_init(drain, 1);
@@ -238,7 +250,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
     tc::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
 
-    const int vwarp = I8 ? 10 : 6;
+    const int vwarp = I8 ? 14 : 6;
     if (warp == 4 || warp == vwarp) {
         // ------------------------------------------------------------ TMA producers: warp 4 K, the last warp V
         // (a warp each: a lane that sleeps in its wait would hold up the other producer)
@@ -254,9 +266,11 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                 const int st = j % NS;
                 if (j >= NS && !tc::mbar_wait(&emptyb[st], ((j / NS) - 1) & 1, abort_flag, 256)) break;
                 const int row = rowbase + j * kTcBK;
-                if (I8) {
+                if (I8) {  // two 128-byte-wide swizzled halves of the 256-byte rows
                     tc::mbar_expect_tx(&fullb[st], kTcBK * kTcD);
-                    tc::tma_load_2d((isK ? sRawK : sRawV) + st * 16384, m, &fullb[st], 0, row);
+                    uint8_t* dst = (isK ? sRawK : sRawV) + st * 16384;
+                    tc::tma_load_2d(dst, m, &fullb[st], 0, row);
+                    tc::tma_load_2d(dst + 8192, m, &fullb[st], 128, row);
                 } else {
                     tc::mbar_expect_tx(&fullb[st], kTileBytes);
                     uint8_t* dst = (isK ? sK : sV) + st * kTileBytes;
@@ -277,7 +291,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             const bool bf = p.mma_bf16 != 0;
             const uint32_t id_qk = tc::idesc_f16(bf, false, false, kTcRows, kTcBK);
             const uint32_t id_pv = tc::idesc_f16(bf, false, true, kTcRows, kTcD);
-            const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), aP = tc::smem_u32(sP);
+            const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV);
             bool ok = tc::mbar_wait_spin(q_full, 0, abort_flag);
             if (ok) tc::tc_fence_after();
             int sj = 0, pj = 0;
@@ -289,18 +303,18 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                 // an issued Q K^T would hold the tensor pipe for its whole duration in front of it.
                 if (pj < sj) {
                     const int st = pj % NS, cb = pj & 1;
-                    bool ready = tc::mbar_test(p_full, pj & 1);
+                    bool ready = tc::mbar_test(&p_full[cb], (pj >> 1) & 1);
                     if (ready) ready = I8 ? tc::mbar_test(&vc_full[cb], (pj >> 1) & 1) : tc::mbar_test(&vfull[st], (pj / NS) & 1);
                     if (ready) {
                         tc::tc_fence_after();
                         const uint32_t vbase = aV + (I8 ? cb : st) * kTileBytes;
 #pragma unroll
-                        for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                            const uint64_t da = tc::sdesc_sw128(aP + kk * 32, 16, 1024);
+                        for (int kk = 0; kk < kTcBK / 16; ++kk) {  // A = P, 16-bit pairs over S buffer cb
                             const uint64_t db = tc::sdesc_sw128(vbase + kk * 2048, 8192, 1024);
-                            tc::mma_f16(tmem + kColO, da, db, id_pv, (pj > 0 || kk > 0) ? 1u : 0u);
+                            tc::mma_f16_ts(tmem + kColO, tmem + kColS + cb * kTcBK + kk * 8, db, id_pv,
+                                           (pj > 0 || kk > 0) ? 1u : 0u);
                         }
-                        tc::mma_commit(p_free);
+                        tc::mma_commit(&sp_free[cb]);
                         tc::mma_commit(I8 ? &vc_empty[cb] : &vempty[st]);
                         ++pj;
                         prog = true;
@@ -309,7 +323,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                 if (sj < ntiles) {
                     const int sb = sj & 1, st = sj % NS;
                     bool ready = I8 ? tc::mbar_test(&kc_full[sb], (sj >> 1) & 1) : tc::mbar_test(&kfull[st], (sj / NS) & 1);
-                    if (ready && sj >= 2) ready = tc::mbar_test(&s_free[sb], ((sj >> 1) - 1) & 1);
+                    if (ready && sj >= 2) ready = tc::mbar_test(&sp_free[sb], ((sj >> 1) - 1) & 1);
                     if (ready) {
                         tc::tc_fence_after();
                         const uint32_t kbase = aK + (I8 ? sb : st) * kTileBytes;
@@ -342,24 +356,47 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                 drain_wait(drain, 0);
             }
         }
+    } else if (I8 && warp >= 10 && warp < 14) {
+        // ------------------------------------------------------------ Int8 V converters
+        const int ct = threadIdx.x - 320;
+        for (int j = 0; j < ntiles; ++j) {
+            const int st = j % NS, cb = j & 1;
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / NS) & 1, abort_flag))) break;
+            const int nk = min(kTcBK, k_end - (k_begin + j * kTcBK));
+            if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vc_empty[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
+            convert_i8_tile(sRawV + st * 16384, sV + cb * kTileBytes, nk, ct);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&vempty[st]);
+                tc::mbar_arrive(&vc_full[cb]);
+            }
+        }
     } else if (I8 && warp >= 6 && warp < 10) {
-        // ------------------------------------------------------------ Int8 converter group
+        // ------------------------------------------------------------ Int8 K converters (and every tile's scales)
         const int ct = threadIdx.x - 192;
         const size_t seq_row = ((size_t)b * p.HKV + kvh) * (size_t)p.s_cap;
         const uint16_t* ksg = p.ks[layer] + seq_row;
         const uint16_t* vsg = p.vs[layer] + seq_row;
+        // threads 0-63 fetch the K scales of a tile, 64-127 its V scales, one tile ahead of the conversion so
+        // that the global load's latency overlaps the previous tile's work
+        const uint16_t* scale_src = (ct < 64 ? ksg : vsg) + (ct & 63);
+        auto fetch_scale = [&](int jj) -> uint16_t {
+            const int k = k_begin + jj * kTcBK + (ct & 63);
+            return (jj < ntiles && k < k_end) ? scale_src[k_begin + jj * kTcBK] : (uint16_t)0;
+        };
+        uint16_t sc_next = fetch_scale(0);
         for (int j = 0; j < ntiles; ++j) {
             const int st = j % NS, cb = j & 1, slot = j & 3;
+            const uint16_t sc_bits = sc_next;
+            sc_next = fetch_scale(j + 1);
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kfull[st], (j / NS) & 1, abort_flag))) break;
             const int key0 = k_begin + j * kTcBK;
             const int nk = min(kTcBK, k_end - key0);
             if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kc_empty[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
-            {  // this tile's scales: threads 0-63 the K scales, 64-127 the V scales.  Slot j & 3 was last read by
-               // the softmax of tile j - 4, which finished before P V of tile j - 3 that the previous V
-               // conversion waited for.
-                const int key = ct & 63;
-                const uint16_t* src = ct < 64 ? ksg : vsg;
-                float v = key < nk ? f16_bits_to_f32(src[key0 + key]) : 0.f;
+            {  // this tile's scales into slot j & 3.  The slot was last read by the softmax of tile j - 4: Q K^T of
+               // tile j - 2, done (waited for above), had waited for P V of tile j - 4, which needed that softmax.
+                float v = f16_bits_to_f32(sc_bits);  // keys past the range fetched 0
                 if (ct < 64) v *= 1.4426950408889634f * 0.0625f;  // K scales carry log2(e) / sqrt(256)
                 sScale[slot * 128 + ct] = v;
                 __syncwarp();
@@ -371,15 +408,6 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             if (lane == 0) {
                 tc::mbar_arrive(&kempty[st]);
                 tc::mbar_arrive(&kc_full[cb]);
-            }
-            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / NS) & 1, abort_flag))) break;
-            if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vc_empty[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
-            convert_i8_tile(sRawV + st * 16384, sV + cb * kTileBytes, nk, ct);
-            tc::fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(&vempty[st]);
-                tc::mbar_arrive(&vc_full[cb]);
             }
         }
     } else if (warp < 4) {
@@ -431,9 +459,6 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             tc::tmem_ld32(tmem + lane_base + kColS + sb * kTcBK, s0);
             tc::tmem_ld32(tmem + lane_base + kColS + sb * kTcBK + 32, s1);
             tc::tmem_wait_ld();
-            tc::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&s_free[sb]);
             const float* ksc = sScale + (j & 3) * 128;  // Int8: [64 K scales x log2(e)/16 | 64 V scales]
             if (I8 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&sc_full[j & 3], (j >> 2) & 1, abort_flag))) { ok = false; break; }
 
@@ -491,10 +516,16 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             const float ps = sm2[0];
             l = l * alpha + ps;
 
-            if (j >= 1) {
-                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(p_free, (j - 1) & 1, abort_flag))) { ok = false; break; }
+            // O *= alpha for this warp's rows, once P V of tile j - 1 is done with O.  Its buffer's barrier has
+            // completed the phase before (P V of tile j - 3, which Q K^T of tile j - 1 waited for) and cannot
+            // complete the one after (P V of tile j + 1) before this P is written, so the parity is exact.
+            if (j >= 1 && __any_sync(0xFFFFFFFFu, resc)) {
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&sp_free[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag))) {
+                    ok = false;
+                    break;
+                }
                 tc::tc_fence_after();
-                if (__any_sync(0xFFFFFFFFu, resc)) {  // O *= alpha for this warp's rows
+                {
 #pragma unroll 1
                     for (int ch = 0; ch < 8; ++ch) {
                         uint32_t o[32];
@@ -517,14 +548,13 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                     *reinterpret_cast<uint4*>(vb + (chunk >> 3) * 8192 + row * 128 + (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch)
-                *reinterpret_cast<uint4*>(sP + r * 128 + ((ch ^ (r & 7)) << 4)) =
-                    make_uint4(pk[4 * ch], pk[4 * ch + 1], pk[4 * ch + 2], pk[4 * ch + 3]);
-            tc::fence_proxy_async_smem();
+            // P over the first 32 columns of this tile's S buffer (read above), 16-bit pairs: the A operand of P V
+            tc::tmem_st32(tmem + lane_base + kColS + sb * kTcBK, pk);
+            tc::tmem_wait_st();
+            if (!I8 && c0 + kTcBK > k_end) tc::fence_proxy_async_smem();  // the zeroed V rows
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(p_full);
+            if (lane == 0) tc::mbar_arrive(&p_full[sb]);
         }
         if (ok && __all_sync(0xFFFFFFFFu, tc::mbar_wait(o_done, 0, abort_flag))) {
             tc::tc_fence_after();
@@ -966,18 +996,18 @@ static EncodeTiledFn encode_fn() {
 // 2-D map over all (sequence, kv head, position) rows of one cache buffer:
 // [B * HKV * s_cap rows, 256 columns].  16-bit caches: boxes of 64 columns x
 // 64 rows with the 128-byte swizzle the MMA operands use.  Int8 caches:
-// whole 256-byte rows, 64 rows per box, unswizzled (the converter re-lays
-// them out).
+// boxes of 128 bytes x 64 rows, 128-byte swizzled too (bank-conflict-free
+// reads for the converter, which re-lays them out as fp16 operand tiles).
 static bool make_kv_map(CUtensorMap* m, const void* base, long long rows, bool i8) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)kTcD, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)kTcD * (i8 ? 1 : 2)};
-    cuuint32_t box[2] = {i8 ? (cuuint32_t)kTcD : 64u, (cuuint32_t)kTcBK};
+    cuuint32_t box[2] = {i8 ? 128u : 64u, (cuuint32_t)kTcBK};
     cuuint32_t es[2] = {1, 1};
     return enc(m, i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               i8 ? CU_TENSOR_MAP_SWIZZLE_NONE : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
