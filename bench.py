@@ -296,25 +296,26 @@ def run_e2e(args, wl, stream):
     import torch
 
     vr, cfg = wl.vr, wl.cfg
-    pin = lambda t: t.detach().cpu().pin_memory()
-    h_par, h_tok, h_hid = pin(vr.parents), pin(vr.tokens), pin(vr.hidden)
-    h_q = [pin(q) for q in vr.q]
-    outs = vr.outs
-    h_out = {k: torch.empty(outs[k].shape, dtype=outs[k].dtype).pin_memory() for k in ("path", "path_len", "emitted", "argmax")}
-    h2d = sum(t.numel() * t.element_size() for t in [h_par, h_tok, h_hid] + h_q)
-    d2h = sum(t.numel() * t.element_size() for t in h_out.values())
-    moved = any(p != list(range(len(p))) for p in wl.round["paths"])
+    # the round's inputs (parents, tokens, hidden, Q per layer, ...) are one device buffer: one pinned H2D copy;
+    # its int32 results (path, path_len, emitted, argmax) one block: one D2H copy
+    h_in = wl.inputs.detach().cpu().pin_memory()
+    res = vr.outs["result"]
+    h_res = torch.empty(res.shape, dtype=res.dtype).pin_memory()
+    h2d = h_in.numel() * h_in.element_size()
+    d2h = h_res.numel() * h_res.element_size()
+
+    if args.graph:  # the public capture / replay pair: one graph of the round's calls over its buffers
+        vr.capture()
+        torch.cuda.synchronize()
 
     def e2e_step():
         wl.restore_tail()
-        vr.parents.copy_(h_par, non_blocking=True)
-        vr.tokens.copy_(h_tok, non_blocking=True)
-        vr.hidden.copy_(h_hid, non_blocking=True)
-        for d, h in zip(vr.q, h_q):
-            d.copy_(h, non_blocking=True)
-        vr.run()
-        for k, h in h_out.items():
-            h.copy_(outs[k], non_blocking=True)
+        wl.inputs.copy_(h_in, non_blocking=True)
+        if args.graph:
+            vr.replay()
+        else:
+            vr.run()
+        h_res.copy_(res, non_blocking=True)
 
     for _ in range(3):
         e2e_step()
@@ -328,7 +329,8 @@ def run_e2e(args, wl, stream):
     torch.cuda.synchronize()
     ms = t0.elapsed_time(t1) / n
     return {"value": cfg.rows / (ms * 1e-3), "unit": "nodes/s", "ms_per_step": ms, "steps": n,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "launch": "VerifyRound.replay (cuda graph)" if args.graph else "VerifyRound.run (eager)"}
 
 
 # ----------------------------------------------------------------------------- oracle on the host

@@ -65,20 +65,23 @@ def alloc_cache(cfg: Config, layer: int, s_cap: int, device) -> dict:
     return out
 
 
-def alloc_q(cfg: Config, layer: int, device) -> torch.Tensor:
-    t = torch.empty(cfg.B, cfg.T, cfg.HQ, cfg.D, dtype=torch.bfloat16, device=device)
+def alloc_q(cfg: Config, layer: int, device, out: torch.Tensor | None = None) -> torch.Tensor:
+    """Q of one layer [B, T, HQ, D] bf16, filled into ``out`` when given (a view into a larger buffer)."""
+    t = out if out is not None else torch.empty(cfg.B, cfg.T, cfg.HQ, cfg.D, dtype=torch.bfloat16, device=device)
     fill(t, NORMAL_BF16, st.key(cfg, st.KIND_Q, layer), (1, 1, cfg.B * cfg.T * cfg.HQ, cfg.D), (0, 0, cfg.D))
     return t
 
 
-def alloc_new_kv(cfg: Config, layer: int, device) -> dict:
-    """The block's new K and V rows [B, T, HKV, D] bf16 (inputs of the block append)."""
-    out = {}
+def alloc_new_kv(cfg: Config, layer: int, device, out: dict | None = None) -> dict:
+    """The block's new K and V rows [B, T, HKV, D] bf16 (inputs of the block append), filled into ``out``'s
+    tensors when given."""
+    res = {}
     for which, kind in (("k_new", st.KIND_KNEW), ("v_new", st.KIND_VNEW)):
-        t = torch.empty(cfg.B, cfg.T, cfg.HKV, cfg.D, dtype=torch.bfloat16, device=device)
+        t = out[which] if out is not None else torch.empty(cfg.B, cfg.T, cfg.HKV, cfg.D, dtype=torch.bfloat16,
+                                                            device=device)
         fill(t, NORMAL_BF16, st.key(cfg, kind, layer), (1, 1, cfg.B * cfg.T * cfg.HKV, cfg.D), (0, 0, cfg.D))
-        out[which] = t
-    return out
+        res[which] = t
+    return res
 
 
 def alloc_head(cfg: Config, device) -> dict:

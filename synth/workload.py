@@ -18,6 +18,22 @@ def bits_to_bf16(bits: np.ndarray, device) -> torch.Tensor:
     return torch.from_numpy(np.ascontiguousarray(bits).view(np.int16)).view(torch.bfloat16).to(device)
 
 
+def _arena(specs, device, align: int = 256):
+    """One uint8 device buffer holding every (name, shape, dtype) of ``specs`` at ``align``-byte offsets; returns
+    the buffer and a dict of typed views into it."""
+    offs, n = [], 0
+    for _, shape, dt in specs:
+        n = (n + align - 1) // align * align
+        offs.append(n)
+        n += int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+    buf = torch.zeros(max(n, 1), dtype=torch.uint8, device=device)
+    views = {}
+    for (name, shape, dt), o in zip(specs, offs):
+        nb = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        views[name] = buf[o:o + nb].view(dt).view(shape)
+    return buf, views
+
+
 class Workload:
     """All device tensors of ``cfg`` (optionally a subset of layers, extra capacity)."""
 
@@ -30,25 +46,41 @@ class Workload:
         L = n_layers or cfg.n_layers
         self.s_cap = s_cap or cfg.NKV
         self.caches = [sd.alloc_cache(cfg, l, self.s_cap, device) for l in range(L)]
-        self.q = [sd.alloc_q(cfg, l, device) for l in range(L)]
         # cfg.rot_dim > 0: every round appends its block first (Q rotated from q_in into q, K/V rows into [S, S+T))
         self.append = cfg.rot_dim > 0
+        # Every per-round input lives in one device buffer (``inputs``), so that a round's inputs arrive with one
+        # host-to-device copy: parents, tokens, hidden, Q (q_in when appending) and new K/V rows per layer, uniforms.
+        B, T = cfg.B, cfg.T
+        specs = [("parents", (B, T), torch.int32), ("tokens", (B, T), torch.int32),
+                 ("hidden", (cfg.rows, cfg.H), torch.bfloat16)]
+        specs += [(f"q{l}", (B, T, cfg.HQ, cfg.D), torch.bfloat16) for l in range(L)]
+        if self.append:
+            specs += [(f"{w}{l}", (B, T, cfg.HKV, cfg.D), torch.bfloat16) for l in range(L) for w in ("k_new", "v_new")]
+        if cfg.sample:
+            specs.append(("uniforms", (cfg.rows,), torch.float32))
+        self.inputs, views = _arena(specs, device)
+        q_fed = [sd.alloc_q(cfg, l, device, out=views[f"q{l}"]) for l in range(L)]
         self.q_in = self.new_kv = None
         if self.append:
-            self.q_in = self.q
+            self.q_in = q_fed
             self.q = [torch.empty_like(t) for t in self.q_in]
-            self.new_kv = [sd.alloc_new_kv(cfg, l, device) for l in range(L)]
+            self.new_kv = [sd.alloc_new_kv(cfg, l, device, out={w: views[f"{w}{l}"] for w in ("k_new", "v_new")})
+                           for l in range(L)]
+        else:
+            self.q = q_fed
         self.head = sd.alloc_head(cfg, device)
         self.round = trees.make_round(cfg, round_id)
         r = self.round
-        self.parents = torch.from_numpy(r["parents"]).to(device)
-        self.tokens = torch.from_numpy(r["tokens"]).to(device)
-        self.hidden = bits_to_bf16(r["hidden"], device)
+        self.parents, self.tokens, self.hidden = views["parents"], views["tokens"], views["hidden"]
+        self.parents.copy_(torch.from_numpy(r["parents"]))
+        self.tokens.copy_(torch.from_numpy(r["tokens"]))
+        self.hidden.copy_(bits_to_bf16(r["hidden"], "cpu"))
         self.kv_len = torch.full((cfg.B,), cfg.S if self.append else cfg.NKV, dtype=torch.int32, device=device)
         self.uniforms = None
         if cfg.sample:  # sampled verification: one uniform per node and round
             from . import tensors as st
-            self.uniforms = torch.from_numpy(st.node_uniforms(cfg, round_id)).to(device)
+            self.uniforms = views["uniforms"]
+            self.uniforms.copy_(torch.from_numpy(st.node_uniforms(cfg, round_id)))
         i8 = cfg.kv_dtype == I8
         self.vr = VerifyRound(
             T=cfg.T, HQ=cfg.HQ, HKV=cfg.HKV, D=cfg.D, V=cfg.V, kv_dtype=cfg.kv_dtype, w_dtype=cfg.w_dtype,

@@ -70,6 +70,29 @@ def test_tiny_every_round(gpu_lib):
         assert rep["ok"], rep
 
 
+@pytest.mark.parametrize("idx", [0, 2])
+def test_replayed_rounds_match_the_oracle(gpu_lib, idx):
+    """One captured graph serves every later round: new inputs copied into the buffers, then replay()."""
+    cfg = configs.CONFIGS[idx]
+    if idx:
+        cfg = configs.scaled(cfg, n_layers=2)
+    wl = Workload(cfg)
+    wl.save_tail()
+    _run(wl)  # one eager round on this stream before the capture (loads the kernels)
+    wl.restore_tail()
+    wl.vr.capture()
+    torch.cuda.synchronize()
+    for rid in range(4):
+        wl.restore_tail()
+        wl.set_round(rid)
+        out = wl.vr.replay()
+        torch.cuda.synchronize()
+        rep = check_round(wl, out, layers=[0], attn_rows="all" if cfg.T <= 16 else 4)
+        assert rep["ok"], (rid, rep)
+    del wl
+    _free()
+
+
 def test_tiny_splits_and_ragged_capacity(gpu_lib):
     cfg = configs.CONFIGS[0]
     for splits in (1, 2, 3):

@@ -278,6 +278,8 @@ class VerifyRound:
 
     Caches (k, v[, k_scale, v_scale]) and the LM head are resident state; the
     per-round inputs are parents, tokens, q (per layer), hidden and kv_len.
+    The int32 results (path, path_len, emitted, argmax) are views into one
+    block, ``outs["result"]``.
     """
     T: int
     HQ: int
@@ -316,8 +318,15 @@ class VerifyRound:
         B, T = self.parents.shape
         z = lambda *s, dt=torch.int32: torch.zeros(*s, dtype=dt, device=dev)
         n = len(self.q)
-        self.outs = dict(anc=z(B, T, dt=torch.int64), depth=z(B, T), argmax=z(B * T), maxlogit=z(B * T, dt=torch.float32),
-                         path=z(B, T), path_len=z(B), emitted=z(B, T), status=z(4),
+        # the round's int32 results share one block (outs["result"]: path, path_len, emitted, argmax, each at a
+        # 64-byte offset), so that a caller reads them back with one copy
+        a16 = lambda m: (m + 15) // 16 * 16
+        BT = B * T
+        res = z(3 * a16(BT) + a16(B))
+        o_len, o_emit, o_arg = a16(BT), a16(BT) + a16(B), 2 * a16(BT) + a16(B)
+        self.outs = dict(anc=z(B, T, dt=torch.int64), depth=z(B, T), argmax=res[o_arg:o_arg + BT],
+                         maxlogit=z(B * T, dt=torch.float32), path=res[:BT].view(B, T), path_len=res[o_len:o_len + B],
+                         emitted=res[o_emit:o_emit + BT].view(B, T), result=res, status=z(4),
                          o=[torch.empty(B, T, self.HQ, self.D, dtype=torch.bfloat16, device=dev) for _ in range(n)])
         self.adesc = attn_desc(self.q, self.k, self.v, self.outs["o"], self.kv_len, self.outs["anc"], T=T, HQ=self.HQ,
                                HKV=self.HKV, D=self.D, kv_dtype=self.kv_dtype, max_kv_len=self.max_kv_len,
@@ -364,3 +373,24 @@ class VerifyRound:
             kv_gather_positions(self.kdesc, self.kv_len, o["path"], o["path_len"], T, dev_status=o["status"],
                                 stream=stream)
         return o
+
+    def capture(self, stages=("mask", "append", "attn", "lm", "walk", "gather")):
+        """Record ``run(stages)`` once as a CUDA graph over this round's buffers.
+
+        Every call reads its per-round inputs (parents, tokens, q, hidden, kv_len, ...) from device memory and
+        takes its launch shapes from sizes fixed at construction, so one graph serves every later round: copy the
+        round's inputs into the buffers, then ``replay()``.  The calls are validated on the host once, here.
+        """
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.run(stages=stages)
+        self._graph = g
+        return g
+
+    def replay(self):
+        """Issue the captured round on the current stream (``capture()`` first)."""
+        g = getattr(self, "_graph", None)
+        if g is None:
+            raise RuntimeError("VerifyRound.replay: capture() has not been called")
+        g.replay()
+        return self.outs
