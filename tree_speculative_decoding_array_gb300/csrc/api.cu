@@ -53,6 +53,7 @@ extern "C" int tsv_version(void) { return 101; }
 namespace tsv {
 
 __global__ void selftest_wait_kernel(int32_t* status) {
+    griddep_begin();
     __shared__ uint64_t bar;
     __shared__ int abort_flag;
     if (threadIdx.x == 0) {
@@ -75,6 +76,6 @@ extern "C" tsv_status tsv_selftest_bounded_wait(int32_t* dev_status, cudaStream_
     using namespace tsv;
     clear_error();
     if (!dev_status) return fail(TSV_EINVAL, "selftest_bounded_wait: dev_status is null");
-    selftest_wait_kernel<<<1, 64, 0, stream>>>(dev_status);
+    launch_pdl(selftest_wait_kernel, 1, 64, 0, stream, dev_status);
     return check_launch("selftest_bounded_wait");
 }

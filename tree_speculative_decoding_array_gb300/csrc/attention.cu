@@ -139,6 +139,7 @@ template <int D>
 __global__ void __launch_bounds__(kAttThreads) attn_simt_kernel(const __grid_constant__ tsv_attn_desc d, int splits,
                                                                 int chunk, float* __restrict__ ws_o,
                                                                 float* __restrict__ ws_ml, int32_t* status) {
+    griddep_begin();
     constexpr int KS = D + 4;                   // padded K row stride (floats)
     constexpr int RPT = kRB * D / 4 / kAttThreads;  // output rows per thread in PV
     static_assert(RPT >= 1, "tile too small");
@@ -330,6 +331,7 @@ __global__ void __launch_bounds__(kAttThreads) attn_simt_kernel(const __grid_con
 // Merge split partials: O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
 __global__ void attn_combine_kernel(const __grid_constant__ tsv_attn_desc d, int splits, const float* __restrict__ ws_o,
                                     const float* __restrict__ ws_ml) {
+    griddep_begin();
     const int rows_unit = (d.HQ / d.HKV) * d.T;
     const int unit = blockIdx.y;
     const int gr = blockIdx.x;
@@ -371,7 +373,7 @@ static void launch_simt(const tsv_attn_desc* d, const AttnGeom& g, float* ws_o, 
     const size_t sm = simt_smem<D>();
     cudaFuncSetAttribute(attn_simt_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
     dim3 grid(g.splits, g.rgs, g.units);
-    attn_simt_kernel<D><<<grid, kAttThreads, sm, stream>>>(*d, g.splits, g.chunk, ws_o, ws_ml, status);
+    launch_pdl(attn_simt_kernel<D>, grid, kAttThreads, sm, stream, *d, g.splits, g.chunk, ws_o, ws_ml, status);
 }
 
 static size_t ws_bytes_for(const tsv_attn_desc* d, const AttnGeom& g) {
@@ -446,7 +448,7 @@ extern "C" tsv_status tsv_tree_verify_attention(const tsv_attn_desc* d, void* wo
         st = launch_tc(d, g.splits, g.chunk, ws_o, ws_ml, dev_status, stream);
         if (st != TSV_OK || g.splits == 1) return st;
         dim3 cg(g.rows_unit, g.units);
-        attn_combine_kernel<<<cg, 128, 0, stream>>>(*d, g.splits, ws_o, ws_ml);
+        launch_pdl(attn_combine_kernel, cg, 128, 0, stream, *d, g.splits, ws_o, ws_ml);
         return check_launch("tree_verify_attention(combine)");
     }
     switch (d->D) {
@@ -457,6 +459,6 @@ extern "C" tsv_status tsv_tree_verify_attention(const tsv_attn_desc* d, void* wo
     st = check_launch("tree_verify_attention");
     if (st != TSV_OK || g.splits == 1) return st;
     dim3 cg(g.rows_unit, g.units);
-    attn_combine_kernel<<<cg, 128, 0, stream>>>(*d, g.splits, ws_o, ws_ml);
+    launch_pdl(attn_combine_kernel, cg, 128, 0, stream, *d, g.splits, ws_o, ws_ml);
     return check_launch("tree_verify_attention(combine)");
 }

@@ -145,6 +145,7 @@ constexpr int kNS = 3;  // stages of the K ring and of the V ring
 
 template <bool I8>
 __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
+    griddep_begin();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // Q, S and P live in TMEM.  16-bit caches: K stages [3 x 32K] at 0, V stages [3 x 32K] at 96K.
@@ -612,6 +613,7 @@ constexpr uint32_t kWKTile = kWK * kTcD * 2;  // 64 KiB
 constexpr int kWSmem = 1024 + 229376 + 512;
 
 __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_constant__ TcParams p) {
+    griddep_begin();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sK = sm;
@@ -1057,13 +1059,13 @@ tsv_status launch_tc(const tsv_attn_desc* d, int splits, int chunk, float* ws_o,
     if (items > 0x7FFFFFFFLL) return fail(TSV_ECAPACITY, "tree_verify_attention: too many work items");
     if (i8) {
         cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-        attn_tc_kernel<true><<<(unsigned)items, kTcThreadsI8, kTcSmem, stream>>>(prm);
+        launch_pdl(attn_tc_kernel<true>, (unsigned)items, kTcThreadsI8, kTcSmem, stream, prm);
     } else if (tc_wide(d)) {
         cudaFuncSetAttribute(attn_tcw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
-        attn_tcw_kernel<<<(unsigned)items, kTcThreads16, kWSmem, stream>>>(prm);
+        launch_pdl(attn_tcw_kernel, (unsigned)items, kTcThreads16, kWSmem, stream, prm);
     } else {
         cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-        attn_tc_kernel<false><<<(unsigned)items, kTcThreads16, kTcSmem, stream>>>(prm);
+        launch_pdl(attn_tc_kernel<false>, (unsigned)items, kTcThreads16, kTcSmem, stream, prm);
     }
     return check_launch("tree_verify_attention(tcgen05)");
 }

@@ -8,10 +8,38 @@
 #include <stdint.h>
 
 #include <climits>
+#include <utility>
 
 #include "../../include/tsv.h"
 
 namespace tsv {
+
+// Programmatic dependent launch.  Every kernel of the library is launched with launch_pdl() and begins with
+// griddep_begin(): griddepcontrol.wait returns once the kernel before it on the stream has completed and its
+// memory is visible (at once when there is no such kernel), and launch_dependents then lets the next kernel's
+// CTAs be scheduled while this one runs, so that launches and ramp-ups overlap the tails of their predecessors.
+// Nothing a kernel reads or writes in global memory, and no TMEM allocation, comes before the wait: a waiting
+// CTA holds no resource that the kernel it waits for could need.
+__device__ __forceinline__ void griddep_begin() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                              A&&... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<A>(args)...);
+}
 
 // Records the reason of a failed call for tsv_last_error() (per host thread).
 tsv_status fail(tsv_status st, const char* fmt, ...);

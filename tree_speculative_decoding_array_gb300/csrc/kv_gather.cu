@@ -63,6 +63,7 @@ __global__ void __launch_bounds__(kGatherThreads) kv_gather_kernel(const __grid_
                                                                    const int32_t* __restrict__ path,
                                                                    const int32_t* __restrict__ path_len, int T,
                                                                    int32_t* status) {
+    griddep_begin();
     __shared__ uint4 buf[TSV_MAX_T * kMaxRowBytes / 16];
     __shared__ uint16_t sbuf[TSV_MAX_T];
     __shared__ int sp[TSV_MAX_T];
@@ -104,6 +105,7 @@ __global__ void __launch_bounds__(kGatherThreads) kv_gather_kernel(const __grid_
 
 __global__ void kv_len_update_kernel(int32_t* __restrict__ kv_len, const int32_t* __restrict__ path,
                                      const int32_t* __restrict__ path_len, int B, int T, int64_t s_cap) {
+    griddep_begin();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B) return;
     const GatherCheck g = gather_check(kv_len, path, path_len, b, T, s_cap, nullptr);
@@ -142,9 +144,9 @@ extern "C" tsv_status tsv_kv_gather_positions(const tsv_kv_desc* kv, int32_t* kv
     const long long units = (long long)kv->n_layers * kv->B * kv->HKV;
     if (units > 0x7FFFFFFFLL) return fail(TSV_ECAPACITY, "kv_gather_positions: too many (layer, seq, head) units");
     dim3 grid((unsigned)units, 2);
-    kv_gather_kernel<<<grid, kGatherThreads, 0, stream>>>(*kv, kv_len, path, path_len, T, dev_status);
+    launch_pdl(kv_gather_kernel, grid, kGatherThreads, 0, stream, *kv, kv_len, path, path_len, T, dev_status);
     tsv_status st = check_launch("kv_gather_positions");
     if (st != TSV_OK) return st;
-    kv_len_update_kernel<<<(kv->B + 127) / 128, 128, 0, stream>>>(kv_len, path, path_len, kv->B, T, kv->s_cap);
+    launch_pdl(kv_len_update_kernel, (kv->B + 127) / 128, 128, 0, stream, kv_len, path, path_len, kv->B, T, kv->s_cap);
     return check_launch("kv_gather_positions(kv_len)");
 }

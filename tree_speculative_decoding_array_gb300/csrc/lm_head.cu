@@ -82,6 +82,7 @@ __global__ void __launch_bounds__(kLmThreads, R <= 4 ? 3 : 2) lm_gemv16_kernel(c
                                                                int V, const uint16_t* __restrict__ W,
                                                                unsigned long long* __restrict__ best, int r0,
                                                                float* __restrict__ logits) {
+    griddep_begin();
     extern __shared__ uint4 smem[];
     __shared__ unsigned long long s_best[8];
     uint4* hs = smem;  // [R][H/8]
@@ -165,6 +166,7 @@ __global__ void __launch_bounds__(kLmThreads, R <= 4 ? 3 : 2) lm_gemv_q4_kernel(
                                                                 const uint16_t* __restrict__ biases,
                                                                 unsigned long long* __restrict__ best, int r0,
                                                                 float* __restrict__ logits) {
+    griddep_begin();
     extern __shared__ uint4 smem[];
     __shared__ unsigned long long s_best[8];
     const int nvec = H >> 5;  // 32-code vectors per row
@@ -235,8 +237,16 @@ __global__ void __launch_bounds__(kLmThreads, R <= 4 ? 3 : 2) lm_gemv_q4_kernel(
     merge_best<R>(mine, s_best, best, r0, rows);
 }
 
+// best[0 .. rows) = 0, the neutral element of the packed-key maximum (a kernel, not a memset, so that the
+// launches around it keep their programmatic overlap).
+__global__ void lm_zero_best_kernel(unsigned long long* __restrict__ best, int rows) {
+    griddep_begin();
+    for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) best[r] = 0ull;
+}
+
 __global__ void lm_unpack_kernel(const unsigned long long* __restrict__ best, int rows, int32_t* __restrict__ argmax,
                                  float* __restrict__ maxlogit) {
+    griddep_begin();
     const int r = blockIdx.x * blockDim.x + threadIdx.x;
     if (r >= rows) return;
     const unsigned long long k = best[r];
@@ -254,18 +264,18 @@ static void launch_group(int grid_unused, cudaStream_t st, const uint16_t* hidde
     if (w_dtype == TSV_Q4_G64) {
         const size_t sm = (size_t)R * (H >> 3) * 16 + (size_t)R * (H >> 5) * 4;
         cudaFuncSetAttribute(lm_gemv_q4_kernel<R>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-        lm_gemv_q4_kernel<R><<<grid, kLmThreads, sm, st>>>(hidden, rows, H, V, (const uint8_t*)W,
+        launch_pdl(lm_gemv_q4_kernel<R>, grid, kLmThreads, sm, st, hidden, rows, H, V, (const uint8_t*)W,
                                                            (const uint16_t*)scales, (const uint16_t*)biases, best, r0,
                                                            logits);
     } else {
         const size_t sm = (size_t)R * (H >> 3) * 16;
         if (w_dtype == TSV_BF16) {
             cudaFuncSetAttribute(lm_gemv16_kernel<R, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-            lm_gemv16_kernel<R, true><<<grid, kLmThreads, sm, st>>>(hidden, rows, H, V, (const uint16_t*)W, best, r0,
+            launch_pdl(lm_gemv16_kernel<R, true>, grid, kLmThreads, sm, st, hidden, rows, H, V, (const uint16_t*)W, best, r0,
                                                                     logits);
         } else {
             cudaFuncSetAttribute(lm_gemv16_kernel<R, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm);
-            lm_gemv16_kernel<R, false><<<grid, kLmThreads, sm, st>>>(hidden, rows, H, V, (const uint16_t*)W, best, r0,
+            launch_pdl(lm_gemv16_kernel<R, false>, grid, kLmThreads, sm, st, hidden, rows, H, V, (const uint16_t*)W, best, r0,
                                                                      logits);
         }
     }
@@ -311,8 +321,7 @@ static tsv_status lm_head_run(const char* name, const void* hidden, int32_t rows
     if (ws_bytes < best_bytes(rows))
         return fail(TSV_ECAPACITY, "%s: workspace %zu < %zu bytes", name, ws_bytes, best_bytes(rows));
     unsigned long long* best = (unsigned long long*)workspace;
-    if (cudaMemsetAsync(best, 0, (size_t)rows * sizeof(unsigned long long), stream) != cudaSuccess)
-        return check_launch(name);
+    launch_pdl(lm_zero_best_kernel, std::min((rows + 255) / 256, sm_count()), 256, 0, stream, best, rows);
     // More than one 8-row pass: the tensor-core kernel, when the workspace also holds what it needs.
     const bool sb_aligned = w_dtype != TSV_Q4_G64 || ((((uintptr_t)scales | (uintptr_t)biases) & 15) == 0);
     if (lm_tc_applies(rows, H, V, w_dtype) && sb_aligned &&
@@ -320,7 +329,7 @@ static tsv_status lm_head_run(const char* name, const void* hidden, int32_t rows
         tsv_status st = launch_lm_tc(hidden, rows, H, V, w_dtype, W, scales, biases, best, logits,
                                      (char*)workspace + best_bytes(rows), stream);
         if (st != TSV_OK || !argmax) return st;
-        lm_unpack_kernel<<<(rows + 127) / 128, 128, 0, stream>>>(best, rows, argmax, maxlogit);
+        launch_pdl(lm_unpack_kernel, (rows + 127) / 128, 128, 0, stream, best, rows, argmax, maxlogit);
         return check_launch(name);
     }
     const int grid = sm_count() * 4;
@@ -336,7 +345,7 @@ static tsv_status lm_head_run(const char* name, const void* hidden, int32_t rows
         if (st != TSV_OK) return st;
     }
     if (!argmax) return TSV_OK;
-    lm_unpack_kernel<<<(rows + 127) / 128, 128, 0, stream>>>(best, rows, argmax, maxlogit);
+    launch_pdl(lm_unpack_kernel, (rows + 127) / 128, 128, 0, stream, best, rows, argmax, maxlogit);
     return check_launch(name);
 }
 

@@ -97,6 +97,7 @@ struct LmTcParams {
 // Shared memory: [TMA ring: stages x (W block 16 KB | hidden block NP x 128 B)] ... [bests | barriers]
 template <bool LOGITS>
 __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_constant__ LmTcParams p) {
+    griddep_begin();
     const int S = p.stages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
@@ -264,6 +265,7 @@ __device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
 // (each M=128 MMA occupies the tensor pipe ~100 cycles at these N; per-k-block barrier traffic would double it).
 template <bool LOGITS>
 __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_constant__ LmQ4Params p) {
+    griddep_begin();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* wring = sm;
@@ -493,6 +495,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
 
 // bf16 hidden rows -> fp16 copy (operand type of the fp16 MMA).
 __global__ void hidden_to_f16_kernel(const uint16_t* __restrict__ in, uint16_t* __restrict__ out, size_t n) {
+    griddep_begin();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n / 2; i += (size_t)gridDim.x * blockDim.x) {
         const uint32_t w = reinterpret_cast<const uint32_t*>(in)[i];
         __half2 h = __floats2half2_rn(bf16_lo(w), bf16_hi(w));
@@ -502,6 +505,7 @@ __global__ void hidden_to_f16_kernel(const uint16_t* __restrict__ in, uint16_t* 
 
 // bf16 hidden rows -> fp16 copy with every 8 features in the 4-bit converter's order (0,4,1,5,2,6,3,7).
 __global__ void hidden_to_f16_q4order_kernel(const uint4* __restrict__ in, uint4* __restrict__ out, size_t n8) {
+    griddep_begin();
     for (size_t i = blockIdx.x * (size_t)blockDim.x + threadIdx.x; i < n8; i += (size_t)gridDim.x * blockDim.x) {
         const uint4 w = in[i];
         const __half2 a = __floats2half2_rn(bf16_lo(w.x), bf16_lo(w.z));  // features 0, 4
@@ -580,7 +584,7 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
     if (GK < 1) return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the 4-bit pipeline");
 
     const size_t n8 = (size_t)rows * H / 8;
-    hidden_to_f16_q4order_kernel<<<sm_count() * 4, 256, 0, stream>>>((const uint4*)hidden, (uint4*)extra, n8);
+    launch_pdl(hidden_to_f16_q4order_kernel, sm_count() * 4, 256, 0, stream, (const uint4*)hidden, (uint4*)extra, n8);
     tsv_status st = check_launch("lm_head_argmax(hidden fp16)");
     if (st != TSV_OK) return st;
 
@@ -609,10 +613,10 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
     const int groups = sms / nchunks > 0 ? sms / nchunks : 1;
     if (logits) {
         cudaFuncSetAttribute(lm_q4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
-        lm_q4_kernel<true><<<groups * nchunks, kQ4Threads, kLmSmem, stream>>>(prm);
+        launch_pdl(lm_q4_kernel<true>, groups * nchunks, kQ4Threads, kLmSmem, stream, prm);
     } else {
         cudaFuncSetAttribute(lm_q4_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
-        lm_q4_kernel<false><<<groups * nchunks, kQ4Threads, kLmSmem, stream>>>(prm);
+        launch_pdl(lm_q4_kernel<false>, groups * nchunks, kQ4Threads, kLmSmem, stream, prm);
     }
     return check_launch("lm_head_argmax(tcgen05, 4-bit)");
 }
@@ -627,7 +631,7 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
     const void* hsrc = hidden;
     if (w_dtype != TSV_BF16) {  // fp16 MMA: fp16 copy of hidden
         const size_t n = (size_t)rows * H;
-        hidden_to_f16_kernel<<<sm_count() * 4, 256, 0, stream>>>((const uint16_t*)hidden, (uint16_t*)extra, n);
+        launch_pdl(hidden_to_f16_kernel, sm_count() * 4, 256, 0, stream, (const uint16_t*)hidden, (uint16_t*)extra, n);
         tsv_status st = check_launch("lm_head_argmax(hidden fp16)");
         if (st != TSV_OK) return st;
         hsrc = extra;
@@ -654,10 +658,10 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
     const int groups = sms / nchunks > 0 ? sms / nchunks : 1;
     if (logits) {
         cudaFuncSetAttribute(lm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
-        lm_tc_kernel<true><<<groups * nchunks, kLmThreads16, kLmSmem, stream>>>(prm);
+        launch_pdl(lm_tc_kernel<true>, groups * nchunks, kLmThreads16, kLmSmem, stream, prm);
     } else {
         cudaFuncSetAttribute(lm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
-        lm_tc_kernel<false><<<groups * nchunks, kLmThreads16, kLmSmem, stream>>>(prm);
+        launch_pdl(lm_tc_kernel<false>, groups * nchunks, kLmThreads16, kLmSmem, stream, prm);
     }
     return check_launch("lm_head_argmax(tcgen05)");
 }

@@ -47,6 +47,7 @@ template <bool FROM_LOGITS>
 __global__ void __launch_bounds__(kSortThreads) topk_chunk_kernel(const void* __restrict__ in, int n, int K,
                                                                   unsigned long long* __restrict__ out,
                                                                   float2* __restrict__ lse_part) {
+    griddep_begin();
     __shared__ unsigned long long wtop[kSortThreads / 32][kMaxTopK];
     __shared__ float2 wlse[kSortThreads / 32];
     const int row = blockIdx.y, ch = blockIdx.x;
@@ -124,6 +125,7 @@ __global__ void __launch_bounds__(kSortThreads) topk_chunk_kernel(const void* __
 // One warp per row: the node's draw from its top K keys (sorted, largest first).
 __global__ void nucleus_draw_kernel(const unsigned long long* __restrict__ top, int rows, int K, float inv_temp,
                                     float top_p, const float* __restrict__ uniforms, int32_t* __restrict__ tokens) {
+    griddep_begin();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= rows) return;
@@ -189,20 +191,20 @@ extern "C" tsv_status tsv_sample_nucleus(const float* logits, int32_t rows, int3
     unsigned long long* buf[2] = {(unsigned long long*)workspace, (unsigned long long*)((char*)workspace + need / 2)};
     int cur = 0;
     int nch = chunks_of(V);
-    topk_chunk_kernel<true><<<dim3(nch, rows), kSortThreads, 0, stream>>>(logits, V, K, buf[cur], nullptr);
+    launch_pdl(topk_chunk_kernel<true>, dim3(nch, rows), kSortThreads, 0, stream, logits, V, K, buf[cur], nullptr);
     tsv_status st = check_launch("sample_nucleus(top-k)");
     if (st != TSV_OK) return st;
     long long n = (long long)nch * K;  // survivors per row
     while (nch > 1) {
         nch = chunks_of(n);
-        topk_chunk_kernel<false><<<dim3(nch, rows), kSortThreads, 0, stream>>>(buf[cur], (int)n, K, buf[cur ^ 1],
+        launch_pdl(topk_chunk_kernel<false>, dim3(nch, rows), kSortThreads, 0, stream, buf[cur], (int)n, K, buf[cur ^ 1],
                                                                               nullptr);
         st = check_launch("sample_nucleus(top-k merge)");
         if (st != TSV_OK) return st;
         cur ^= 1;
         n = (long long)nch * K;
     }
-    nucleus_draw_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(buf[cur], rows, K, 1.f / temperature, top_p, uniforms,
+    launch_pdl(nucleus_draw_kernel, (rows + 7) / 8, 256, 0, stream, buf[cur], rows, K, 1.f / temperature, top_p, uniforms,
                                                             tokens);
     return check_launch("sample_nucleus(draw)");
 }
@@ -218,6 +220,7 @@ namespace tsv {
 // One warp per row: log(sum exp(x)) from the chunks' (max, sum) partials, then the row's K children.
 __global__ void draft_children_kernel(const unsigned long long* __restrict__ top, const float2* __restrict__ lse_part,
                                       int nch, int rows, int K, int32_t* __restrict__ tokens, float* __restrict__ logp) {
+    griddep_begin();
     const int lane = threadIdx.x & 31;
     const int row = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (row >= rows) return;
@@ -268,20 +271,20 @@ extern "C" tsv_status tsv_draft_children(const float* draft_logits, int32_t rows
     const int K = top_k;
     const int nch0 = chunks_of(V);
     int cur = 0, nch = nch0;
-    topk_chunk_kernel<true><<<dim3(nch, rows), kSortThreads, 0, stream>>>(draft_logits, V, K, buf[cur], lse_part);
+    launch_pdl(topk_chunk_kernel<true>, dim3(nch, rows), kSortThreads, 0, stream, draft_logits, V, K, buf[cur], lse_part);
     tsv_status st = check_launch("draft_children(top-k)");
     if (st != TSV_OK) return st;
     long long n = (long long)nch * K;
     while (nch > 1) {
         nch = chunks_of(n);
-        topk_chunk_kernel<false><<<dim3(nch, rows), kSortThreads, 0, stream>>>(buf[cur], (int)n, K, buf[cur ^ 1],
+        launch_pdl(topk_chunk_kernel<false>, dim3(nch, rows), kSortThreads, 0, stream, buf[cur], (int)n, K, buf[cur ^ 1],
                                                                               nullptr);
         st = check_launch("draft_children(top-k merge)");
         if (st != TSV_OK) return st;
         cur ^= 1;
         n = (long long)nch * K;
     }
-    draft_children_kernel<<<(rows + 7) / 8, 256, 0, stream>>>(buf[cur], lse_part, nch0, rows, K, child_tokens,
+    launch_pdl(draft_children_kernel, (rows + 7) / 8, 256, 0, stream, buf[cur], lse_part, nch0, rows, K, child_tokens,
                                                               child_logp);
     return check_launch("draft_children");
 }

@@ -132,6 +132,7 @@ struct ApParams {
 template <int D>
 __global__ void __launch_bounds__(kApThreads) tree_append_kernel(const __grid_constant__ ApParams ap,
                                                                  const int32_t* __restrict__ kv_len, int32_t* status) {
+    griddep_begin();
     const tsv_append_desc& d = ap.d;
     constexpr int E = D / 32;  // features per lane
     __shared__ float cs[128], sn[128];
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(kApThreads) tree_append_kernel(const __grid_co
 // kv_len[b] += T for every sequence the append kernel wrote.
 __global__ void append_kv_len_kernel(const int32_t* __restrict__ depth, int B, int T, int64_t s_cap,
                                      int32_t* __restrict__ kv_len) {
+    griddep_begin();
     const int b = blockIdx.x * blockDim.x + threadIdx.x;
     if (b >= B || depth[(size_t)b * T] != 0) return;
     const int S = kv_len[b];
@@ -241,11 +243,11 @@ extern "C" tsv_status tsv_tree_append(const tsv_append_desc* d, int32_t* kv_len,
     ap.d = *d;
     for (int j = 0; j < d->rot_dim / 2; ++j) ap.inv_freq[j] = pow(d->rope_base, -2.0 * j / d->rot_dim);
     const dim3 grid((unsigned)(d->B * d->T), (unsigned)d->n_layers);
-    if (d->D == 64) tree_append_kernel<64><<<grid, kApThreads, 0, stream>>>(ap, kv_len, dev_status);
-    else if (d->D == 128) tree_append_kernel<128><<<grid, kApThreads, 0, stream>>>(ap, kv_len, dev_status);
-    else tree_append_kernel<256><<<grid, kApThreads, 0, stream>>>(ap, kv_len, dev_status);
+    if (d->D == 64) launch_pdl(tree_append_kernel<64>, grid, kApThreads, 0, stream, ap, kv_len, dev_status);
+    else if (d->D == 128) launch_pdl(tree_append_kernel<128>, grid, kApThreads, 0, stream, ap, kv_len, dev_status);
+    else launch_pdl(tree_append_kernel<256>, grid, kApThreads, 0, stream, ap, kv_len, dev_status);
     st = check_launch("tree_append");
     if (st != TSV_OK) return st;
-    append_kv_len_kernel<<<(d->B + 127) / 128, 128, 0, stream>>>(d->depth, d->B, d->T, d->s_cap, kv_len);
+    launch_pdl(append_kv_len_kernel, (d->B + 127) / 128, 128, 0, stream, d->depth, d->B, d->T, d->s_cap, kv_len);
     return check_launch("tree_append(kv_len)");
 }

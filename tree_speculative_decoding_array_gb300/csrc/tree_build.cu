@@ -24,6 +24,7 @@ __global__ void __launch_bounds__(kSelThreads) tree_select_kernel(const int32_t*
                                                                   int32_t* __restrict__ tokens,
                                                                   int32_t* __restrict__ cand_index,
                                                                   int32_t* __restrict__ sizes, int32_t* status) {
+    griddep_begin();
     __shared__ int par[kSelThreads], dep[kSelThreads], where[kSelThreads];
     __shared__ float score[kSelThreads];
     __shared__ unsigned long long key[kSelThreads];
@@ -116,7 +117,7 @@ extern "C" tsv_status tsv_tree_select(const int32_t* cand_parents, const int32_t
     if (B == 0) return TSV_OK;
     if (!cand_parents || !cand_tokens || !cand_logp || !parents || !tokens || !cand_index || !sizes)
         return fail(TSV_EINVAL, "tree_select: null pointer argument");
-    tree_select_kernel<<<B, kSelThreads, 0, stream>>>(cand_parents, cand_tokens, cand_logp, N, T, depth_max, parents,
+    launch_pdl(tree_select_kernel, B, kSelThreads, 0, stream, cand_parents, cand_tokens, cand_logp, N, T, depth_max, parents,
                                                       tokens, cand_index, sizes, dev_status);
     return check_launch("tree_select");
 }

@@ -16,6 +16,7 @@ namespace tsv {
 __global__ void __launch_bounds__(64) tree_mask_kernel(const int32_t* __restrict__ parents, int B, int T,
                                                        uint64_t* __restrict__ anc, int32_t* __restrict__ depth,
                                                        int32_t* status) {
+    griddep_begin();
     __shared__ int par[TSV_MAX_T];
     __shared__ int bad;
     const int b = blockIdx.x;
@@ -52,6 +53,7 @@ __global__ void __launch_bounds__(64) tree_mask_kernel(const int32_t* __restrict
 // ancestor-or-self block columns, -1e9 elsewhere.
 __global__ void dense_mask_kernel(const uint64_t* __restrict__ anc, int B, int T, int offset,
                                   float* __restrict__ mask) {
+    griddep_begin();
     const int W = offset + T;
     const size_t n = (size_t)B * T * W;
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
@@ -75,12 +77,12 @@ extern "C" tsv_status tsv_tree_mask(const int32_t* parents, int32_t B, int32_t T
     if (B == 0 || T == 0) return TSV_OK;
     if (!parents || !anc || !depth) return fail(TSV_EINVAL, "tree_mask: parents, anc and depth must be non-null");
     if (dense_mask && mask_offset < 0) return fail(TSV_EINVAL, "tree_mask: mask_offset=%d < 0", mask_offset);
-    tree_mask_kernel<<<B, 64, 0, stream>>>(parents, B, T, anc, depth, dev_status);
+    launch_pdl(tree_mask_kernel, B, 64, 0, stream, parents, B, T, anc, depth, dev_status);
     tsv_status st = check_launch("tree_mask");
     if (st != TSV_OK || !dense_mask) return st;
     const size_t n = (size_t)B * T * (size_t)(mask_offset + T);
     const int grid = (int)((n + 255) / 256 < (size_t)sm_count() * 8 ? (n + 255) / 256 : (size_t)sm_count() * 8);
-    dense_mask_kernel<<<grid, 256, 0, stream>>>(anc, B, T, mask_offset, dense_mask);
+    launch_pdl(dense_mask_kernel, grid, 256, 0, stream, anc, B, T, mask_offset, dense_mask);
     return check_launch("tree_mask(dense)");
 }
 
@@ -95,6 +97,7 @@ extern "C" tsv_status tsv_tree_mask(const int32_t* parents, int32_t B, int32_t T
 namespace tsv {
 
 __global__ void sliding_band_kernel(float* __restrict__ mask, int B, int T, int offset, int window) {
+    griddep_begin();
     const int W = offset + T;
     const size_t n = (size_t)B * T * W;
     for (size_t e = blockIdx.x * (size_t)blockDim.x + threadIdx.x; e < n; e += (size_t)gridDim.x * blockDim.x) {
@@ -119,6 +122,6 @@ extern "C" tsv_status tsv_sliding_band_mask(float* dense_mask, int32_t B, int32_
     if (!dense_mask) return fail(TSV_EINVAL, "sliding_band_mask: dense_mask is null");
     const size_t n = (size_t)B * T * (size_t)(mask_offset + T);
     const int grid = (int)((n + 255) / 256 < (size_t)sm_count() * 8 ? (n + 255) / 256 : (size_t)sm_count() * 8);
-    sliding_band_kernel<<<grid, 256, 0, stream>>>(dense_mask, B, T, mask_offset, window);
+    launch_pdl(sliding_band_kernel, grid, 256, 0, stream, dense_mask, B, T, mask_offset, window);
     return check_launch("sliding_band_mask");
 }

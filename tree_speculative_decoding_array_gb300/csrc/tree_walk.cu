@@ -19,6 +19,7 @@ __global__ void __launch_bounds__(128) tree_walk_kernel(const int32_t* __restric
                                                         const int32_t* __restrict__ parents, int B, int T,
                                                         int32_t* __restrict__ path, int32_t* __restrict__ path_len,
                                                         int32_t* __restrict__ emitted, int32_t* status) {
+    griddep_begin();
     const int b = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (b >= B) return;
@@ -82,7 +83,7 @@ extern "C" tsv_status tsv_tree_accept_walk(const int32_t* argmax, const int32_t*
         return fail(TSV_EINVAL, "tree_accept_walk: null pointer argument");
     const int warps_per_block = 4;
     const int grid = (B + warps_per_block - 1) / warps_per_block;
-    tree_walk_kernel<<<grid, 32 * warps_per_block, 0, stream>>>(argmax, tokens, parents, B, T, path, path_len,
+    launch_pdl(tree_walk_kernel, grid, 32 * warps_per_block, 0, stream, argmax, tokens, parents, B, T, path, path_len,
                                                                   emitted, dev_status);
     return check_launch("tree_accept_walk");
 }
