@@ -31,7 +31,7 @@ DEFAULT_CONFIG = 1
 # ncu dram bytes (read + write) per launch of the dominant kernel, with the source hash it was measured on
 # (a changed kernel source makes the number stale and it is reported as null).
 TRAFFIC = {
-    ("chain3_27b_bf16", "lm_head.cu"): {"hash": "fd976532ea849480", "bytes": 2542870016 + 2677504},
+    ("chain3_27b_bf16", ("lm_head.cu", "common.cuh")): {"hash": "2530ef189b03e4bc", "bytes": 2543127040 + 2785024},
 }
 
 
@@ -44,10 +44,12 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def src_hash(name):
-    p = os.path.join(ROOT, "tree_speculative_decoding_array_gb300", "csrc", name)
-    with open(p, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+def src_hash(names):
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "tree_speculative_decoding_array_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
 
 
 # ----------------------------------------------------------------------------- clocks
@@ -492,7 +494,7 @@ def main():
     dom_bytes = cfg.lm_bytes() if dom == "lm" else cfg.kv_bytes() + cfg.kv_scale_bytes()
     dom_ms = r["per_kernel"][dom]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    src = {"lm": "lm_head.cu", "attn": "attention.cu"}[dom]
+    src = {"lm": ("lm_head.cu", "common.cuh"), "attn": ("attention.cu", "attention_tc.cu", "common.cuh", "tc.cuh")}[dom]
     tr = TRAFFIC.get((cfg.name, src))
     traffic = tr["bytes"] if tr and tr["hash"] == src_hash(src) else None
     line = {
