@@ -222,14 +222,14 @@ def run_ours(args, rank, world, local_rank):
     e2e = run_e2e(args, wl, stream) if rank == 0 else None
 
     # launches of our kernels per step
-    if cfg.rows > 8:  # tensor-core LM head: (fp16 copy of hidden) + kernel + unpack (sampled: + the sampler)
-        lm_launches = 1 + (cfg.w_dtype != configs.BF16) + 1
-    else:  # CUDA-core GEMV: one launch per group of up to 8 rows + unpack
+    if cfg.rows > 8:  # tensor-core LM head: key reset + (fp16 copy of hidden) + kernel + unpack (sampled: + sampler)
+        lm_launches = 1 + 1 + (cfg.w_dtype != configs.BF16) + 1
+    else:  # CUDA-core GEMV: key reset + one launch per group of up to 8 rows + unpack
         lm_groups, left = 0, cfg.rows
         while left > 0:
             left -= 8 if left >= 8 else (4 if left >= 4 else left)
             lm_groups += 1
-        lm_launches = lm_groups + 1
+        lm_launches = 1 + lm_groups + 1
     if cfg.sample:  # no unpack; top-k passes (one per 4096-entry chunk level) and the draw
         n, passes = cfg.V, 0
         while True:
