@@ -23,7 +23,13 @@
  *   *_workspace_size() call returns.
  * Streams: every call only enqueues work on `stream` (0 = legacy default
  *   stream) and returns without synchronising.  Results are ready when the
- *   stream reaches them.
+ *   stream reaches them.  Calls are capturable in CUDA graphs.  Every kernel
+ *   is launched with programmatic stream serialization: it waits for the
+ *   kernel before it on the stream to complete before it touches memory, and
+ *   lets the kernel after it be scheduled early.  A kernel of the caller's
+ *   launched after a call with that attribute set must therefore wait
+ *   (griddepcontrol.wait / cudaGridDependencySynchronize) before it reads the
+ *   call's outputs; ordinary launches, copies and events need nothing.
  * Host errors: a call returns TSV_OK when its work was enqueued.  Any other
  *   status means nothing was enqueued; tsv_last_error() then names the reason
  *   (a per-thread string, valid until the next call on the same thread).

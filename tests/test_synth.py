@@ -113,3 +113,27 @@ def test_planting_reduced_vocab(idx):
     cfg = configs.scaled(configs.CONFIGS[idx], V=6144, B=min(configs.CONFIGS[idx].B, 2))
     g = _check_planting(cfg, 0)
     assert g > 1.0
+
+
+def test_input_arena_layout():
+    """Per-round inputs share one buffer: 256-byte aligned, disjoint, typed views that write through."""
+    import torch
+    from synth.workload import _arena
+
+    specs = [("parents", (2, 3), torch.int32), ("hidden", (6, 40), torch.bfloat16), ("q0", (2, 3, 4, 8), torch.bfloat16),
+             ("u", (5,), torch.float32)]
+    buf, views = _arena(specs, "cpu")
+    spans = []
+    for name, shape, dt in specs:
+        v = views[name]
+        assert v.dtype == dt and tuple(v.shape) == shape and v.is_contiguous()
+        off = v.data_ptr() - buf.data_ptr()
+        assert off % 256 == 0
+        spans.append((off, off + v.numel() * v.element_size()))
+    spans.sort()
+    assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))
+    assert spans[-1][1] <= buf.numel()
+    views["u"].fill_(1.5)
+    views["parents"].fill_(-1)
+    assert torch.equal(buf[spans[-1][0]:spans[-1][1]].view(torch.float32), torch.full((5,), 1.5))
+    assert int(buf.view(torch.uint8)[:4].view(torch.int32)[0]) == -1

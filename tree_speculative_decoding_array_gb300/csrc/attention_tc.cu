@@ -25,12 +25,13 @@
 //              MN-major).  An S buffer is reused once the P V of the P
 //              written over it is done, so the softmax of tile j + 1 never
 //              waits for the P V of tile j (except to rescale O).
-// Int8 caches (Int8 codes with fp16 per-token scales) use 352 threads: warps
-// 6-9 are a converter group and warp 10 the V producer.  TMA brings the raw
+// Int8 caches (Int8 codes with fp16 per-token scales) use 480 threads: warps
+// 6-9 convert K tiles (and stage each tile's scales, fetched a tile ahead),
+// warps 10-13 convert V tiles, warp 14 is the V producer.  TMA brings the raw
 // int8 tiles (128-byte swizzled halves) into 2-stage staging rings; the
-// converter writes the codes as fp16 (exact) into 2-stage operand rings and
-// the tile's scales (fetched a tile ahead) into shared memory; the softmax
-// warpgroup multiplies S column c by k_scale[c] and folds v_scale[c] into P.
+// converters write the codes as fp16 (exact) into 2-stage operand rings; the
+// softmax warpgroup multiplies S column c by k_scale[c] and folds v_scale[c]
+// into P.
 // Warp-collective roles take every wait decision warp-uniformly (__all_sync),
 // so that tcgen05.ld / __syncwarp never see a partial warp.
 // Every mbarrier wait is bounded in time: on expiry the CTA raises a shared
