@@ -6,7 +6,7 @@ round's tree block is considered appended; the gather advanced kv_len).  Default
 4096-token bf16 prefix at the 27B-like shape (16 layers, 24 q / 4 kv heads, D=256, hidden 5120, bf16 LM head
 248,320 x 5120); its inputs (2.81 GB per round) are larger than L2, so no flush is needed between steps.
 
-python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config I]
+python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--config WORKLOAD]
 Under torchrun every rank runs its own replica on its own GPU (the path has no exchange step); rank 0 prints
 one JSON line.  --impl reference times the fp64 CPU oracle on a bounded sample on the host cores instead.
 """
@@ -26,7 +26,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "tree-verify nodes/s per round and achieved HBM GB/s as fraction of GB300 peak"
-DEFAULT_CONFIG = 1
+DEFAULT_CONFIG = "chain3_27b_bf16"
+DEFAULT_ROUND = {"chain3_27b_bf16": 2}  # the round that accepts the whole chain (3 tokens emitted)
 
 # ncu dram bytes (read + write) per launch of the dominant kernel, with the source hash it was measured on
 # (a changed kernel source makes the number stale and it is reported as null).
@@ -133,7 +134,7 @@ def run_ours(args, rank, world, local_rank):
     tsv.load()
     dev = f"cuda:{local_rank}"
     torch.cuda.set_device(dev)
-    cfg = configs.CONFIGS[args.config]
+    cfg = configs.workload(args.config)
     if args.layers:
         cfg = configs.scaled(cfg, n_layers=args.layers)
     if args.sliding:
@@ -144,7 +145,7 @@ def run_ours(args, rank, world, local_rank):
     if args.sampled:
         t, k, p = args.sampled.split(":")
         cfg = configs.scaled(cfg, name=f"{cfg.name}+sampled{args.sampled}", sample=(float(t), int(k), float(p)))
-    round_id = args.round if args.round is not None else ({1: 2}.get(args.config, 0))
+    round_id = args.round if args.round is not None else DEFAULT_ROUND.get(args.config, 0)
     wl = Workload(cfg, device=dev, round_id=round_id, attn_path=args.attn_path)
     vr = wl.vr
     wl.save_tail()
@@ -342,7 +343,7 @@ sys.path.insert(0, {root!r})
 import numpy as np
 from oracle import attention as oa, lm_head as ol, storage as osd, tree as ot, gather as og
 from synth import configs, tensors, trees
-cfg = configs.CONFIGS[{cfg_idx}]
+cfg = configs.workload({cfg_name!r})
 r = trees.make_round(cfg, {round_id})
 par = r["parents"][0].tolist()
 # inputs for the sample (untimed): one (layer, kv head) unit of attention, a slice of the LM head
@@ -386,8 +387,8 @@ print(json.dumps(dict(t_round=t_round, t_attn_unit=t_attn, t_lm_slice=t_lm, voca
 """
 
 
-def run_oracle(cfg_idx, round_id, budget=6.0, vocab_rows=16384):
-    code = ORACLE_SAMPLE.format(root=ROOT, cfg_idx=cfg_idx, round_id=round_id, vocab_rows=vocab_rows, budget=budget)
+def run_oracle(cfg_name, round_id, budget=6.0, vocab_rows=16384):
+    code = ORACLE_SAMPLE.format(root=ROOT, cfg_name=cfg_name, round_id=round_id, vocab_rows=vocab_rows, budget=budget)
     env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
     t0 = time.perf_counter()
     r = subprocess.run([sys.executable, "-c", code], capture_output=True, text=True, env=env, timeout=900)
@@ -397,7 +398,7 @@ def run_oracle(cfg_idx, round_id, budget=6.0, vocab_rows=16384):
     res = json.loads(r.stdout.strip().splitlines()[-1])
     from synth import configs
 
-    cfg = configs.CONFIGS[cfg_idx]
+    cfg = configs.workload(cfg_name)
     res["nodes_per_s"] = cfg.rows / res["t_round"]
     res["wall_s"] = wall
     res["sample"] = (f"one (layer, seq, kv head) attention unit over {cfg.NKV} keys (x{res['units']} units) and "
@@ -413,7 +414,9 @@ def main():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
-    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG)
+    ap.add_argument("--config", default=DEFAULT_CONFIG, metavar="WORKLOAD",
+                    help="tiny_tree7, chain3_27b_bf16 (default), specinfer16_27b_i8, eagle32x8_27b_f16, "
+                         "eagle64x32_27b_i8")
     ap.add_argument("--round", type=int, default=None)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--attn-path", type=int, default=0, help="0 auto, 1 CUDA-core kernel, 2 tcgen05 kernel")
@@ -443,7 +446,7 @@ def main():
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     from synth import configs
 
-    cfg = configs.CONFIGS[args.config]
+    cfg = configs.workload(args.config)
     if args.layers:
         cfg = configs.scaled(cfg, n_layers=args.layers)
     if args.sliding:
@@ -459,7 +462,7 @@ def main():
               "lm_head": configs.DTYPE_NAMES[cfg.w_dtype], "topology": cfg.topology,
               "l2": f"inputs larger than L2 ({cfg.algorithmic_bytes() / 1e9:.2f} GB read per round), no flush",
               "parallelism": f"replicas x{args.gpus}", "launch": "cuda graph" if args.graph else "eager"}
-    round_id = args.round if args.round is not None else ({1: 2}.get(args.config, 0))
+    round_id = args.round if args.round is not None else DEFAULT_ROUND.get(args.config, 0)
 
     if args.impl == "reference":
         if rank != 0:

@@ -131,6 +131,18 @@ CONFIGS = [
 ]
 
 
+WORKLOADS = {c.name: c for c in CONFIGS}
+
+
+def workload(name: str) -> Config:
+    """The workload of that name (tiny_tree7, chain3_27b_bf16, specinfer16_27b_i8, eagle32x8_27b_f16,
+    eagle64x32_27b_i8)."""
+    try:
+        return WORKLOADS[name]
+    except KeyError:
+        raise KeyError(f"unknown workload {name!r}; known: {', '.join(WORKLOADS)}") from None
+
+
 def scaled(cfg: Config, **kw) -> Config:
     """A copy of ``cfg`` with some fields replaced (reduced-size parity cases)."""
     d = dict(cfg.__dict__)

@@ -34,8 +34,8 @@ def _run(wl, round_id=0):
 
 def test_device_fill_matches_host_generator(gpu_lib):
     from synth import tensors
-    for idx in (0, 2):
-        cfg = configs.scaled(configs.CONFIGS[idx], n_layers=1, S=300, V=777)
+    for name in ("tiny_tree7", "specinfer16_27b_i8"):
+        cfg = configs.scaled(configs.workload(name), n_layers=1, S=300, V=777)
         c = sd.alloc_cache(cfg, 0, cfg.NKV + 5, "cuda")
         for w in ("k", "v"):
             host = tensors.kv_full(cfg, w, 0)
@@ -60,7 +60,7 @@ def test_device_fill_matches_host_generator(gpu_lib):
 
 
 def test_tiny_every_round(gpu_lib):
-    cfg = configs.CONFIGS[0]
+    cfg = configs.workload("tiny_tree7")
     wl = Workload(cfg)
     wl.save_tail()
     for rid in range(6):
@@ -70,11 +70,11 @@ def test_tiny_every_round(gpu_lib):
         assert rep["ok"], rep
 
 
-@pytest.mark.parametrize("idx", [0, 2])
-def test_replayed_rounds_match_the_oracle(gpu_lib, idx):
+@pytest.mark.parametrize("name", ["tiny_tree7", "specinfer16_27b_i8"])
+def test_replayed_rounds_match_the_oracle(gpu_lib, name):
     """One captured graph serves every later round: new inputs copied into the buffers, then replay()."""
-    cfg = configs.CONFIGS[idx]
-    if idx:
+    cfg = configs.workload(name)
+    if cfg.n_layers > 2:
         cfg = configs.scaled(cfg, n_layers=2)
     wl = Workload(cfg)
     wl.save_tail()
@@ -94,7 +94,7 @@ def test_replayed_rounds_match_the_oracle(gpu_lib, idx):
 
 
 def test_tiny_splits_and_ragged_capacity(gpu_lib):
-    cfg = configs.CONFIGS[0]
+    cfg = configs.workload("tiny_tree7")
     for splits in (1, 2, 3):
         wl = Workload(cfg, s_cap=cfg.NKV + 61, splits=splits)
         out = _run(wl)
@@ -104,7 +104,7 @@ def test_tiny_splits_and_ragged_capacity(gpu_lib):
 
 def test_chain3_bf16_every_accept_length(gpu_lib):
     """Linear chain T=3: mask == causal, walk == chain walk, gather == trim_to (identity), all accept lengths."""
-    cfg = configs.CONFIGS[1]
+    cfg = configs.workload("chain3_27b_bf16")
     wl = Workload(cfg)
     wl.save_tail()
     seen = set()
@@ -121,7 +121,7 @@ def test_chain3_bf16_every_accept_length(gpu_lib):
 
 
 def test_specinfer16_int8_q4(gpu_lib):
-    cfg = configs.CONFIGS[2]
+    cfg = configs.workload("specinfer16_27b_i8")
     wl = Workload(cfg)
     wl.save_tail()
     accepts = set()
@@ -138,7 +138,7 @@ def test_specinfer16_int8_q4(gpu_lib):
 
 
 def test_eagle32x8_f16(gpu_lib):
-    cfg = configs.CONFIGS[3]
+    cfg = configs.workload("eagle32x8_27b_f16")
     wl = Workload(cfg)
     out = _run(wl)
     paths = wl.round["paths"]
@@ -150,7 +150,7 @@ def test_eagle32x8_f16(gpu_lib):
 
 
 def test_eagle64x32_int8_q4_long_context(gpu_lib):
-    cfg = configs.CONFIGS[4]
+    cfg = configs.workload("eagle64x32_27b_i8")
     free, total = torch.cuda.mem_get_info()
     need = cfg.kv_bytes() + cfg.kv_scale_bytes() + cfg.lm_bytes() + (4 << 30)
     if free < need:
@@ -165,10 +165,10 @@ def test_eagle64x32_int8_q4_long_context(gpu_lib):
     _free()
 
 
-@pytest.mark.parametrize("idx,window,every", [(3, 1024, 6), (2, 2048, 4)])
-def test_sliding_hybrid_full_size(gpu_lib, idx, window, every):
+@pytest.mark.parametrize("name,window,every", [("eagle32x8_27b_f16", 1024, 6), ("specinfer16_27b_i8", 2048, 4)])
+def test_sliding_hybrid_full_size(gpu_lib, name, window, every):
     """Hybrid sliding/full models at full size: sliding layers see the tree mask intersected with their band."""
-    cfg = configs.with_sliding_layers(configs.CONFIGS[idx], window, every)
+    cfg = configs.with_sliding_layers(configs.workload(name), window, every)
     assert cfg.layer_window(0) == window and cfg.layer_window(every - 1) == 0
     wl = Workload(cfg)
     out = _run(wl)
@@ -178,11 +178,11 @@ def test_sliding_hybrid_full_size(gpu_lib, idx, window, every):
     _free()
 
 
-@pytest.mark.parametrize("idx,rot_dim", [(1, 256), (2, 64)])
-def test_round_that_appends_its_block_full_size(gpu_lib, idx, rot_dim):
+@pytest.mark.parametrize("name,rot_dim", [("chain3_27b_bf16", 256), ("specinfer16_27b_i8", 64)])
+def test_round_that_appends_its_block_full_size(gpu_lib, name, rot_dim):
     """A round that first appends its block (rotary positions S + depth, Int8 quantised on append for the
     specinfer workload), then verifies it: every stage against the oracle of the appended cache."""
-    cfg = configs.scaled(configs.CONFIGS[idx], name=configs.CONFIGS[idx].name + f"+append{rot_dim}", rot_dim=rot_dim)
+    cfg = configs.scaled(configs.workload(name), name=name + f"+append{rot_dim}", rot_dim=rot_dim)
     wl = Workload(cfg)
     assert wl.kv_len.tolist() == [cfg.S] * cfg.B
     out = _run(wl)
@@ -192,8 +192,8 @@ def test_round_that_appends_its_block_full_size(gpu_lib, idx, rot_dim):
     _free()
 
 
-@pytest.mark.parametrize("idx", [1, 2])
-def test_sampled_round_full_size(gpu_lib, idx):
+@pytest.mark.parametrize("name", ["chain3_27b_bf16", "specinfer16_27b_i8"])
+def test_sampled_round_full_size(gpu_lib, name):
     """Sampled verification at full vocabulary: each node's draw (temperature 1, top-k 20, top-p 0.95, its own
     uniform) against the oracle's draw from its own fp64 logits; the walk on those draws.  The GPU logits differ
     from the oracle's by fp32 accumulation (and the 4-bit head's fp16 dequantisation), so a draw may take any
@@ -206,7 +206,7 @@ def test_sampled_round_full_size(gpu_lib, idx):
 
     from .parity import head_rows_fn
 
-    base = configs.CONFIGS[idx]
+    base = configs.workload(name)
     cfg = configs.scaled(base, name=base.name + "+sampled", sample=(1.0, 20, 0.95))
     wl = Workload(cfg)
     out = _run(wl)

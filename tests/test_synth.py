@@ -38,7 +38,7 @@ def test_distributions():
 
 
 def test_slices_match_full_tensors():
-    cfg = configs.CONFIGS[0]
+    cfg = configs.workload("tiny_tree7")
     K = tensors.kv_full(cfg, "k", 0)
     assert np.array_equal(tensors.kv_rows(cfg, "k", 0, 0, 1, 3, 9), K[0, 1, 3:9])
     Q = tensors.q_full(cfg, 0)
@@ -55,9 +55,9 @@ def test_specinfer_topology():
     assert sum(1 for x in d if x == 1) == 2  # rank-0 and rank-1 children of the root
 
 
-@pytest.mark.parametrize("idx", [2, 3, 4])
-def test_best_first_topologies(idx):
-    cfg = configs.CONFIGS[idx]
+@pytest.mark.parametrize("name", ["specinfer16_27b_i8", "eagle32x8_27b_f16", "eagle64x32_27b_i8"])
+def test_best_first_topologies(name):
+    cfg = configs.workload(name)
     r = trees.make_round(cfg, 0, plant=False)
     for b in range(cfg.B):
         par = r["parents"][b].tolist()
@@ -74,8 +74,7 @@ def test_best_first_topologies(idx):
 
 
 def test_walk_finds_planned_path_from_targets():
-    for idx in range(5):
-        cfg = configs.CONFIGS[idx]
+    for cfg in configs.CONFIGS:
         r = trees.make_round(cfg, 1, plant=False)
         for b in range(cfg.B):
             path, _ = ot.accept_walk(r["targets"][b], r["tokens"][b], r["parents"][b])
@@ -104,13 +103,13 @@ def _check_planting(cfg, round_id):
 
 def test_planting_tiny():
     for rid in range(4):
-        _check_planting(configs.CONFIGS[0], rid)
+        _check_planting(configs.workload("tiny_tree7"), rid)
 
 
-@pytest.mark.parametrize("idx", [1, 2, 3])
-def test_planting_reduced_vocab(idx):
+@pytest.mark.parametrize("name", ["chain3_27b_bf16", "specinfer16_27b_i8", "eagle32x8_27b_f16"])
+def test_planting_reduced_vocab(name):
     """The 27B-shaped workloads at hidden 5120 with a 6144-row vocabulary (full vocab: GPU tests)."""
-    cfg = configs.scaled(configs.CONFIGS[idx], V=6144, B=min(configs.CONFIGS[idx].B, 2))
+    cfg = configs.scaled(configs.workload(name), V=6144, B=min(configs.workload(name).B, 2))
     g = _check_planting(cfg, 0)
     assert g > 1.0
 
