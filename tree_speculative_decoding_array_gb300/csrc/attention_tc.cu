@@ -47,8 +47,11 @@ namespace tsv {
 constexpr int kTcRows = 128;
 constexpr int kTcBK = 64;
 constexpr int kTcD = 256;
-constexpr int kTcThreads16 = 224;  // + warp 6: V producer
-constexpr int kTcThreadsI8 = 480;  // + warps 6-9: K converters, 10-13: V converters, warp 14: V producer
+constexpr int kTcThreads16 = 224;  // 128-key kernel: + warp 6: V producer
+// 64-key kernel: 16-bit: warp 6 V producer, warps 7-10 the softmax's second half; Int8: warps 6-9 K converters,
+// 10-13 V converters, warp 14 V producer, warps 15-18 the softmax's second half
+constexpr int kTc64Threads16 = 352;
+constexpr int kTcThreadsI8 = 608;
 constexpr int kTcSmem = 1024 + 215040 + 512;
 constexpr uint32_t kTileBytes = kTcBK * kTcD * 2;  // one K (or V) tile: 32 KiB
 
@@ -145,19 +148,22 @@ __device__ __forceinline__ void convert_i8_tile(const uint8_t* raw, uint8_t* dst
 constexpr int kNS = 3;  // stages of the K ring and of the V ring
 
 template <bool I8>
-__global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
+__global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc_kernel(const __grid_constant__ TcParams p) {
     griddep_begin();
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     // Q, S and P live in TMEM.  16-bit caches: K stages [3 x 32K] at 0, V stages [3 x 32K] at 96K.
     // Int8 caches: fp16 K tiles [2 x 32K] at 0, fp16 V tiles [2 x 32K] at 64K, raw K stages [2 x 16K] at 128K,
-    // raw V stages [2 x 16K] at 160K.
+    // raw V stages [2 x 16K] at 160K.  Both: the softmax halves' exchange [2 slots x 2 halves x 128 rows] fp32
+    // at 192K.
     constexpr int NS = I8 ? 2 : kNS;  // stages of the TMA rings
+    constexpr int kSoftB = I8 ? 15 : 7;  // first warp of the softmax's second half
     uint8_t* sK = sm;
     uint8_t* sV = sm + (I8 ? 65536 : 98304);
     uint8_t* sRawK = sm + 131072;
     uint8_t* sRawV = sm + 163840;
     float* sScale = reinterpret_cast<float*>(sm + 212992);  // Int8: [4 slots][64 K scales x log2(e)/16 | 64 V scales]
+    float* xv = reinterpret_cast<float*>(sm + 196608);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 215040);
     uint64_t* kfull = bars + 0;      // [3] K tile (16-bit) / raw K tile (Int8) landed
     uint64_t* kempty = bars + 3;     // [3] stage free again: after Q K^T (16-bit) / after conversion (Int8)
@@ -176,6 +182,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
     uint64_t* sc_full = bars + 29;   // Int8: [4] scale slot written
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 34);
+    uint64_t* xch = bars + 36;       // [4 lane quarters][2 parities] both softmax halves posted their value
     // TMEM columns: Q [0, 128) as 16-bit pairs, S [128, 192) and [192, 256) (P, 16-bit pairs, over the first 32
     // columns of its S tile once the softmax has read it), O [256, 512).
     constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
@@ -231,13 +238,14 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&s_full[s], 1);
             tc::mbar_init(&sp_free[s], 1);
-            tc::mbar_init(&p_full[s], 4);
+            tc::mbar_init(&p_full[s], 8);  // both softmax halves
             tc::mbar_init(&kc_full[s], 4);
             tc::mbar_init(&kc_empty[s], 1);
             tc::mbar_init(&vc_full[s], 4);
             tc::mbar_init(&vc_empty[s], 1);
         }
         for (int s = 0; s < 4; ++s) tc::mbar_init(&sc_full[s], 4);
+        for (int s = 0; s < 8; ++s) tc::mbar_init(&xch[s], 2);
         tc::mbar_init(o_done, 1);
         tc::mbar_init(q_full, 4);
         tc::mbar_init(drain, 1);
@@ -412,9 +420,17 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                 tc::mbar_arrive(&kc_full[cb]);
             }
         }
-    } else if (warp < 4) {
-        // ------------------------------------------------------------ softmax warpgroup
-        const int r = threadIdx.x;  // row within the tile == TMEM lane
+    } else if (warp < 4 || warp >= kSoftB) {
+        // ------------------------------------------------------------ softmax, in two halves
+        // Half 0 (warps 0-3) takes key columns 0-31 of every tile, half 1 (the last four warps) columns 32-63,
+        // of the same rows.  The two warps owning one TMEM lane quarter exchange their row maxima (and at the
+        // end their row sums) through shared memory, one mbarrier per warp pair and tile parity, so both take
+        // the same lazy-rescale decisions; each rescales and reads out its 128 columns of O and writes its 16
+        // columns of P.  Half 1 writes P over S columns that half 0 reads, so only after the exchange, which
+        // half 0 enters once its scores are in registers.
+        const int h = warp < 4 ? 0 : 1;
+        const int qd = warp & 3;
+        const int r = qd * 32 + lane;  // row within the tile == TMEM lane
         const int gr = row0 + r;
         const bool row_ok = gr < p.R;
         const int node = row_ok ? gr / p.G : 0;
@@ -422,8 +438,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
         const uint64_t anc = row_ok ? p.anc[(size_t)b * T + node] : 0ull;
         const int lo_row = win > 0 ? S + node - win + 1 : INT_MIN;  // sliding band of this row
         const bool bf = p.mma_bf16 != 0;
-        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-        {  // Q row -> TMEM lane r, 16-bit pairs (rounded to fp16 when the MMA runs in fp16)
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        if (h == 0) {  // Q row -> TMEM lane r, 16-bit pairs (rounded to fp16 when the MMA runs in fp16)
             const uint4* src = reinterpret_cast<const uint4*>(p.q[layer] + ((size_t)(b * T + node) * p.HQ + head) * kTcD);
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
@@ -450,6 +466,18 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(q_full);
         }
+        // exchange number jj (one per tile, then one for the row sums): xv[(jj & 1) * 2 + half][row]
+        auto exchange = [&](int jj, float mine, float& other) -> bool {
+            const int slot = jj & 1;
+            xv[(slot * 2 + h) * kTcRows + r] = mine;
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&xch[qd * 2 + slot]);
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&xch[qd * 2 + slot], (jj >> 1) & 1, abort_flag))) return false;
+            tc::tc_fence_after();
+            other = xv[(slot * 2 + (h ^ 1)) * kTcRows + r];
+            return true;
+        };
         const float qk_scale = 1.4426950408889634f * 0.0625f;  // log2(e) / sqrt(256)
         float m_ref = -INFINITY, l = 0.f;
         bool ok = true;
@@ -457,41 +485,40 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             const int sb = j & 1;
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag))) { ok = false; break; }
             tc::tc_fence_after();
-            uint32_t s0[32], s1[32];
-            tc::tmem_ld32(tmem + lane_base + kColS + sb * kTcBK, s0);
-            tc::tmem_ld32(tmem + lane_base + kColS + sb * kTcBK + 32, s1);
+            uint32_t sc[32];
+            tc::tmem_ld32(tmem + lane_base + kColS + sb * kTcBK + h * 32, sc);
             tc::tmem_wait_ld();
-            const float* ksc = sScale + (j & 3) * 128;  // Int8: [64 K scales x log2(e)/16 | 64 V scales]
+            // Int8: this half's 32 K scales (x log2(e)/16); its V scales 64 further
+            const float* ksc = sScale + (j & 3) * 128 + h * 32;
             if (I8 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&sc_full[j & 3], (j >> 2) & 1, abort_flag))) { ok = false; break; }
 
-            const int c0 = k_begin + j * kTcBK;
+            const int ct = k_begin + j * kTcBK;  // first key of the tile
+            const int c0 = ct + h * 32;          // first key of this half
             // Scores in the log2 domain.  Tiles whose 64 keys are all history keys inside the range need no mask.
-            float x[64];
             // (padding rows past the unit's G*T rows take it too: their Q is zero and their results are dropped)
-            if (c0 + kTcBK <= k_end && c0 + kTcBK <= S && c0 >= lo_last) {
+            float x[32];
+            if (ct + kTcBK <= k_end && ct + kTcBK <= S && ct >= lo_last) {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
-                    const float raw = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
-                    x[c] = raw * (I8 ? ksc[c] : qk_scale);
-                }
+                for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(sc[c]) * (I8 ? ksc[c] : qk_scale);
             } else {
 #pragma unroll
-                for (int c = 0; c < 64; ++c) {
+                for (int c = 0; c < 32; ++c) {
                     const int key = c0 + c;
                     bool v = row_ok && key < k_end && key >= lo_row;
                     if (key >= S) v = v && ((anc >> ((key - S) & 63)) & 1ull);
-                    const float raw = __uint_as_float(c < 32 ? s0[c] : s1[c - 32]);
-                    x[c] = v ? raw * (I8 ? ksc[c] : qk_scale) : -INFINITY;
+                    x[c] = v ? __uint_as_float(sc[c]) * (I8 ? ksc[c] : qk_scale) : -INFINITY;
                 }
             }
-            float mx[32];
+            float mx[16];
 #pragma unroll
-            for (int c = 0; c < 32; ++c) mx[c] = fmaxf(x[c], x[c + 32]);
+            for (int c = 0; c < 16; ++c) mx[c] = fmaxf(x[c], x[c + 16]);
 #pragma unroll
-            for (int w = 16; w >= 1; w >>= 1)
+            for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
                 for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
-            const float mt_ = mx[0];
+            float mo;
+            if (!exchange(j, mx[0], mo)) { ok = false; break; }
+            const float mt_ = fmaxf(mx[0], mo);  // the row's tile maximum, the same in both halves
             float alpha = 1.f;
             bool resc = false;
             if (mt_ > m_ref + 8.f) {  // also when m_ref is still -inf
@@ -501,10 +528,10 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
             }
             // m_ref == -inf only while every score so far was masked (then every p below is 0)
             const float msub = m_ref == -INFINITY ? 0.f : m_ref;
-            uint32_t pk[32];
-            float sm2[32];
+            uint32_t pk[16];
+            float sm2[16];
 #pragma unroll
-            for (int c = 0; c < 64; c += 2) {
+            for (int c = 0; c < 32; c += 2) {
                 const float p0 = tc::ex2_approx(x[c] - msub);
                 const float p1 = tc::ex2_approx(x[c + 1] - msub);
                 sm2[c >> 1] = p0 + p1;
@@ -512,58 +539,61 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                 else pk[c >> 1] = pack2(p0, p1, bf);
             }
 #pragma unroll
-            for (int w = 16; w >= 1; w >>= 1)
+            for (int w = 8; w >= 1; w >>= 1)
 #pragma unroll
                 for (int c = 0; c < w; ++c) sm2[c] += sm2[c + w];
-            const float ps = sm2[0];
-            l = l * alpha + ps;
+            l = l * alpha + sm2[0];  // this half's part of the row sum
 
-            // O *= alpha for this warp's rows, once P V of tile j - 1 is done with O.  Its buffer's barrier has
-            // completed the phase before (P V of tile j - 3, which Q K^T of tile j - 1 waited for) and cannot
-            // complete the one after (P V of tile j + 1) before this P is written, so the parity is exact.
+            // O *= alpha for this warp's rows and half of the columns, once P V of tile j - 1 is done with O.  Its
+            // buffer's barrier has completed the phase before (P V of tile j - 3, which Q K^T of tile j - 1 waited
+            // for) and cannot complete the one after (P V of tile j + 1) before this P is written.
             if (j >= 1 && __any_sync(0xFFFFFFFFu, resc)) {
                 if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&sp_free[(j - 1) & 1], ((j - 1) >> 1) & 1, abort_flag))) {
                     ok = false;
                     break;
                 }
                 tc::tc_fence_after();
-                {
 #pragma unroll 1
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
-                        tc::tmem_wait_ld();
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tmem + lane_base + kColO + (h * 4 + ch) * 32, o);
+                    tc::tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tc::tmem_st32(tmem + lane_base + kColO + ch * 32, o);
-                    }
-                    tc::tmem_wait_st();
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tc::tmem_st32(tmem + lane_base + kColO + (h * 4 + ch) * 32, o);
                 }
+                tc::tmem_wait_st();
             }
-            if (!I8 && c0 + kTcBK > k_end) {  // last tile: zero V rows past the key range (their bytes are not ours)
+            const bool zero_v = !I8 && h == 0 && ct + kTcBK > k_end;
+            if (zero_v) {  // last tile: zero V rows past the key range (their bytes are not ours)
                 const int st = j % NS;
                 if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / NS) & 1, abort_flag))) { ok = false; break; }
-                const int nk = k_end - c0;
+                const int nk = k_end - ct;
                 uint8_t* vb = sV + st * kTileBytes;
                 for (int e = r; e < (kTcBK - nk) * 32; e += kTcRows) {
                     const int row = nk + e / 32, chunk = e % 32;
                     *reinterpret_cast<uint4*>(vb + (chunk >> 3) * 8192 + row * 128 + (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
-            // P over the first 32 columns of this tile's S buffer (read above), 16-bit pairs: the A operand of P V
-            tc::tmem_st32(tmem + lane_base + kColS + sb * kTcBK, pk);
+            // this half's 32 keys of P, 16-bit pairs, over S columns [16 h, 16 h + 16) (the A operand of P V)
+            tc::tmem_st16(tmem + lane_base + kColS + sb * kTcBK + h * 16, pk);
             tc::tmem_wait_st();
-            if (!I8 && c0 + kTcBK > k_end) tc::fence_proxy_async_smem();  // the zeroed V rows
+            if (zero_v) tc::fence_proxy_async_smem();  // the zeroed V rows
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&p_full[sb]);
+        }
+        if (ok) {  // the row sum of both halves
+            float lo;
+            if (exchange(ntiles, l, lo)) l += lo;
+            else ok = false;
         }
         if (ok && __all_sync(0xFFFFFFFFu, tc::mbar_wait(o_done, 0, abort_flag))) {
             tc::tc_fence_after();
             const size_t slot = ((size_t)unit * p.splits + split) * p.R + gr;
             const float inv = l > 0.f ? 1.f / l : 0.f;
 #pragma unroll 1
-            for (int ch = 0; ch < 8; ++ch) {
+            for (int ch = h * 4; ch < h * 4 + 4; ++ch) {
                 uint32_t o[32];
                 tc::tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
                 tc::tmem_wait_ld();
@@ -587,13 +617,12 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTcThreads16, 1) attn_tc_k
                                              __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
                 }
             }
-            if (row_ok && p.splits > 1) {
+            if (h == 0 && row_ok && p.splits > 1) {
                 p.ws_ml[2 * slot] = m_ref;
                 p.ws_ml[2 * slot + 1] = l;
             }
         }
     }
-
     __syncthreads();
     if (*abort_flag && threadIdx.x == 0) dev_fail(p.status, TSV_DEV_TIMEOUT, b, blockIdx.x);
     if (warp == 5) {
@@ -1066,7 +1095,7 @@ tsv_status launch_tc(const tsv_attn_desc* d, int splits, int chunk, float* ws_o,
         launch_pdl(attn_tcw_kernel, (unsigned)items, kTcThreads16, kWSmem, stream, prm);
     } else {
         cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-        launch_pdl(attn_tc_kernel<false>, (unsigned)items, kTcThreads16, kTcSmem, stream, prm);
+        launch_pdl(attn_tc_kernel<false>, (unsigned)items, kTc64Threads16, kTcSmem, stream, prm);
     }
     return check_launch("tree_verify_attention(tcgen05)");
 }
