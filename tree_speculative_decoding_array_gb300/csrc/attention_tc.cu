@@ -8,13 +8,17 @@
 // #728, "Earlier shader evidence": split-KV tree attention with fp32 partials
 // and statistics; mlxcel issue #1204, "What this needs" item 1).
 //
-// One CTA = one 128-row tile of one unit and one key range; 224 threads:
-//   warps 0-3  softmax warpgroup: thread r owns query row r = TMEM lane r.
-//              Stores Q into TMEM, reads S from TMEM, applies the
-//              scale and the ancestor bits, runs the online softmax (fp32,
-//              log2 domain, lazy rescale of O when the max grows by > 2^8),
-//              writes P as 16-bit pairs back over its S tile in TMEM,
-//              finally reads O.
+// One CTA = one 128-row tile of one unit and one key range; 352 threads:
+//   warps 0-3  softmax, first half: lane r of warp q owns query row
+//              32 q + r = TMEM lane.  Stores Q into TMEM, reads its 32 of
+//              the tile's 64 S columns from TMEM, applies the scale and the
+//              ancestor bits, runs the online softmax (fp32, log2 domain,
+//              lazy rescale of O when the max grows by > 2^8), writes its
+//              P columns as 16-bit pairs back over the S tile in TMEM,
+//              finally reads out its half of O.
+//   warps 7-10 softmax, second half: the other 32 columns of the same rows;
+//              each pair of warps on one lane quarter exchanges its row
+//              maxima (and at the end its row sums) through shared memory.
 //   warp 4, 6  TMA producers (4: K, 6: V; one lane each): tiles of 64 keys x
 //              256, 128-byte swizzled, each in its own 3-stage ring (a K
 //              stage frees after Q K^T, a V stage after P V).
@@ -25,9 +29,10 @@
 //              MN-major).  An S buffer is reused once the P V of the P
 //              written over it is done, so the softmax of tile j + 1 never
 //              waits for the P V of tile j (except to rescale O).
-// Int8 caches (Int8 codes with fp16 per-token scales) use 480 threads: warps
+// Int8 caches (Int8 codes with fp16 per-token scales) use 608 threads: warps
 // 6-9 convert K tiles (and stage each tile's scales, fetched a tile ahead),
-// warps 10-13 convert V tiles, warp 14 is the V producer.  TMA brings the raw
+// warps 10-13 convert V tiles, warp 14 is the V producer, warps 15-18 the
+// softmax's second half.  TMA brings the raw
 // int8 tiles (128-byte swizzled halves) into 2-stage staging rings; the
 // converters write the codes as fp16 (exact) into 2-stage operand rings; the
 // softmax warpgroup multiplies S column c by k_scale[c] and folds v_scale[c]
