@@ -256,3 +256,111 @@ def test_sliding_mask_from_caller_properties():
             for i in range(T):
                 cols = np.flatnonzero(got[i] == 0.0).tolist()
                 assert cols == ot.visible_keys(par, i, S, window)
+
+
+# ----------------------------------------------------------------------------- rounding to 16-bit storage
+# Values are decoded from bit patterns with integer arithmetic (sign, biased exponent, fraction), independently
+# of the oracle's view-based decoders; each pattern's neighbours fix where round-to-nearest-even must land.
+def bf16_value(p: int) -> float:
+    s, e, m = p >> 15, (p >> 7) & 0xFF, p & 0x7F
+    assert 0 < e < 255, "normal range only"
+    return (-1.0) ** s * math.ldexp(128 + m, e - 127 - 7)
+
+
+def f16_value(p: int) -> float:
+    s, e, m = p >> 15, (p >> 10) & 0x1F, p & 0x3FF
+    assert e < 31
+    mag = math.ldexp(m, -24) if e == 0 else math.ldexp(1024 + m, e - 15 - 10)
+    return -mag if s else mag
+
+
+def _nearest_even_cases(value, patterns):
+    """(x, expected) pairs around every positive pattern p: inside half an ulp -> p, beyond -> the neighbour,
+    exactly half an ulp -> whichever of the two has an even fraction (ties to even)."""
+    cases = []
+    for p in patterns:
+        v, up = value(p), value(p + 1)
+        dn = value(p - 1) if p > 0 else None
+        even = (p & 1) == 0
+        cases += [(v, v), (v + 0.49 * (up - v), v), (v + 0.51 * (up - v), up),
+                  (v + 0.5 * (up - v), v if even else up)]
+        if dn is not None:
+            cases += [(v - 0.49 * (v - dn), v), (v - 0.51 * (v - dn), dn), (v - 0.5 * (v - dn), v if even else dn)]
+    return cases + [(-x, -y) for x, y in cases]
+
+
+def test_round_bf16_hand_decoded_values():
+    r = lambda x: float(osd.round_bf16(np.array([x]))[0])
+    assert r(1.0 + 2.0 ** -8) == 1.0                      # tie between 0x3F80 and 0x3F81 -> even 0x3F80
+    assert r(1.0 + 3 * 2.0 ** -8) == 1.0 + 2.0 ** -6      # tie between 0x3F81 and 0x3F82 -> even 0x3F82
+    assert r(1.0 + 2.0 ** -8 + 2.0 ** -30) == 1.0 + 2.0 ** -7  # just above the tie -> 0x3F81
+    assert r(2.0 - 2.0 ** -10) == 2.0                     # just under a power of two rounds up across it
+    assert r(2.0 - 3 * 2.0 ** -9) == bf16_value(0x3FFF) == 1.9921875
+    assert r(1.0 / 3.0) == bf16_value(0x3EAB) == 0.333984375
+    assert r(-(1.0 + 2.0 ** -8 + 2.0 ** -30)) == bf16_value(0xBF81)
+    assert r(3.0e38) == bf16_value(0x7F62)                # large normal values keep 8 significant bits
+
+
+def test_round_bf16_lands_on_the_nearest_even_neighbour():
+    rng = np.random.default_rng(11)
+    pats = [0x3F80, 0x3F81, 0x3FFF, 0x4000, 0x0081, 0x7F7E, 0x3E80]
+    pats += [int(p) for p in rng.integers(0x0081, 0x7F7E, size=300)]
+    cases = _nearest_even_cases(bf16_value, pats)
+    x = np.array([c[0] for c in cases])
+    want = np.array([c[1] for c in cases])
+    assert np.array_equal(osd.round_bf16(x), want)
+
+
+def test_round_bf16_agrees_with_torch_on_float32_inputs():
+    # fp32 -> bf16 in torch is round-to-nearest-even with no intermediate rounding
+    rng = np.random.default_rng(12)
+    bits = rng.integers(0x00800000, 0x7F000000, size=20000, dtype=np.int64).astype(np.uint32)
+    bits |= (rng.integers(0, 2, size=bits.size).astype(np.uint32) << np.uint32(31))
+    x = bits.view(np.float32)
+    ref = torch.from_numpy(x.copy()).to(torch.bfloat16).to(torch.float64).numpy()
+    assert np.array_equal(osd.round_bf16(x.astype(np.float64)), ref)
+
+
+@pytest.mark.parametrize("fn", ["storage.round_f16", "append.f16_round"])
+def test_round_f16_hand_decoded_values(fn):
+    from oracle import append as oap
+    f = osd.round_f16 if fn == "storage.round_f16" else oap.f16_round
+    r = lambda x: float(f(np.array([x]))[0])
+    assert r(1.0 + 2.0 ** -11) == 1.0                     # tie -> even 0x3C00
+    assert r(1.0 + 3 * 2.0 ** -11) == 1.0 + 2.0 ** -9     # tie -> even 0x3C02
+    assert r(2049.0) == 2048.0 and r(2051.0) == 2052.0    # ulp 2 above 2048: ties to even
+    with np.errstate(over="ignore"):
+        assert r(65519.0) == 65504.0 and r(65520.0) == math.inf  # largest finite, then overflow
+    assert r(2.0 ** -25) == 0.0                           # half the smallest subnormal -> even zero
+    assert r(3 * 2.0 ** -25) == 2.0 ** -23                # tie between subnormals 1 and 2 -> even 2
+    assert r(2.0 ** -24 * 1.49) == 2.0 ** -24
+    assert r(-(1.0 / 3.0)) == f16_value(0xB555)           # -0.333251953125
+
+
+@pytest.mark.parametrize("fn", ["storage.round_f16", "append.f16_round"])
+def test_round_f16_lands_on_the_nearest_even_neighbour(fn):
+    from oracle import append as oap
+    f = osd.round_f16 if fn == "storage.round_f16" else oap.f16_round
+    rng = np.random.default_rng(13)
+    pats = [0x0001, 0x0002, 0x03FF, 0x0400, 0x3C00, 0x3BFF, 0x7BFE]
+    pats += [int(p) for p in rng.integers(0x0001, 0x7BFE, size=300)]
+    cases = _nearest_even_cases(f16_value, pats)
+    x = np.array([c[0] for c in cases])
+    want = np.array([c[1] for c in cases])
+    assert np.array_equal(f(x), want)
+
+
+def test_logits_streamed_equals_integer_matmul_across_chunks():
+    # integer-valued weights and hidden rows: every logit is an exact integer, computed independently by an
+    # int64 matmul; the head spans two full chunks and a ragged third, so a chunk-offset slip changes values
+    V, H = 2 * ol.CHUNK_ROWS + 77, 6
+    v = np.arange(V)[:, None]
+    k = np.arange(H)[None, :]
+    Wi = ((v * 7 + k * 3 + (v // ol.CHUNK_ROWS) * 5) % 11 - 5).astype(np.int64)
+    hi = np.array([[1, -2, 3, 0, 5, -1], [2, 2, -1, 4, 0, 3]], dtype=np.int64)
+    got = ol.logits_streamed(lambda r0, r1: Wi[r0:r1].astype(np.float64), hi.astype(np.float64), V)
+    assert got.shape == (2, V)
+    assert np.array_equal(got, (hi @ Wi.T).astype(np.float64))
+    a, t, g = ol.argmax_streamed(lambda r0, r1: Wi[r0:r1].astype(np.float64), hi.astype(np.float64), V)
+    exact = hi @ Wi.T
+    assert a.tolist() == np.argmax(exact, axis=1).tolist()
