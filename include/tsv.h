@@ -78,8 +78,9 @@ typedef enum {
 #define TSV_DEV_OK 0
 #define TSV_DEV_BAD_ROOT 1    /* parents[b][0] != -1 */
 #define TSV_DEV_BAD_PARENT 2  /* parents[b][i] outside [0, i) for i >= 1 */
-#define TSV_DEV_BAD_PATH 3    /* path not strictly increasing from 0, or path_len outside [1, T] */
-#define TSV_DEV_BAD_KV_LEN 4  /* kv_len[b] < T, or kv_len[b] > capacity */
+#define TSV_DEV_BAD_PATH 3    /* path not strictly increasing from 0, or path_len outside [1, T]; or a
+                                 kept list / kept_len of tsv_gather_positions out of order or range */
+#define TSV_DEV_BAD_KV_LEN 4  /* kv_len[b] < T (< 0 for tsv_gather_positions), or kv_len[b] > capacity */
 #define TSV_DEV_TIMEOUT 5     /* a bounded wait inside a kernel expired (a library bug; outputs unspecified) */
 
 #define TSV_MAX_T 64
@@ -306,6 +307,14 @@ tsv_status tsv_sample_nucleus(const float* logits, int32_t rows, int32_t V, floa
  *   one array, so calls whose work overlaps on the GPU (on different streams,
  *   or from different host threads) race and give wrong results; serialise
  *   them on one stream.
+ *   Speed: the array holds only the running bests, not the fp16 copy of hidden
+ *   that the tensor-core kernel needs for fp16 and 4-bit heads.  For those two
+ *   formats every call therefore takes the CUDA-core kernel, which streams the
+ *   whole head once per 8 hidden rows: ceil(rows / 8) passes (a 4-bit head of
+ *   248,320 x 5120 rows costs about 0.1 ms per pass, so 4096 rows take about
+ *   50 ms instead of a few).  bf16 heads above 8 rows keep the tensor-core
+ *   kernel.  Callers with many rows and an fp16 or 4-bit head should use
+ *   tsv_lm_head_argmax with a workspace.
  */
 #define TSV_NOALLOC_MAX_ROWS 4096
 
@@ -361,6 +370,37 @@ typedef struct {
 
 tsv_status tsv_kv_gather_positions(const tsv_kv_desc* kv, int32_t* kv_len, const int32_t* path,
                                    const int32_t* path_len, int32_t T, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * tsv_gather_positions - the absolute form of the compaction: keep the cache
+ * positions listed in kept, in order, and close them up from position 0.
+ *   [1212] gather_positions commit: select and compact positions on the
+ *   sequence axis (kept strictly increasing); Int8 scale sidecars move with
+ *   their tokens; a prefix selection [0, 1, ..., n-1] equals trim_to(n) and
+ *   the identity selection moves nothing.  tsv_kv_gather_positions is the
+ *   tail form of the same selection ([1212] gather_within_tail commit) for
+ *   kept = [0, S_b) followed by S_b + path[b][j].
+ *   For every layer, sequence b and kv head:
+ *     rows j <- rows kept[b][j] for j < kept_len[b] (K, V and, for Int8,
+ *     k_scale and v_scale); then kv_len[b] = kept_len[b].
+ *   Rows at or beyond the new kv_len are not written.  Rows below the first j
+ *   with kept[b][j] != j are not written either, so a prefix or identity
+ *   selection moves no cache byte.
+ *   kept      int32 [B, max_kept] (row stride max_kept): kept[b][0..kept_len[b])
+ *             strictly increasing within [0, kv_len[b]).  May be NULL when
+ *             max_kept == 0.
+ *   kept_len  int32 [B]: 0 <= kept_len[b] <= min(max_kept, kv_len[b]).
+ *   kv_len    int32 [B], in/out: in, the current length (<= s_cap); out,
+ *             kept_len[b].
+ *   The list may be as long as the cache; every (layer, sequence, kv head)
+ *   moves its rows in ascending chunks, so the cost is the rows moved.
+ *   Device errors: TSV_DEV_BAD_PATH (a kept list that is not strictly
+ *   increasing, leaves [0, kv_len[b]), or a kept_len out of range),
+ *   TSV_DEV_BAD_KV_LEN (kv_len[b] outside [0, s_cap]); that sequence is left
+ *   untouched, kv_len included.
+ */
+tsv_status tsv_gather_positions(const tsv_kv_desc* kv, int32_t* kv_len, const int32_t* kept, const int32_t* kept_len,
+                                int32_t max_kept, int32_t* dev_status, cudaStream_t stream);
 
 /*
  * tsv_tree_append - append the verify block to every layer's cache, each node

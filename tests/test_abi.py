@@ -32,7 +32,7 @@ def test_every_declared_symbol_is_exported():
 
 def test_version_and_error_string():
     lib = tsv.load()
-    assert lib.tsv_version() == 101
+    assert lib.tsv_version() == 102
     assert lib.tsv_last_error() == b""
 
 
@@ -85,6 +85,15 @@ def test_host_validation_refuses_without_launching():
     k.n_layers, k.B, k.HKV, k.D, k.s_cap, k.kv_dtype = 1, 1, 1, 64, 10, 3
     st = lib.tsv_kv_gather_positions(C.byref(k), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), 4, None, None)
     assert st == _abi.EUNSUPPORTED and b"gather" in lib.tsv_last_error()
+    st = lib.tsv_gather_positions(C.byref(k), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), 4, None, None)
+    assert st == _abi.EUNSUPPORTED and b"gather" in lib.tsv_last_error()  # absolute form: same refusal
+    k.kv_dtype = 0
+    assert lib.tsv_gather_positions(C.byref(k), C.c_void_p(16), C.c_void_p(16), C.c_void_p(16), -1, None,
+                                    None) == _abi.EINVAL  # negative max_kept
+    assert lib.tsv_gather_positions(C.byref(k), C.c_void_p(16), None, C.c_void_p(16), 4, None,
+                                    None) == _abi.EINVAL  # no kept list for max_kept > 0
+    k.B = 0
+    assert lib.tsv_gather_positions(C.byref(k), None, None, None, 4, None, None) == _abi.OK  # empty batch
     st = lib.tsv_lm_head_argmax(C.c_void_p(16), 1, 100, 10, 1, C.c_void_p(16), None, None, C.c_void_p(16), None,
                                 C.c_void_p(16), 64, None)
     assert st == _abi.EINVAL  # H not a multiple of 256

@@ -1,5 +1,5 @@
-"""The bench's reference arm on the host: it times the fp64 oracle on a bounded sample and prints the contract's
-JSON line (no GPU needed)."""
+"""The bench's reference arm on the host: it times the fp64 oracle on a bounded sample with one process per core
+and prints the contract's JSON line (no GPU needed)."""
 import json
 import os
 import subprocess
@@ -9,14 +9,40 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def test_reference_arm_prints_the_contract_line():
-    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "1",
-                        "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=ROOT)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--steps", "2",
+                        "--warmup", "3", "--config", "chain3_27b_bf16", "--cpu-workers", "2"],
+                       capture_output=True, text=True, timeout=600, cwd=ROOT)
     assert r.returncode == 0, r.stderr[-2000:]
     line = json.loads([l for l in r.stdout.splitlines() if l.startswith("{")][-1])
     assert line["impl"] == "reference" and line["unit"] == "nodes/s" and line["higher_is_better"] is True
     assert line["value"] > 0 and line["ms_per_step"] > 0 and line["n_gpus"] == 1
+    assert line["steps"] == 2  # the passes actually timed
     assert line["config"]["workload"] == "chain3_27b_bf16"
+    ex = line["extrapolation"]
+    assert ex["attn_factor"] > 1 and ex["lm_factor"] > 1 and ex["round_s"] > 0
     cb = line["cpu_baseline"]
-    assert cb["kind"] == "oracle" and cb["cores"] >= 1 and cb["value"] == line["value"] and cb["sample"]
+    assert cb["kind"] == "oracle" and cb["cores"] == 2 and cb["value"] == line["value"] and cb["sample"]
+    assert cb["nproc"] >= 1 and cb["cpu_model"]
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
+
+
+def test_default_workload_is_the_largest_single_gpu_config():
+    sys.path.insert(0, ROOT)
+    import bench
+    from synth import configs
+
+    assert bench.DEFAULT_CONFIG == "eagle64x32_27b_i8"
+    big = max(configs.CONFIGS, key=lambda c: c.algorithmic_bytes())
+    assert big.name == bench.DEFAULT_CONFIG
+    assert bench.tensor_bound(configs.workload("eagle64x32_27b_i8"))
+    assert not bench.tensor_bound(configs.workload("eagle32x8_27b_f16"))
+    assert not bench.tensor_bound(configs.workload("specinfer16_27b_i8"))
+
+
+def test_percentiles():
+    sys.path.insert(0, ROOT)
+    import bench
+
+    xs = list(range(11))
+    assert bench.pct(xs, 10) == 1 and bench.pct(xs, 50) == 5 and bench.pct(xs, 90) == 9

@@ -3,8 +3,9 @@
 Some callers cannot allocate device memory themselves (their host framework owns every device buffer through
 its own pool, or their latency budget cannot absorb cudaMalloc's implicit synchronisation).  For them the
 library keeps the LM head's scratch in a fixed device array.  This test compares that entry point with the
-workspace entry point on two calls in a row, with different row counts so that entries left over from the
-first call would show up in the second.  It runs last in the suite and also passes alone in a fresh process.
+workspace entry point on four calls in a row, with different row counts so that entries left over from one
+call would show up in the next, in every weight format, above and below the 8 rows of one CUDA-core pass.
+It runs last in the suite and also passes alone in a fresh process.
 """
 import ctypes as C
 
@@ -23,17 +24,26 @@ def test_noalloc_matches_workspace_entry_point(gpu_lib):
     lib = gpu_lib.load()
     stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
     V, H = 5003, 512
-    for call, (rows, w_dtype) in enumerate([(13, 1), (5, 3)]):
+    # bf16 above 8 rows (tensor-core kernel), 4-bit below 8, and 4-bit and fp16 above 8 rows: there the fixed
+    # array has no room for the tensor-core kernel's fp16 copy of hidden, so the call streams the head once per
+    # 8 rows through the CUDA-core kernel while the workspace call takes the tensor-core one
+    for call, (rows, w_dtype) in enumerate([(13, 1), (5, 3), (20, 3), (20, 0)]):
         rng = np.random.default_rng(100 + call)
-        hidden = torch.from_numpy(rng.standard_normal((rows, H)).astype(np.float32)).to(torch.bfloat16).cuda()
+        target = rng.integers(0, V, size=rows)
         if w_dtype == 3:
             codes = rng.integers(0, 16, size=(V, H))
             W = torch.from_numpy((codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)).cuda()
             sc = torch.from_numpy(rng.uniform(0.005, 0.008, size=(V, H // 64)).astype(np.float32)).to(torch.bfloat16).cuda()
             bi = torch.from_numpy(rng.uniform(-0.06, -0.05, size=(V, H // 64)).astype(np.float32)).to(torch.bfloat16).cuda()
+            direction = (codes[target] - 7.5) / 4.6
         else:
-            W = torch.from_numpy((rng.standard_normal((V, H)) * 0.05).astype(np.float32)).to(torch.bfloat16).cuda()
+            w = rng.standard_normal((V, H))
+            W = torch.from_numpy((w * 0.05).astype(np.float32)).to(torch.bfloat16 if w_dtype == 1 else torch.float16).cuda()
             sc = bi = None
+            direction = w[target]
+        # each row leans towards its own target row, so the two kernels' roundings cannot swap the argmax
+        h = rng.standard_normal((rows, H)) + 2.0 * direction
+        hidden = torch.from_numpy(h.astype(np.float32)).to(torch.bfloat16).cuda()
         ref_arg = torch.full((rows,), -7, dtype=torch.int32, device="cuda")
         ref_max = torch.zeros(rows, dtype=torch.float32, device="cuda")
         ws = torch.empty(lib.tsv_lm_head_workspace_size(rows, H, V, w_dtype), dtype=torch.uint8, device="cuda")
@@ -49,6 +59,7 @@ def test_noalloc_matches_workspace_entry_point(gpu_lib):
         assert torch.equal(arg, ref_arg), call
         assert torch.allclose(mx, ref_max, rtol=1e-4, atol=1e-3), call
         assert int(arg.min()) >= 0 and int(arg.max()) < V
+        assert arg.cpu().numpy().tolist() == target.tolist(), call
 
     too_many = gpu_lib._abi.NOALLOC_MAX_ROWS + 1
     st = lib.tsv_lm_head_argmax_noalloc(_p(hidden), too_many, H, V, 1, _p(W), None, None, _p(arg), None, stream)

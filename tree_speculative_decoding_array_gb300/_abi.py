@@ -74,6 +74,7 @@ SIGNATURES = {
     "tsv_lm_head_argmax_noalloc": (C.c_int, [_vp, _i32, _i32, _i32, _i32, _vp, _vp, _vp, _vp, _vp, _vp]),
     "tsv_tree_accept_walk": (C.c_int, [_vp, _vp, _vp, _i32, _i32, _vp, _vp, _vp, _vp, _vp]),
     "tsv_kv_gather_positions": (C.c_int, [C.POINTER(KvDesc), _vp, _vp, _vp, _i32, _vp, _vp]),
+    "tsv_gather_positions": (C.c_int, [C.POINTER(KvDesc), _vp, _vp, _vp, _i32, _vp, _vp]),
     "tsv_tree_append": (C.c_int, [C.POINTER(AppendDesc), _vp, _vp, _vp]),
 }
 

@@ -271,6 +271,22 @@ def kv_gather_positions(desc: KvDesc, kv_len, path, path_len, T: int, dev_status
                                       _stream(stream)), "kv_gather_positions")
 
 
+def gather_positions(desc: KvDesc, kv_len, kept, kept_len, dev_status=None, stream=None):
+    """Absolute form: every cache keeps positions kept[b, :kept_len[b]] (strictly increasing), closed up from 0;
+    kv_len[b] becomes kept_len[b].  kept int32 [B, max_kept], kept_len int32 [B]."""
+    _cuda(kv_len, "kv_len", torch.int32, (desc.B,))
+    _cuda(kept_len, "kept_len", torch.int32, (desc.B,))
+    if kept is None or kept.numel() == 0:
+        kept, max_kept = None, 0
+    else:
+        _cuda(kept, "kept", torch.int32)
+        if kept.dim() != 2 or kept.shape[0] != desc.B:
+            raise ValueError(f"kept must have shape [B={desc.B}, max_kept], got {tuple(kept.shape)}")
+        max_kept = kept.shape[1]
+    check(load().tsv_gather_positions(C.byref(desc), _p(kv_len), _p(kept), _p(kept_len), int(max_kept), _p(dev_status),
+                                      _stream(stream)), "gather_positions")
+
+
 # ----------------------------------------------------------------------------- one verify round
 @dataclass
 class VerifyRound:

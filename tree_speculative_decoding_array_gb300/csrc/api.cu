@@ -40,7 +40,7 @@ int sm_count() {
 
 extern "C" const char* tsv_last_error(void) { return tsv::g_err; }
 
-extern "C" int tsv_version(void) { return 101; }
+extern "C" int tsv_version(void) { return 102; }
 
 // ---------------------------------------------------------------------------
 // tsv_selftest_bounded_wait: one CTA of the library's bounded waits on a
