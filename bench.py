@@ -210,6 +210,8 @@ def make_cfg(args, name=None):
         cfg = configs.scaled(cfg, n_layers=args.layers)
     if args.batch:
         cfg = configs.scaled(cfg, name=f"{cfg.name}+B{args.batch}", B=args.batch)
+    if args.prefix:
+        cfg = configs.scaled(cfg, name=f"{cfg.name}+S{args.prefix}", S=args.prefix)
     if args.sliding:
         w, e = (int(x) for x in args.sliding.split(":"))
         cfg = configs.with_sliding_layers(cfg, w, e)
@@ -715,6 +717,8 @@ def main():
                     help="attention layers (default: the workload's); fewer only for small profiler captures")
     ap.add_argument("--batch", type=int, default=None,
                     help="sequences (default: the workload's); fewer only for small profiler captures")
+    ap.add_argument("--prefix", type=int, default=None,
+                    help="cached prefix length S (default: the workload's); shorter only for small profiler captures")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -755,8 +759,8 @@ def main():
     r = run_ours(args, cfg, rank, world, local_rank, args.steps, args.warmup)
     free_device()
     extra = {}
-    default_line = args.config == DEFAULT_CONFIG and not (args.layers or args.batch or args.sliding or args.append
-                                                          or args.sampled or args.build_tree)
+    default_line = args.config == DEFAULT_CONFIG and not (args.layers or args.batch or args.prefix or args.sliding
+                                                          or args.append or args.sampled or args.build_tree)
     if world == 1 and default_line and not args.no_extra:
         for name in EXTRA_CONFIGS:
             ecfg = make_cfg(args, name)
@@ -785,7 +789,7 @@ def main():
     if extra:
         line["configs"] = extra
     if not args.no_cpu_baseline and world == 1 and not (args.sliding or args.append or args.sampled or
-                                                          args.build_tree or args.layers or args.batch):
+                                                          args.build_tree or args.layers or args.batch or args.prefix):
         try:
             o = run_oracle_sample(args.config, r["round_id"], 2, 1, host_workers(cfg, args.cpu_workers))
             line["cpu_baseline"] = cpu_baseline_json(o)
