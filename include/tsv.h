@@ -215,13 +215,18 @@ typedef struct {
 } tsv_attn_desc;
 
 /* Kernel choice.  AUTO takes the tensor-core (tcgen05) kernel where it applies
- * (D == 256 with an fp16 or bf16 cache) and the CUDA-core kernel elsewhere.
+ * (D == 256 with an fp16, bf16 or Int8 cache) and the CUDA-core kernel elsewhere.
+ * TCGEN05 lets the library pick the tensor-core kernel's score-tile width (128
+ * keys for Int8 caches and for units of more than 128 query rows, else 64);
+ * TCGEN05_64 and TCGEN05_128 force one (both compute the same result).
  * On the tensor-core path Q is rounded to the cache's 16-bit type for the
  * Q K^T product (exact for bf16; for fp16 caches |q| must lie in fp16 range)
  * and the softmax weights P enter P V as 16-bit values. */
 #define TSV_ATTN_AUTO 0
 #define TSV_ATTN_SIMT 1
 #define TSV_ATTN_TCGEN05 2
+#define TSV_ATTN_TCGEN05_64 3
+#define TSV_ATTN_TCGEN05_128 4
 
 size_t tsv_attention_workspace_size(const tsv_attn_desc* d);
 

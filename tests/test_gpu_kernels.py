@@ -170,12 +170,13 @@ def test_attention_small(gpu_lib, kv_dtype, T, S_list, splits):
                   splits=splits)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 2, 3, 4])
 @pytest.mark.parametrize("kv_dtype", [0, 1, 2])
 @pytest.mark.parametrize("T,S_list,splits", [(1, [0, 63], 0), (3, [64, 4096], 0), (16, [65, 1000], 3),
                                              (22, [127, 5], 1), (33, [500, 200], 0), (64, [64, 1337], 2)])
 def test_attention_both_kernels(gpu_lib, path, kv_dtype, T, S_list, splits):
-    """CUDA-core (path 1) and tcgen05 (path 2) kernels on the same inputs; 1 to 3 tiles of 128 rows, ragged tails."""
+    """The CUDA-core kernel (path 1) and the tcgen05 kernels (path 2: the library's choice of score-tile width,
+    3: 64-key tiles, 4: 128-key tiles) on the same inputs; 1 to 3 tiles of 128 rows, ragged tails."""
     rng = np.random.default_rng(T * 7 + kv_dtype)
     run_attn_case(gpu_lib, rng, B=2, T=T, HQ=24, HKV=4, D=256, S_list=S_list, kv_dtype=kv_dtype, splits=splits,
                   path=path, cap_extra=70)
@@ -197,7 +198,7 @@ def test_attention_head_dims_and_layers(gpu_lib, D):
     run_attn_case(gpu_lib, rng, B=1, T=5, HQ=8, HKV=2, D=D, S_list=[77], kv_dtype=0, splits=0, layers=3)
 
 
-@pytest.mark.parametrize("path", [1, 2])
+@pytest.mark.parametrize("path", [1, 3, 4])
 @pytest.mark.parametrize("kv_dtype", [0, 1, 2])
 @pytest.mark.parametrize("T,S_list,splits,window", [(7, [300, 129], 0, [64]), (16, [1000, 33], 3, [5]),
                                                     (33, [500, 200], 0, [1, 100, 0]), (64, [1337, 64], 2, [200]),
@@ -228,11 +229,13 @@ def test_sliding_band_mask_exact(gpu_lib, window):
         gpu_lib.sliding_band_mask(dense, offset, 0)
 
 
-def test_attention_splits_agree(gpu_lib):
-    """The result holds across split counts (two split choices and more)."""
+@pytest.mark.parametrize("path", [3, 4])
+def test_attention_splits_agree(gpu_lib, path):
+    """The result holds across split counts (two split choices and more), for both score-tile widths."""
     for splits in (1, 2, 5, 0):
         rng = np.random.default_rng(42)
-        run_attn_case(gpu_lib, rng, B=1, T=16, HQ=24, HKV=4, D=256, S_list=[2048], kv_dtype=2, splits=splits)
+        run_attn_case(gpu_lib, rng, B=1, T=16, HQ=24, HKV=4, D=256, S_list=[2048], kv_dtype=2, splits=splits,
+                      path=path)
 
 
 def test_attention_bad_kv_len(gpu_lib):
@@ -414,9 +417,9 @@ def test_gather_bad_path(gpu_lib):
 # ----------------------------------------------------------------------------- limits and failure paths
 def test_attention_maximum_layer_count(gpu_lib):
     """All TSV_MAX_LAYERS layers in one launch, on both kernels."""
-    for path in (1, 2):
+    for path, kv_dtype in ((1, 1), (2, 1), (4, 2)):
         rng = np.random.default_rng(64 + path)
-        run_attn_case(gpu_lib, rng, B=1, T=3, HQ=6, HKV=2, D=256, S_list=[70], kv_dtype=1, splits=0, layers=64,
+        run_attn_case(gpu_lib, rng, B=1, T=3, HQ=6, HKV=2, D=256, S_list=[70], kv_dtype=kv_dtype, splits=0, layers=64,
                       path=path)
 
 

@@ -14,7 +14,7 @@ LIB_PATH = os.path.join(_HERE, "libtsv.so")
 OK, EINVAL, ETOPOLOGY, EUNSUPPORTED, ECAPACITY, ECUDA = range(6)
 F16, BF16, I8_SCALED, Q4_G64 = range(4)
 DEV_OK, DEV_BAD_ROOT, DEV_BAD_PARENT, DEV_BAD_PATH, DEV_BAD_KV_LEN, DEV_TIMEOUT = range(6)
-ATTN_AUTO, ATTN_SIMT, ATTN_TCGEN05 = range(3)
+ATTN_AUTO, ATTN_SIMT, ATTN_TCGEN05, ATTN_TCGEN05_64, ATTN_TCGEN05_128 = range(5)
 MAX_T = 64
 MAX_CANDIDATES = 1024
 MAX_LAYERS = 64

@@ -43,7 +43,7 @@ static AttnGeom attn_geom(const tsv_attn_desc* d) {
     g.rows_unit = (d->HQ / d->HKV) * d->T;
     g.units = d->n_layers * d->B * d->HKV;
     g.rgs = (g.rows_unit + kRB - 1) / kRB;
-    g.path = (d->path == TSV_ATTN_TCGEN05 || (d->path == TSV_ATTN_AUTO && tc_supported(d))) ? TSV_ATTN_TCGEN05
+    g.path = (d->path >= TSV_ATTN_TCGEN05 || (d->path == TSV_ATTN_AUTO && tc_supported(d))) ? TSV_ATTN_TCGEN05
                                                                                            : TSV_ATTN_SIMT;
     // key tiles: 128 for the tcgen05 128-key kernel, 64 for its 64-key kernels, kBK for the CUDA cores
     const int key_tile = g.path == TSV_ATTN_TCGEN05 ? (tc_wide(d) ? 128 : 64) : kBK;
@@ -402,9 +402,9 @@ static tsv_status check_desc(const tsv_attn_desc* d) {
     if (d->splits < 0) return fail(TSV_EINVAL, "tree_verify_attention: splits=%d < 0", d->splits);
     for (int l = 0; l < d->n_layers; ++l)
         if (d->window[l] < 0) return fail(TSV_EINVAL, "tree_verify_attention: layer %d window=%d < 0", l, d->window[l]);
-    if (d->path < TSV_ATTN_AUTO || d->path > TSV_ATTN_TCGEN05)
+    if (d->path < TSV_ATTN_AUTO || d->path > TSV_ATTN_TCGEN05_128)
         return fail(TSV_EINVAL, "tree_verify_attention: path=%d", d->path);
-    if (d->path == TSV_ATTN_TCGEN05 && !tc_supported(d))
+    if (d->path >= TSV_ATTN_TCGEN05 && !tc_supported(d))
         return fail(TSV_EUNSUPPORTED, "tree_verify_attention: the tcgen05 kernel needs D == 256 and an fp16 or bf16 "
                                       "cache of fewer than 2^31 rows");
     if (d->B == 0) return TSV_OK;  // an empty batch: no pointer is read

@@ -150,6 +150,43 @@ __device__ __forceinline__ void convert_i8_tile(const uint8_t* raw, uint8_t* dst
     }
 }
 
+// The same 16 codes times a per-token scale: fp16(code) exact, then one rounding of code * scale.
+__device__ __forceinline__ void i8x16_to_f16x16_scaled(uint4 in, __half2 s2, uint32_t (&out)[8]) {
+    i8x16_to_f16x16(in, out);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const __half2 w = __hmul2(*reinterpret_cast<const __half2*>(&out[k]), s2);
+        out[k] = *reinterpret_cast<const uint32_t*>(&w);
+    }
+}
+
+// convert_i8_tile with every key's codes multiplied by its scale (scale2: this thread's key, both halves).
+__device__ __forceinline__ void convert_i8_tile_scaled(const uint8_t* raw, uint8_t* dst, int nk, int ct, __half2 scale2) {
+    const int key = ct & 63, k7 = key & 7;
+    uint4 in[8];
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const int q = 2 * s + (ct >> 6);
+        in[s] = key < nk ? *reinterpret_cast<const uint4*>(raw + (q >> 3) * 8192 + key * 128 + (((q & 7) ^ k7) << 4))
+                         : make_uint4(0, 0, 0, 0);
+    }
+    uint8_t* row = dst + key * 128;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const int q = 2 * s + (ct >> 6);
+        uint32_t w[8];
+        i8x16_to_f16x16_scaled(in[s], scale2, w);
+        if (key >= nk) {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) w[e] = 0;
+        }
+        const int cc0 = (q & 3) * 2;
+        uint8_t* rb = row + (q >> 2) * 8192;
+        *reinterpret_cast<uint4*>(rb + ((cc0 ^ k7) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+        *reinterpret_cast<uint4*>(rb + (((cc0 + 1) ^ k7) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+    }
+}
+
 constexpr int kNS = 3;  // stages of the K ring and of the V ring
 
 template <bool I8>
@@ -1012,6 +1049,492 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
     }
 }
 
+// ------------------------------------------------------------------ Int8 caches: 128-key score tiles
+// The same 128-key Q K^T (N = 128) for Int8 caches.  TMEM as in attn_tcw_kernel: Q [0, 128), S [128, 256) (one
+// buffer, freed as soon as the softmax has read it), O [256, 512).  An fp16 K tile of 128 keys (64 KB) does
+// not fit twice beside the other rings, so K moves in dim quarters (128 keys x 64 dims): TMA lands a raw quarter
+// (8 KB, 64-byte swizzle) in a 3-stage ring, the K converters write its fp16 copy (16 KB, 128-byte swizzle) into
+// a 4-slot ring -- slot q holds quarter q of the current tile -- and Q K^T issues the quarter's MMAs as soon as
+// it is there.  V moves in 64-key halves (raw halves, fp16 halves); P goes to shared memory in two 64-key
+// halves, one per softmax half, and P V reads A from there.
+// The converters fold each token's scale into its fp16 row (code exact, then one rounding of code * scale), and
+// Q is stored pre-multiplied by log2(e) / sqrt(256), so S arrives in the log2 domain and the softmax multiplies
+// nothing but P.
+// The issuer takes whichever group of four MMAs is ready, P V first (the softmax waits for it): a quarter of
+// Q K^T or a half of P V.  Measured and rejected: alternating single MMAs of the two (barrier tests between them
+// cost 2.7x) and alternating the two groups' MMAs without tests (1.24x slower: the two shapes do not overlap).
+// 608 threads (104 registers each: a softmax thread holds its 64 scores):
+//   warps 0-3, 7-10  softmax halves 0 and 1 (key columns 64 h .. 64 h + 63 of the tile; lane quarter = warp & 3);
+//                    half 0 also stores Q into TMEM
+//   warp 4           TMEM allocation and the MMA issuer
+//   warp 5, 6        TMA producers: raw K quarters, raw V halves
+//   warps 11-14      K converters (thread = key of the quarter)
+//   warps 15-18      V converters
+constexpr int kW8Threads = 608;
+
+// Keys c0 .. c0 + 63 as a bit mask (bit c = key c0 + c) of what one query row sees: keys below k_end and at or
+// above lo_row (the sliding band), history keys (< S) in full, block keys S + i where bit i of anc is set.
+__device__ __forceinline__ uint64_t visible64(int c0, int k_end, int lo_row, int S, uint64_t anc, bool row_ok) {
+    if (!row_ok) return 0ull;
+    const int n_end = min(max(k_end - c0, 0), 64);                              // keys < k_end
+    uint64_t m = n_end >= 64 ? ~0ull : ((1ull << n_end) - 1ull);
+    if (lo_row > c0) m &= lo_row - c0 >= 64 ? 0ull : (~0ull << (lo_row - c0));  // keys >= lo_row
+    const int sh = S - c0;                                                       // first block key's bit
+    if (sh <= 0) m &= -sh >= 64 ? 0ull : (anc >> (-sh));
+    else if (sh < 64) m &= ((1ull << sh) - 1ull) | (anc << sh);
+    return m;
+}
+
+constexpr int kW8KR = 3;                          // raw K quarter stages
+constexpr uint32_t kW8OffKh = 0;                  // 4 x 16 KB fp16 K quarters [128 keys][128 B]
+constexpr uint32_t kW8OffKr = 65536;              // 3 x 8 KB raw K quarters [128 keys][64 B], 64-byte swizzle
+constexpr uint32_t kW8OffVh = 90112;              // 2 x 32 KB fp16 V halves [4 dim blocks][64 keys][128 B]
+constexpr uint32_t kW8OffVr = 155648;             // 2 x 16 KB raw V halves [2][64 keys][128 B]
+constexpr uint32_t kW8OffP = 188416;              // 2 x 16 KB P halves [128 rows][128 B]
+constexpr uint32_t kW8OffX = 221184;              // softmax halves' exchange [2 slots][2 halves][128 rows] fp32
+constexpr uint32_t kW8OffBar = 223232;            // barriers, TMEM slot, abort flag
+constexpr int kW8Smem = 1024 + 223232 + 512;
+constexpr float kLog2eOverSqrtD = 1.4426950408889634f * 0.0625f;
+
+
+__global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_constant__ TcParams p) {
+    griddep_begin();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* sKh = sm + kW8OffKh;
+    uint8_t* sKr = sm + kW8OffKr;
+    uint8_t* sVh = sm + kW8OffVh;
+    uint8_t* sVr = sm + kW8OffVr;
+    uint8_t* sP = sm + kW8OffP;
+    float* xv = reinterpret_cast<float*>(sm + kW8OffX);
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + kW8OffBar);
+    uint64_t* kr_full = bars + 0;    // [3] raw K quarter landed
+    uint64_t* kr_empty = bars + 3;   // [3] the K converters are done with it
+    uint64_t* kq_full = bars + 6;    // [4] fp16 K quarter written
+    uint64_t* kq_empty = bars + 10;  // [4] Q K^T done with it
+    uint64_t* vr_full = bars + 14;   // [2] raw V half landed
+    uint64_t* vr_empty = bars + 16;  // [2] the V converters are done with it
+    uint64_t* vh_full = bars + 18;   // [2] fp16 V half written
+    uint64_t* vh_empty = bars + 20;  // [2] P V done with it
+    uint64_t* s_full = bars + 22;    // Q K^T of a tile done
+    uint64_t* s_free = bars + 23;    // both softmax halves read S (8 warps)
+    uint64_t* p_full = bars + 24;    // [2] P half written (4 warps)
+    uint64_t* p_free = bars + 26;    // [2] P V done with the P half
+    uint64_t* xch = bars + 28;       // [4 lane quarters][2 parities] both halves posted their value
+    uint64_t* q_full = bars + 36;
+    uint64_t* o_done = bars + 37;
+    uint64_t* drain = bars + 38;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 39);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 40);
+    constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    int item = blockIdx.x;
+    const int mt = item % p.mtiles;
+    item /= p.mtiles;
+    const int split = item % p.splits;
+    const int unit = item / p.splits;
+    const int kvh = unit % p.HKV;
+    const int b = (unit / p.HKV) % p.B;
+    const int layer = unit / (p.HKV * p.B);
+    const int T = p.T;
+    const int kvl = p.kv_len[b];
+    if (kvl < T || kvl > p.max_kv_len || (int64_t)kvl > p.s_cap) {
+        if (split == 0 && mt == 0 && kvh == 0 && layer == 0 && threadIdx.x == 0)
+            dev_fail(p.status, TSV_DEV_BAD_KV_LEN, b, kvl);
+        return;
+    }
+    const int S = kvl - T;
+    const int row0 = mt * kTcRows;
+    const int k_end = min(kvl, split * p.chunk + p.chunk);
+    const int win = p.window[layer];
+    const int lo_first = win > 0 ? S + row0 / p.G - win + 1 : INT_MIN;
+    const int lo_last = win > 0 ? S + (min(p.R, row0 + kTcRows) - 1) / p.G - win + 1 : INT_MIN;
+    int k_begin = split * p.chunk;
+    if (lo_first > k_begin) k_begin += ((lo_first - k_begin) / kWK) * kWK;
+    const int ntiles = k_end > k_begin ? (k_end - k_begin + kWK - 1) / kWK : 0;  // 128-key tiles
+    const int nhalves = 2 * ntiles;
+
+    if (p.status != nullptr && *reinterpret_cast<volatile int32_t*>(p.status) == TSV_DEV_TIMEOUT) return;
+    if (ntiles == 0) {
+        if (threadIdx.x < kTcRows && row0 + (int)threadIdx.x < p.R) {
+            const size_t slot = ((size_t)unit * p.splits + split) * p.R + row0 + threadIdx.x;
+            p.ws_ml[2 * slot] = -INFINITY;
+            p.ws_ml[2 * slot + 1] = 0.f;
+        }
+        return;
+    }
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kW8KR; ++s) {
+            tc::mbar_init(&kr_full[s], 1);
+            tc::mbar_init(&kr_empty[s], 4);
+        }
+        for (int s = 0; s < 4; ++s) {
+            tc::mbar_init(&kq_full[s], 4);
+            tc::mbar_init(&kq_empty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&vr_full[s], 1);
+            tc::mbar_init(&vr_empty[s], 4);
+            tc::mbar_init(&vh_full[s], 4);
+            tc::mbar_init(&vh_empty[s], 1);
+            tc::mbar_init(&p_full[s], 4);
+            tc::mbar_init(&p_free[s], 1);
+        }
+        for (int s = 0; s < 8; ++s) tc::mbar_init(&xch[s], 2);
+        tc::mbar_init(s_full, 1);
+        tc::mbar_init(s_free, 8);
+        tc::mbar_init(q_full, 4);
+        tc::mbar_init(o_done, 1);
+        tc::mbar_init(drain, 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    if (warp == 4) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int rowbase = (int)(((int64_t)b * p.HKV + kvh) * p.s_cap + k_begin);
+    const size_t seq_row = ((size_t)b * p.HKV + kvh) * (size_t)p.s_cap;
+
+    if (warp == 5 || warp == 6) {
+        // ------------------------------------------------------------ TMA producers (lane 0 of each warp)
+        if (lane == 0) {
+            const bool isK = warp == 5;
+            const CUtensorMap* m = isK ? &p.kmap[layer] : &p.vmap[layer];
+            tc::tma_prefetch_desc(m);
+            const int n = isK ? 4 * ntiles : nhalves;
+            const int NS = isK ? kW8KR : 2;
+            uint64_t* fullb = isK ? kr_full : vr_full;
+            uint64_t* emptyb = isK ? kr_empty : vr_empty;
+            int issued = 0;
+            for (int g = 0; g < n; ++g) {
+                const int st = g % NS;
+                if (g >= NS && !tc::mbar_wait(&emptyb[st], ((g / NS) - 1) & 1, abort_flag, 256)) break;
+                if (isK) {  // quarter g & 3 of tile g >> 2: 128 keys x 64 bytes
+                    tc::mbar_expect_tx(&fullb[st], 8192);
+                    tc::tma_load_2d(sKr + st * 8192, m, &fullb[st], (g & 3) * 64, rowbase + (g >> 2) * kWK);
+                } else {    // 64 keys x 256 bytes as two 128-byte-wide halves
+                    tc::mbar_expect_tx(&fullb[st], 16384);
+                    uint8_t* dst = sVr + st * 16384;
+                    tc::tma_load_2d(dst, m, &fullb[st], 0, rowbase + g * kTcBK);
+                    tc::tma_load_2d(dst + 8192, m, &fullb[st], 128, rowbase + g * kTcBK);
+                }
+                issued = g + 1;
+            }
+            if (*abort_flag)
+                for (int g = max(0, issued - NS); g < issued; ++g) drain_wait(&fullb[g % NS], (g / NS) & 1);
+        }
+    } else if (warp == 4) {
+        // ------------------------------------------------------------ MMA issuer
+        if (lane == 0) {
+            const uint32_t id_qk = tc::idesc_f16(false, false, false, kTcRows, kWK);
+            const uint32_t id_pv = tc::idesc_f16(false, false, true, kTcRows, kTcD);
+            // one descriptor per operand ring; every MMA below is a constant offset from one of them
+            const uint64_t dK = tc::sdesc_sw128(tc::smem_u32(sKh), 16, 1024);
+            const uint64_t dV = tc::sdesc_sw128(tc::smem_u32(sVh), 8192, 1024);
+            const uint64_t dP = tc::sdesc_sw128(tc::smem_u32(sP), 16, 1024);
+            const uint32_t tS = tmem + kColS, tO = tmem + kColO;
+            bool ok = tc::mbar_wait_spin(q_full, 0, abort_flag);
+            if (ok) tc::tc_fence_after();
+            int sj = 0, sq = 0, pq = 0;  // next Q K^T tile and quarter, next P V half
+            uint32_t idle = 0;
+            uint64_t t_idle = 0;
+            while (ok && pq < nhalves) {
+                bool prog = false;
+                if ((pq >> 1) < sj) {  // P V of half pq: P written, fp16 V half there
+                    const int h = pq & 1, jt = pq >> 1;
+                    if (tc::mbar_test(&p_full[h], jt & 1) && tc::mbar_test(&vh_full[h], jt & 1)) {
+                        tc::tc_fence_after();
+                        const uint64_t a = tc::sdesc_add(dP, h * 16384), bv = tc::sdesc_add(dV, h * 32768);
+                        tc::mma_f16(tO, a, bv, id_pv, pq > 0 ? 1u : 0u);
+                        tc::mma_f16(tO, tc::sdesc_add(a, 32), tc::sdesc_add(bv, 2048), id_pv, 1u);
+                        tc::mma_f16(tO, tc::sdesc_add(a, 64), tc::sdesc_add(bv, 4096), id_pv, 1u);
+                        tc::mma_f16(tO, tc::sdesc_add(a, 96), tc::sdesc_add(bv, 6144), id_pv, 1u);
+                        tc::mma_commit(&p_free[h]);
+                        tc::mma_commit(&vh_empty[h]);
+                        ++pq;
+                        prog = true;
+                    }
+                }
+                if (sj < ntiles) {
+                    bool ready = sq > 0 || sj == 0 || tc::mbar_test(s_free, (sj - 1) & 1);
+                    if (ready) ready = tc::mbar_test(&kq_full[sq], sj & 1);
+                    if (ready) {
+                        tc::tc_fence_after();
+                        const uint64_t bk = tc::sdesc_add(dK, sq * 16384);
+                        const uint32_t aq = tmem + kColQ + sq * 32;  // Q columns of features 64 sq ..
+                        tc::mma_f16_ts(tS, aq, bk, id_qk, sq > 0 ? 1u : 0u);
+                        tc::mma_f16_ts(tS, aq + 8, tc::sdesc_add(bk, 32), id_qk, 1u);
+                        tc::mma_f16_ts(tS, aq + 16, tc::sdesc_add(bk, 64), id_qk, 1u);
+                        tc::mma_f16_ts(tS, aq + 24, tc::sdesc_add(bk, 96), id_qk, 1u);
+                        tc::mma_commit(&kq_empty[sq]);
+                        if (++sq == 4) {
+                            tc::mma_commit(s_full);
+                            sq = 0;
+                            ++sj;
+                        }
+                        prog = true;
+                    }
+                }
+                if (prog) {
+                    idle = 0;
+                } else if ((++idle & 63) == 1) {  // bounded: give up after kWaitNs without progress
+                    const uint64_t now = tc::globaltimer();
+                    if (idle == 1) t_idle = now;
+                    if (*abort_flag || now - t_idle > tc::kWaitNs) {
+                        *abort_flag = 1;
+                        ok = false;
+                    }
+                }
+            }
+            if (ok) {
+                tc::mma_commit(o_done);
+            } else {
+                tc::mma_commit(drain);
+                drain_wait(drain, 0);
+            }
+        }
+    } else if (warp >= 11 && warp < 15) {
+        // ------------------------------------------------------------ K converters: thread = key of the quarter
+        const int key = threadIdx.x - 352;
+        const uint16_t* ksg = p.ks[layer] + seq_row;
+        auto scale_of = [&](int jj) -> float {  // this thread's key of tile jj; keys past the range: 0
+            const int k = k_begin + jj * kWK + key;
+            return (jj < ntiles && k < k_end) ? f16_bits_to_f32(ksg[k]) : 0.f;
+        };
+        float sc_cur = scale_of(0), sc_nxt = 0.f;
+        __half2 s2 = __floats2half2_rn(sc_cur, sc_cur);
+        for (int g = 0; g < 4 * ntiles; ++g) {
+            const int rs = g % kW8KR, q = g & 3;
+            if (q == 0) {  // a new tile: this key's scale, and the next tile's fetched ahead
+                s2 = __floats2half2_rn(sc_cur, sc_cur);
+                sc_nxt = scale_of((g >> 2) + 1);
+            }
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kr_full[rs], (g / kW8KR) & 1, abort_flag))) break;
+            if (g >= 4 &&
+                !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kq_empty[q], ((g >> 2) - 1) & 1, abort_flag)))
+                break;
+            // raw row: 64 bytes, 16-byte chunk c at ((c ^ ((key >> 1) & 3)) << 4) (64-byte swizzle)
+            const uint8_t* raw = sKr + rs * 8192 + key * 64;
+            uint4 in[4];
+#pragma unroll
+            for (int c = 0; c < 4; ++c) in[c] = *reinterpret_cast<const uint4*>(raw + ((c ^ ((key >> 1) & 3)) << 4));
+            uint8_t* row = sKh + q * 16384 + key * 128;  // fp16 row: chunk c at ((c ^ (key & 7)) << 4)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) {
+                uint32_t w[8];
+                i8x16_to_f16x16_scaled(in[c], s2, w);
+                *reinterpret_cast<uint4*>(row + (((2 * c) ^ (key & 7)) << 4)) = make_uint4(w[0], w[1], w[2], w[3]);
+                *reinterpret_cast<uint4*>(row + (((2 * c + 1) ^ (key & 7)) << 4)) = make_uint4(w[4], w[5], w[6], w[7]);
+            }
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&kr_empty[rs]);
+                tc::mbar_arrive(&kq_full[q]);
+            }
+            if (q == 3) sc_cur = sc_nxt;
+        }
+    } else if (warp >= 15) {
+        // ------------------------------------------------------------ V converters: 64-key halves
+        const int ct = threadIdx.x - 480;
+        const uint16_t* vsg = p.vs[layer] + seq_row;
+        auto scale_of = [&](int hh) -> float {  // key ct & 63 of half hh; keys past the range: 0
+            const int k = k_begin + hh * kTcBK + (ct & 63);
+            return (hh < nhalves && k < k_end) ? f16_bits_to_f32(vsg[k]) : 0.f;
+        };
+        float sc_cur = scale_of(0);
+        for (int hh = 0; hh < nhalves; ++hh) {
+            const int st = hh & 1;
+            const __half2 s2 = __floats2half2_rn(sc_cur, sc_cur);
+            const float sc_nxt = scale_of(hh + 1);
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vr_full[st], (hh >> 1) & 1, abort_flag))) break;
+            if (hh >= 2 &&
+                !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vh_empty[st], ((hh >> 1) - 1) & 1, abort_flag)))
+                break;
+            const int nk = min(kTcBK, k_end - (k_begin + hh * kTcBK));  // keys >= nk (past the range) become 0
+            convert_i8_tile_scaled(sVr + st * 16384, sVh + st * 32768, nk, ct, s2);
+            tc::fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tc::mbar_arrive(&vr_empty[st]);
+                tc::mbar_arrive(&vh_full[st]);
+            }
+            sc_cur = sc_nxt;
+        }
+    } else {
+        // ------------------------------------------------------------ softmax halves (warps 0-3 and 7-10)
+        const int h = warp < 4 ? 0 : 1;
+        const int qd = warp & 3;
+        const int r = qd * 32 + lane;  // row within the tile == TMEM lane
+        const int gr = row0 + r;
+        const bool row_ok = gr < p.R;
+        const int node = row_ok ? gr / p.G : 0;
+        const int head = kvh * p.G + (row_ok ? gr % p.G : 0);
+        const uint64_t anc = row_ok ? p.anc[(size_t)b * T + node] : 0ull;
+        const int lo_row = win > 0 ? S + node - win + 1 : INT_MIN;
+        const uint32_t lane_base = (uint32_t)(qd * 32) << 16;
+        if (h == 0) {  // Q row x log2(e)/16 -> TMEM lane r as fp16 pairs, 64 features (32 columns) at a time
+            const uint4* src = reinterpret_cast<const uint4*>(p.q[layer] + ((size_t)(b * T + node) * p.HQ + head) * kTcD);
+#pragma unroll 1
+            for (int c4 = 0; c4 < 4; ++c4) {
+                uint32_t w[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 v = row_ok ? src[c4 * 8 + i] : make_uint4(0, 0, 0, 0);
+                    const uint32_t in[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const __half2 hh2 = __floats2half2_rn(bf16_lo(in[e]) * kLog2eOverSqrtD,
+                                                             bf16_hi(in[e]) * kLog2eOverSqrtD);
+                        w[4 * i + e] = *reinterpret_cast<const uint32_t*>(&hh2);
+                    }
+                }
+                tc::tmem_st32(tmem + lane_base + kColQ + c4 * 32, w);
+            }
+            tc::tmem_wait_st();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(q_full);
+        }
+        auto exchange = [&](int jj, float mine, float& other) -> bool {
+            const int slot = jj & 1;
+            xv[(slot * 2 + h) * kTcRows + r] = mine;
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&xch[qd * 2 + slot]);
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&xch[qd * 2 + slot], (jj >> 1) & 1, abort_flag))) return false;
+            other = xv[(slot * 2 + (h ^ 1)) * kTcRows + r];
+            return true;
+        };
+        float m_ref = -INFINITY, l = 0.f;
+        bool ok = true;
+        for (int j = 0; j < ntiles; ++j) {
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(s_full, j & 1, abort_flag))) { ok = false; break; }
+            tc::tc_fence_after();
+            float x[64];  // scores of this half, already in the log2 domain
+#pragma unroll
+            for (int c2 = 0; c2 < 2; ++c2) {
+                uint32_t sv[32];
+                tc::tmem_ld32(tmem + lane_base + kColS + h * 64 + c2 * 32, sv);
+                tc::tmem_wait_ld();
+#pragma unroll
+                for (int c = 0; c < 32; ++c) x[c2 * 32 + c] = __uint_as_float(sv[c]);
+            }
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(s_free);
+            const int ct = k_begin + j * kWK;  // first key of the tile
+            const int c0 = ct + h * 64;        // first key of this half
+            if (!(ct + kWK <= k_end && ct + kWK <= S && ct >= lo_last)) {  // some key of the tile is masked
+                const uint64_t vis = visible64(c0, k_end, lo_row, S, anc, row_ok);  // bit c: key c0 + c
+#pragma unroll
+                for (int c = 0; c < 64; ++c) x[c] = ((vis >> c) & 1ull) ? x[c] : -INFINITY;
+            }
+            float mx = x[0];
+#pragma unroll
+            for (int c = 1; c < 64; ++c) mx = fmaxf(mx, x[c]);
+            float mo;
+            if (!exchange(j, mx, mo)) { ok = false; break; }
+            const float mt_ = fmaxf(mx, mo);
+            float alpha = 1.f;
+            bool resc = false;
+            if (mt_ > m_ref + 8.f) {
+                alpha = tc::ex2_approx(m_ref - mt_);
+                m_ref = mt_;
+                resc = true;
+            }
+            const float msub = m_ref == -INFINITY ? 0.f : m_ref;
+            if (j >= 1) {  // P V of the previous tile done: the P halves are free again and O is stable
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&p_free[1], (j - 1) & 1, abort_flag))) { ok = false; break; }
+                tc::tc_fence_after();
+            }
+            float ps = 0.f;
+            uint8_t* prow = sP + h * 16384 + r * 128;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {  // 8 keys per 16-byte chunk of this row's P half
+                uint32_t pk[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const int c = ch * 8 + 2 * e;
+                    const float p0 = tc::ex2_approx(x[c] - msub);
+                    const float p1 = tc::ex2_approx(x[c + 1] - msub);
+                    ps += p0 + p1;
+                    pk[e] = pack2(p0, p1, false);
+                }
+                *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+            }
+            // O *= alpha for this half's 128 columns (the scores are dead by now); P V of this tile waits for p_full
+            if (j >= 1 && __any_sync(0xFFFFFFFFu, resc)) {
+#pragma unroll 1
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tmem + lane_base + kColO + h * 128 + ch * 32, o);
+                    tc::tmem_wait_ld();
+#pragma unroll
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tc::tmem_st32(tmem + lane_base + kColO + h * 128 + ch * 32, o);
+                }
+                tc::tmem_wait_st();
+            }
+            tc::fence_proxy_async_smem();
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&p_full[h]);
+            l = l * alpha + ps;
+        }
+        if (ok) {  // the row sum of both halves
+            float lo;
+            if (exchange(ntiles, l, lo)) l += lo;
+            else ok = false;
+        }
+        if (ok && __all_sync(0xFFFFFFFFu, tc::mbar_wait(o_done, 0, abort_flag))) {
+            tc::tc_fence_after();
+            const size_t slot = ((size_t)unit * p.splits + split) * p.R + gr;
+            const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll 1
+            for (int ch = h * 4; ch < h * 4 + 4; ++ch) {
+                uint32_t o[32];
+                tc::tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
+                tc::tmem_wait_ld();
+                if (!row_ok) continue;
+                if (p.splits == 1) {
+                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<__nv_bfloat16*>(p.o[layer]) +
+                                                          ((size_t)(b * T + node) * p.HQ + head) * kTcD + ch * 32);
+#pragma unroll
+                    for (int k = 0; k < 4; ++k) {
+                        uint32_t w[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e)
+                            w[e] = pack2(__uint_as_float(o[8 * k + 2 * e]) * inv, __uint_as_float(o[8 * k + 2 * e + 1]) * inv, true);
+                        dst[k] = make_uint4(w[0], w[1], w[2], w[3]);
+                    }
+                } else {
+                    float4* dst = reinterpret_cast<float4*>(p.ws_o + slot * kTcD + ch * 32);
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        dst[k] = make_float4(__uint_as_float(o[4 * k]), __uint_as_float(o[4 * k + 1]),
+                                             __uint_as_float(o[4 * k + 2]), __uint_as_float(o[4 * k + 3]));
+                }
+            }
+            if (h == 0 && row_ok && p.splits > 1) {  // the row's maximum and sum in the log2 domain, for the combine
+                p.ws_ml[2 * slot] = m_ref;
+                p.ws_ml[2 * slot + 1] = l;
+            }
+        }
+    }
+    __syncthreads();
+    if (*abort_flag && threadIdx.x == 0) dev_fail(p.status, TSV_DEV_TIMEOUT, b, blockIdx.x);
+    if (warp == 4) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
 // ------------------------------------------------------------------ host side
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1035,16 +1558,18 @@ static EncodeTiledFn encode_fn() {
 // 64 rows with the 128-byte swizzle the MMA operands use.  Int8 caches:
 // boxes of 128 bytes x 64 rows, 128-byte swizzled too (bank-conflict-free
 // reads for the converter, which re-lays them out as fp16 operand tiles).
-static bool make_kv_map(CUtensorMap* m, const void* base, long long rows, bool i8) {
+// quarters = true (Int8 K for the 128-key kernel): boxes of 64 bytes x 128 rows (one dim quarter of a 128-key
+// tile) with the 64-byte swizzle.
+static bool make_kv_map(CUtensorMap* m, const void* base, long long rows, bool i8, bool quarters = false) {
     EncodeTiledFn enc = encode_fn();
     if (!enc) return false;
     cuuint64_t dims[2] = {(cuuint64_t)kTcD, (cuuint64_t)rows};
     cuuint64_t strides[1] = {(cuuint64_t)kTcD * (i8 ? 1 : 2)};
-    cuuint32_t box[2] = {i8 ? 128u : 64u, (cuuint32_t)kTcBK};
+    cuuint32_t box[2] = {quarters ? 64u : (i8 ? 128u : 64u), quarters ? (cuuint32_t)kWK : (cuuint32_t)kTcBK};
     cuuint32_t es[2] = {1, 1};
     return enc(m, i8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_UINT16, 2, const_cast<void*>(base), dims,
                strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
-               CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               quarters ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -1055,17 +1580,24 @@ bool tc_supported(const tsv_attn_desc* d) {
 
 int tc_mtiles(const tsv_attn_desc* d) { return ((d->HQ / d->HKV) * d->T + kTcRows - 1) / kTcRows; }
 
-// The 128-key kernel for 16-bit caches when a unit has more than one 128-row tile of query rows: there the
-// halved Q K^T issue cost wins; with a single, mostly empty row tile the deeper 64-key pipeline is faster.
-bool tc_wide(const tsv_attn_desc* d) { return d->kv_dtype != TSV_I8_SCALED && tc_mtiles(d) >= 2; }
+// 128-key score tiles or 64-key ones.  TSV_ATTN_TCGEN05_64 / _128 choose; otherwise the 128-key kernel for
+// 16-bit caches when a unit has more than one 128-row tile of query rows (there the halved Q K^T issue cost wins;
+// with a single, mostly empty row tile the deeper 64-key pipeline is faster).  Int8 caches take the 64-key
+// kernel: on the 16- and 64-node workloads the 128-key Int8 kernel measured level with it or up to 2 % slower.
+bool tc_wide(const tsv_attn_desc* d) {
+    if (d->path == TSV_ATTN_TCGEN05_64) return false;
+    if (d->path == TSV_ATTN_TCGEN05_128) return true;
+    return d->kv_dtype != TSV_I8_SCALED && tc_mtiles(d) >= 2;
+}
 
 tsv_status launch_tc(const tsv_attn_desc* d, int splits, int chunk, float* ws_o, float* ws_ml, int32_t* status,
                      cudaStream_t stream) {
     static thread_local TcParams prm;
     const bool i8 = d->kv_dtype == TSV_I8_SCALED;
+    const bool wide = tc_wide(d);
     const long long rows = (long long)d->B * d->HKV * d->s_cap;
     for (int l = 0; l < d->n_layers; ++l) {
-        if (!make_kv_map(&prm.kmap[l], d->k[l], rows, i8) || !make_kv_map(&prm.vmap[l], d->v[l], rows, i8))
+        if (!make_kv_map(&prm.kmap[l], d->k[l], rows, i8, i8 && wide) || !make_kv_map(&prm.vmap[l], d->v[l], rows, i8))
             return fail(TSV_ECUDA, "tree_verify_attention: tensor map encoding failed for layer %d", l);
         prm.q[l] = reinterpret_cast<const uint16_t*>(d->q[l]);
         prm.o[l] = d->o[l];
@@ -1092,10 +1624,13 @@ tsv_status launch_tc(const tsv_attn_desc* d, int splits, int chunk, float* ws_o,
     prm.mma_bf16 = d->kv_dtype == TSV_BF16;
     const long long items = (long long)d->n_layers * d->B * d->HKV * splits * prm.mtiles;
     if (items > 0x7FFFFFFFLL) return fail(TSV_ECAPACITY, "tree_verify_attention: too many work items");
-    if (i8) {
+    if (i8 && wide) {
+        cudaFuncSetAttribute(attn_tcw8_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kW8Smem);
+        launch_pdl(attn_tcw8_kernel, (unsigned)items, kW8Threads, kW8Smem, stream, prm);
+    } else if (i8) {
         cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
         launch_pdl(attn_tc_kernel<true>, (unsigned)items, kTcThreadsI8, kTcSmem, stream, prm);
-    } else if (tc_wide(d)) {
+    } else if (wide) {
         cudaFuncSetAttribute(attn_tcw_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kWSmem);
         launch_pdl(attn_tcw_kernel, (unsigned)items, kTcThreads16, kWSmem, stream, prm);
     } else {

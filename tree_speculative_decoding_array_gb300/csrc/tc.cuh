@@ -57,16 +57,18 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
 // shared-memory and tensor-core instructions of the thread on the critical path.  Waiters that are far ahead
 // of the pipeline pass a long maximum, waiters on the critical path a short one.  Gives up (returns false and
 // raises *abort) after kWaitNs nanoseconds, or as soon as another thread of the CTA raised *abort; no wait can
-// hang the kernel.
+// hang the kernel.  `spins` polls come before the first sleep: a waiter on the critical path keeps a few; one
+// that runs ahead of the pipeline (a producer, a converter) takes none, since every poll is an issue slot that
+// the warps sharing its SM sub-partition lose.
 constexpr uint64_t kWaitNs = 1000000000ull;  // 1 s: far above any legitimate wait
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint32_t max_sleep_ns = 32) {
+                                          uint32_t max_sleep_ns = 32, uint32_t spins = 16) {
     if (mbar_test(bar, parity)) return true;
     const uint64_t t0 = globaltimer();
     uint32_t sleep_ns = 32;
     for (uint32_t i = 1;; ++i) {
         if (mbar_test(bar, parity)) return true;
-        if (i > 16) {
+        if (i > spins) {
             __nanosleep(sleep_ns);
             if (sleep_ns < max_sleep_ns) sleep_ns <<= 1;
         }
@@ -146,6 +148,12 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_byt
     return d;
 }
 
+// A descriptor of the same layout `bytes` further on (bytes a multiple of 16; shared addresses stay below 256 KB,
+// so the 14-bit address field cannot carry into the next field).  Issuers build one descriptor per ring and
+// advance it with this add: descriptor arithmetic inside an MMA issue sequence costs issue slots on the critical
+// path.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor of kind::f16 with fp32 accumulation.
 // ab_bf16: operands are bf16 (else fp16); a_mn / b_mn: operand is MN-major.
 __host__ __device__ constexpr uint32_t idesc_f16(bool ab_bf16, bool a_mn, bool b_mn, int M, int N) {
@@ -185,6 +193,14 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
     asm volatile("tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+                 : "r"(taddr));
+}
+
+// 16 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+                   "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
                  : "r"(taddr));
 }
 
