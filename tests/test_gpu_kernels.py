@@ -269,7 +269,8 @@ def q4_pack(codes):
 
 @pytest.mark.parametrize("w_dtype", [0, 1, 3])
 @pytest.mark.parametrize("rows,V,H", [(1, 1000, 256), (3, 4099, 512), (5, 777, 256), (8, 2048, 1024), (13, 3001, 256),
-                                      (16, 1280, 5120), (64, 5003, 512), (200, 2303, 256), (257, 1000, 1024),
+                                      (16, 1280, 5120), (17, 257, 512), (29, 3001, 1024), (64, 5003, 512),
+                                      (200, 2303, 256), (257, 1000, 1024),
                                       (600, 700, 256), (600, 700, 512)])
 def test_lm_head_exact(gpu_lib, w_dtype, rows, V, H):
     rng = np.random.default_rng(rows * 1000 + V + w_dtype)

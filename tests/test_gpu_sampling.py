@@ -21,7 +21,7 @@ def q4_pack(codes):
 
 
 @pytest.mark.parametrize("w_dtype", [0, 1, 3])
-@pytest.mark.parametrize("rows,V,H", [(3, 4099, 512), (16, 1280, 5120), (130, 1100, 512)])
+@pytest.mark.parametrize("rows,V,H", [(3, 4099, 512), (16, 1280, 5120), (30, 1100, 1024), (130, 1100, 512)])
 def test_lm_head_logits_match_oracle(gpu_lib, w_dtype, rows, V, H):
     rng = np.random.default_rng(rows + V + w_dtype)
     h = torch.from_numpy(rng.standard_normal((rows, H)).astype(np.float32)).to(torch.bfloat16)

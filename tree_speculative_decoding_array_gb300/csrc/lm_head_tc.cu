@@ -241,6 +241,7 @@ struct LmQ4Params {
     float* logits;     // NULL, or [rows][V] fp32 written by the epilogue
     int rows, H, V, NP, DC, NA, HS, nchunks, vtiles;
     int GK;            // k-blocks per A-slot group and per hidden stage (1, 2 or 4): one wait and one commit each
+    int WS;            // W stages (lm_q4s_kernel; lm_q4_kernel has kQ4WStages)
 };
 
 // One 32-bit word of codes (features 8j..8j+7, feature 8j+i in bits 4i..4i+3) -> four fp16 pairs
@@ -257,6 +258,52 @@ __device__ __forceinline__ void q4_word(uint32_t x, __half2 s2, __half2 b2, __ha
 
 __device__ __forceinline__ uint32_t u4_word(const uint4& v, int i) {
     return i == 0 ? v.x : i == 1 ? v.y : i == 2 ? v.z : v.w;
+}
+
+// Row r (= this thread's TMEM lane) of k-block kk of a landed W stage: 64 codes -> 32 fp16 pairs
+// w = scale * q + bias, stored to TMEM columns [taddr, taddr + 32) (HALVES: as two stores of 16 columns,
+// which keeps fewer registers live).  The caller waits for the store.
+template <bool HALVES = false>
+__device__ __forceinline__ void q4_convert_row(const uint8_t* st, int r, int kk, float sf, float bf, __half2 k1024,
+                                               uint32_t taddr) {
+    const __half2 s2 = __floats2half2_rn(sf, sf), b2 = __floats2half2_rn(bf, bf);
+    // this row's 32 bytes of codes: 16-byte chunks c0, c0 + 1 of box kk / 4 (128-byte swizzle)
+    const uint8_t* rowp = st + (kk >> 2) * 16384 + r * 128;
+    const int c0 = (kk & 3) * 2;
+    const uint4 lo = *reinterpret_cast<const uint4*>(rowp + ((c0 ^ (r & 7)) << 4));
+    const uint4 hi = *reinterpret_cast<const uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4));
+    if (HALVES) {
+        uint32_t h[16];
+        q4_word(lo.x, s2, b2, k1024, h + 0);
+        q4_word(lo.y, s2, b2, k1024, h + 4);
+        q4_word(lo.z, s2, b2, k1024, h + 8);
+        q4_word(lo.w, s2, b2, k1024, h + 12);
+        tc::tmem_st16(taddr, h);
+        q4_word(hi.x, s2, b2, k1024, h + 0);
+        q4_word(hi.y, s2, b2, k1024, h + 4);
+        q4_word(hi.z, s2, b2, k1024, h + 8);
+        q4_word(hi.w, s2, b2, k1024, h + 12);
+        tc::tmem_st16(taddr + 16, h);
+        return;
+    }
+    uint32_t out[32];
+    q4_word(lo.x, s2, b2, k1024, out + 0);
+    q4_word(lo.y, s2, b2, k1024, out + 4);
+    q4_word(lo.z, s2, b2, k1024, out + 8);
+    q4_word(lo.w, s2, b2, k1024, out + 12);
+    q4_word(hi.x, s2, b2, k1024, out + 16);
+    q4_word(hi.y, s2, b2, k1024, out + 20);
+    q4_word(hi.z, s2, b2, k1024, out + 24);
+    q4_word(hi.w, s2, b2, k1024, out + 28);
+    tc::tmem_st32(taddr, out);
+}
+
+template <bool HALVES = false>
+__device__ __forceinline__ void q4_convert_kblock(const uint8_t* st, int r, int kk, const uint4& sc8, const uint4& bi8,
+                                                  __half2 k1024, uint32_t taddr) {
+    const uint32_t sw = u4_word(sc8, kk >> 1), bw = u4_word(bi8, kk >> 1);
+    q4_convert_row<HALVES>(st, r, kk, (kk & 1) ? bf16_hi(sw) : bf16_lo(sw), (kk & 1) ? bf16_hi(bw) : bf16_lo(bw), k1024,
+                           taddr);
 }
 
 // Shared memory: [W ring: 3 x 36 KB] [hidden ring: HS x NP*128 B] ... [bests | barriers].
@@ -439,25 +486,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                         break;
                     }
                     tc::tc_fence_after();
-                    const uint32_t sw = u4_word(sc8, kk >> 1), bw = u4_word(bi8, kk >> 1);
-                    const float sf = (kk & 1) ? bf16_hi(sw) : bf16_lo(sw);
-                    const float bf = (kk & 1) ? bf16_hi(bw) : bf16_lo(bw);
-                    const __half2 s2 = __floats2half2_rn(sf, sf), b2 = __floats2half2_rn(bf, bf);
-                    // this row's 32 bytes of codes: 16-byte chunks c0, c0 + 1 of box kk / 4 (128-byte swizzle)
-                    const uint8_t* rowp = st + (kk >> 2) * 16384 + r * 128;
-                    const int c0 = (kk & 3) * 2;
-                    const uint4 lo = *reinterpret_cast<const uint4*>(rowp + ((c0 ^ (r & 7)) << 4));
-                    const uint4 hi = *reinterpret_cast<const uint4*>(rowp + (((c0 + 1) ^ (r & 7)) << 4));
-                    uint32_t out[32];
-                    q4_word(lo.x, s2, b2, k1024, out + 0);
-                    q4_word(lo.y, s2, b2, k1024, out + 4);
-                    q4_word(lo.z, s2, b2, k1024, out + 8);
-                    q4_word(lo.w, s2, b2, k1024, out + 12);
-                    q4_word(hi.x, s2, b2, k1024, out + 16);
-                    q4_word(hi.y, s2, b2, k1024, out + 20);
-                    q4_word(hi.z, s2, b2, k1024, out + 24);
-                    q4_word(hi.w, s2, b2, k1024, out + 28);
-                    tc::tmem_st32(tmem + lane_base + a_col + (uint32_t)(as * GK + gi) * 32, out);
+                    q4_convert_kblock(st, r, kk, sc8, bi8, k1024, tmem + lane_base + a_col + (uint32_t)(as * GK + gi) * 32);
                     tc::tmem_wait_st();
                     tc::tc_fence_before();
                     __syncwarp();
@@ -477,6 +506,292 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
             tc::tc_fence_after();
             lm_epilogue_tile<LOGITS>(tmem + lane_base + buf * p.DC, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane,
                              p.logits, chunk * p.NP);
+            tc::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
+        }
+    }
+
+    __syncthreads();
+    if (!*abort_flag)
+        for (int c = threadIdx.x; c < nrows; c += blockDim.x)
+            if (s_best[c]) atomicMax(&p.best[chunk * p.NP + c], s_best[c]);
+    if (warp == 5) {
+        tc::tc_fence_after();
+        tc::tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ 4-bit heads, few hidden rows
+// An M = 128 MMA holds its issuing thread for ~44 cycles whatever N is up to 64, while at N = 16 the tensor
+// pipe needs ~8, and one thread issuing every MMA of a tile (4 per k-block) falls behind the converters.
+// Here every converter set has an issuer warp of its own (warps 6 .. 6 + NI - 1, each on its own SM
+// sub-partition) and each issuer its own accumulator: the k-blocks of a tile are split NI ways and the
+// epilogue adds the NI partial sums (fp32) before the argmax.  Set par converts the k-blocks kb = par mod 4
+// into a ring of NAS A slots of its own; issuer i takes the sets par = i mod NI.  Hidden stages hold 4
+// k-blocks, one per set.
+constexpr int kQ4sMaxNP = 32;
+constexpr int kQ4sKBPerHStage = kQ4Sets;
+constexpr int kQ4sMaxWStages = 8;
+constexpr int kQ4sMinHStages = 4;  // the rest of shared memory goes to W stages: they carry the DRAM latency
+// polls before the first sleep: every poll is an issue slot taken from the converters
+constexpr uint32_t kQ4sConvSpins = 2, kQ4sIssSpins = 4;
+
+template <int NI>
+struct Q4s {
+    static constexpr int kConv0 = 6 + NI;                        // first converter warp
+    static constexpr int kThreads = kLmEpi + 64 + NI * 32 + kQ4Conv;
+};
+
+// Sum of the NI accumulators (columns taddr + i * DC) of one tile, then the argmax over this warp's 32
+// vocabulary rows for each of the nrows hidden rows, as lm_epilogue_tile.
+template <bool LOGITS, int NI>
+__device__ __forceinline__ void lm_epilogue_sum(uint32_t taddr, int DC, int nrows, int v, int V,
+                                                unsigned long long* s_best, int lane, float* logits, int row0) {
+    const uint32_t v0 = (uint32_t)(v - lane);
+    for (int c0 = 0; c0 < nrows; c0 += 16) {
+        float acc[16];
+        uint32_t d[16];
+        tc::tmem_ld16(taddr + c0, d);
+        tc::tmem_wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) acc[k] = __uint_as_float(d[k]);
+#pragma unroll
+        for (int i = 1; i < NI; ++i) {
+            tc::tmem_ld16(taddr + (uint32_t)(i * DC) + c0, d);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < 16; ++k) acc[k] += __uint_as_float(d[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+            if (c0 + k < nrows) {  // uniform across the warp
+                if (LOGITS && v < V) logits[(size_t)(row0 + c0 + k) * V + v] = acc[k];
+                const uint32_t o = v < V ? orderable(acc[k]) : 0u;
+                const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, o);
+                const uint32_t who = __ballot_sync(0xFFFFFFFFu, o == mx);
+                if (lane == 0 && mx != 0u) {
+                    const uint32_t idx = v0 + (uint32_t)(__ffs(who) - 1);
+                    atomicMax(&s_best[c0 + k], ((unsigned long long)mx << 32) | (unsigned long long)(0xFFFFFFFFu - idx));
+                }
+            }
+        }
+    }
+}
+
+// Shared memory: [W ring: WS x 36 KB] [hidden ring: HS stages of 4 k-blocks] ... [bests | barriers]; the W ring
+// takes all but kQ4sMinHStages hidden stages, since its stages carry the DRAM latency (~5 us from TMA issue to
+// landing under full load) while the hidden blocks come from L2.  TMEM: accumulators [buf][issuer] of DC
+// columns from 0, then 4 x NAS A slots of 32 columns (set par owns slots par * NAS .. par * NAS + NAS - 1).
+template <bool LOGITS, int NI>
+__global__ void __launch_bounds__(Q4s<NI>::kThreads, 1) lm_q4s_kernel(const __grid_constant__ LmQ4Params p) {
+    griddep_begin();
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* sm = align1024(smem_raw);
+    uint8_t* wring = sm;
+    uint8_t* hring = sm + p.WS * kQ4WStage;
+    uint8_t* tail = sm + kLmUsable;
+    unsigned long long* s_best = reinterpret_cast<unsigned long long*>(tail);  // [256]
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tail + 2048);
+    uint64_t* wfull = bars;           // [8]
+    uint64_t* wempty = bars + 8;      // [8] every converter warp is done with the stage
+    uint64_t* hfull = bars + 16;      // [16]
+    uint64_t* hempty = bars + 32;     // [16] the MMAs of all 4 k-blocks of the stage are done
+    uint64_t* afull = bars + 48;      // [16] slot written by its set's 4 warps
+    uint64_t* aempty = bars + 64;     // [16] MMAs done with the slot
+    uint64_t* acc_full = bars + 80;   // [2] every issuer's MMAs of the tile are done
+    uint64_t* acc_empty = bars + 82;  // [2]
+    uint64_t* drain = bars + 84;      // [4] one per issuer
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 88);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 89);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int chunk = blockIdx.x % p.nchunks;
+    const int group = blockIdx.x / p.nchunks;
+    const int groups = gridDim.x / p.nchunks;
+    const int KB = p.H / kLmKB;
+    const int NSt = KB / kQ4KBPerStage;
+    const int NAS = p.NA, HS = p.HS, DC = p.DC, WS = p.WS;  // A slots per set, hidden and W stages, accumulator columns
+    const int nrows = min(p.NP, p.rows - chunk * p.NP);
+    if (group >= p.vtiles || nrows <= 0) return;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < WS; ++s) {
+            tc::mbar_init(&wfull[s], 1);
+            tc::mbar_init(&wempty[s], kQ4Conv / 32);
+        }
+        for (int s = 0; s < HS; ++s) {
+            tc::mbar_init(&hfull[s], 1);
+            tc::mbar_init(&hempty[s], kQ4sKBPerHStage);
+        }
+        for (int s = 0; s < kQ4Sets * NAS; ++s) {
+            tc::mbar_init(&afull[s], 4);
+            tc::mbar_init(&aempty[s], 1);
+        }
+        for (int s = 0; s < 2; ++s) {
+            tc::mbar_init(&acc_full[s], NI);
+            tc::mbar_init(&acc_empty[s], kLmEpi / 32);
+        }
+        for (int s = 0; s < NI; ++s) tc::mbar_init(&drain[s], 1);
+        *abort_flag = 0;
+        tc::fence_mbar_init();
+    }
+    for (int c = threadIdx.x; c < 256; c += blockDim.x) s_best[c] = 0ull;
+    if (warp == 5) {
+        tc::tmem_alloc(tmem_slot, 512);
+        tc::tmem_relinquish();
+    }
+    __syncthreads();
+    tc::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const uint32_t a_col = 2u * (uint32_t)(NI * DC);
+    const uint32_t h_bytes = (uint32_t)p.NP * 128;
+
+    if (warp == 4) {
+        if (lane == 0) {
+            // -------------------------------------------------------- W stages: codes, scales, biases of 8 k-blocks
+            tc::tma_prefetch_desc(&p.wmap);
+            tc::tma_prefetch_desc(&p.smap);
+            tc::tma_prefetch_desc(&p.bmap);
+            int c = 0, issued = 0, s = 0;
+            uint32_t fill = 0;  // parity of stage s's current fill
+            bool ok = true;
+            for (int vt = group; ok && vt < p.vtiles; vt += groups) {
+                for (int i = 0; i < NSt; ++i, ++c) {
+                    if (c >= WS && !tc::mbar_wait(&wempty[s], fill ^ 1u, abort_flag, 512)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = wring + s * kQ4WStage;
+                    tc::mbar_expect_tx(&wfull[s], kQ4WStage);
+                    tc::tma_load_2d(st, &p.wmap, &wfull[s], i * 256, vt * kLmM);
+                    tc::tma_load_2d(st + 16384, &p.wmap, &wfull[s], i * 256 + 128, vt * kLmM);
+                    tc::tma_load_2d(st + 32768, &p.smap, &wfull[s], i * kQ4KBPerStage, vt * kLmM);
+                    tc::tma_load_2d(st + 34816, &p.bmap, &wfull[s], i * kQ4KBPerStage, vt * kLmM);
+                    issued = c + 1;
+                    if (++s == WS) { s = 0; fill ^= 1u; }
+                }
+            }
+            if (*abort_flag)
+                for (int q = max(0, issued - WS); q < issued; ++q)
+                    lm_drain_wait(&wfull[q % WS], (q / WS) & 1);
+        }
+    } else if (warp == 5) {
+        if (lane == 0) {
+            // -------------------------------------------------------- hidden blocks, 4 k-blocks per stage
+            tc::tma_prefetch_desc(&p.hmap);
+            int g = 0, issued = 0, s = 0;
+            uint32_t fill = 0;
+            bool ok = true;
+            for (int vt = group; ok && vt < p.vtiles; vt += groups) {
+                for (int kb = 0; kb < KB; kb += kQ4sKBPerHStage, ++g) {
+                    if (g >= HS && !tc::mbar_wait(&hempty[s], fill ^ 1u, abort_flag, 512)) { ok = false; break; }
+                    tc::mbar_expect_tx(&hfull[s], h_bytes * kQ4sKBPerHStage);
+                    for (int u = 0; u < kQ4sKBPerHStage; ++u)
+                        tc::tma_load_2d(hring + (s * kQ4sKBPerHStage + u) * h_bytes, &p.hmap, &hfull[s], (kb + u) * kLmKB,
+                                        chunk * p.NP);
+                    issued = g + 1;
+                    if (++s == HS) { s = 0; fill ^= 1u; }
+                }
+            }
+            if (*abort_flag)
+                for (int q = max(0, issued - HS); q < issued; ++q) lm_drain_wait(&hfull[q % HS], (q / HS) & 1);
+        }
+    } else if (warp >= 6 && warp < Q4s<NI>::kConv0) {
+        // ------------------------------------------------------------ issuer iss: k-blocks of sets iss, iss + NI, ...
+        const int iss = warp - 6;
+        if (lane == 0) {
+            const uint32_t idesc = tc::idesc_f16(false, false, false, kLmM, p.NP);
+            const uint64_t hdesc0 = tc::sdesc_sw128(tc::smem_u32(hring), 16, 1024);
+            int it = 0, hs = 0, slot = 0;  // hidden stage; A slot (the same in every set: one k-block per stage each)
+            uint32_t hph = 0, aph = 0;
+            bool ok = true;
+            for (int vt = group; ok && vt < p.vtiles; vt += groups, ++it) {
+                const int buf = it & 1;
+                if (it >= 2 && !tc::mbar_wait_spin(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
+                tc::tc_fence_after();
+                const uint32_t d = tmem + (uint32_t)((buf * NI + iss) * DC);
+                for (int kb0 = 0; ok && kb0 < KB; kb0 += kQ4sKBPerHStage) {
+                    if (!tc::mbar_wait(&hfull[hs], hph, abort_flag, 64, kQ4sIssSpins)) { ok = false; break; }
+                    for (int u = iss; u < kQ4sKBPerHStage; u += NI) {  // set u converts k-block kb0 + u
+                        const int sl = u * NAS + slot;
+                        if (!tc::mbar_wait(&afull[sl], aph, abort_flag, 64, kQ4sIssSpins)) { ok = false; break; }
+                        tc::tc_fence_after();
+                        const uint32_t a = tmem + a_col + (uint32_t)sl * 32;
+                        const uint64_t b = tc::sdesc_add(hdesc0, (uint32_t)(hs * kQ4sKBPerHStage + u) * h_bytes);
+                        const uint32_t first = (kb0 == 0 && u == iss) ? 0u : 1u;
+                        tc::mma_f16_ts(d, a, b, idesc, first);
+                        tc::mma_f16_ts(d, a + 8, tc::sdesc_add(b, 32), idesc, 1u);
+                        tc::mma_f16_ts(d, a + 16, tc::sdesc_add(b, 64), idesc, 1u);
+                        tc::mma_f16_ts(d, a + 24, tc::sdesc_add(b, 96), idesc, 1u);
+                        tc::mma_commit(&aempty[sl]);
+                        tc::mma_commit(&hempty[hs]);
+                    }
+                    if (++slot == NAS) { slot = 0; aph ^= 1u; }
+                    if (++hs == HS) { hs = 0; hph ^= 1u; }
+                }
+                if (ok) tc::mma_commit(&acc_full[buf]);
+            }
+            tc::mma_commit(&drain[iss]);
+            lm_drain_wait(&drain[iss], 0);
+        }
+    } else if (warp >= Q4s<NI>::kConv0) {
+        // ------------------------------------------------------------ converters: codes -> fp16 A slots in TMEM
+        // Set par converts k-blocks par and par + 4 of every W stage into its own ring of NAS slots; every
+        // index and parity advances by increments (no division on this path), and warp-level arrivals are
+        // predicated on one elected lane.
+        const int cw = warp - Q4s<NI>::kConv0;
+        const int par = cw >> 2, quad = warp & 3;
+        const int r = quad * 32 + lane;  // vocabulary row within the tile = TMEM lane
+        const uint32_t a_set = tmem + ((uint32_t)(quad * 32) << 16) + a_col + (uint32_t)(par * NAS) * 32;
+        uint64_t* afull_set = afull + par * NAS;
+        uint64_t* aempty_set = aempty + par * NAS;
+        const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
+        int ws = 0, slot = 0, n = 0;  // W stage, A slot, k-blocks converted
+        uint32_t wph = 0, use = 0;    // parity of stage ws's fill; parity of slot's current use
+        bool ok = true;
+        for (int vt = group; ok && vt < p.vtiles; vt += groups) {
+            for (int i = 0; ok && i < NSt; ++i) {
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&wfull[ws], wph, abort_flag, 256, kQ4sConvSpins))) {
+                    ok = false;
+                    break;
+                }
+                const uint8_t* st = wring + ws * kQ4WStage;
+                const uint16_t* scr = reinterpret_cast<const uint16_t*>(st + 32768 + r * 16);
+                const uint16_t* bir = reinterpret_cast<const uint16_t*>(st + 34816 + r * 16);
+#pragma unroll
+                for (int h = 0; h < kQ4KBPerStage / kQ4Sets; ++h) {
+                    const int kk = par + kQ4Sets * h;
+                    if (n >= NAS && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&aempty_set[slot], use ^ 1u, abort_flag, 256,
+                                                                           kQ4sConvSpins))) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    q4_convert_row<true>(st, r, kk, __uint_as_float((uint32_t)scr[kk] << 16),
+                                         __uint_as_float((uint32_t)bir[kk] << 16), k1024, a_set + (uint32_t)slot * 32);
+                    tc::tmem_wait_st();
+                    tc::tc_fence_before();
+                    __syncwarp();
+                    tc::mbar_arrive_one(&afull_set[slot]);
+                    ++n;
+                    if (++slot == NAS) { slot = 0; use ^= 1u; }
+                }
+                __syncwarp();
+                tc::mbar_arrive_one(&wempty[ws]);
+                if (++ws == WS) { ws = 0; wph ^= 1u; }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ argmax epilogue (warps 0-3)
+        const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+        int it = 0;
+        for (int vt = group; vt < p.vtiles; vt += groups, ++it) {
+            const int buf = it & 1;
+            if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, 1024))) break;
+            tc::tc_fence_after();
+            lm_epilogue_sum<LOGITS, NI>(tmem + lane_base + (uint32_t)(buf * NI * DC), DC, nrows, vt * kLmM + warp * 32 + lane,
+                                        p.V, s_best, lane, p.logits, chunk * p.NP);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
@@ -611,6 +926,28 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
     prm.vtiles = (V + kLmM - 1) / kLmM;
     const int sms = sm_count();
     const int groups = sms / nchunks > 0 ? sms / nchunks : 1;
+    if (NP <= kQ4sMaxNP) {
+        // few hidden rows: one issuer and one accumulator per converter set
+        constexpr int NI = kQ4Sets;
+        prm.DC = NP;
+        prm.NA = (512 - 2 * NI * NP) / 32 / kQ4Sets;
+        prm.NA = prm.NA > 4 ? 4 : prm.NA;
+        const int hst = NP * 128 * kQ4sKBPerHStage;
+        const int ws = (kLmUsable - kQ4sMinHStages * hst) / kQ4WStage;
+        prm.WS = ws > kQ4sMaxWStages ? kQ4sMaxWStages : ws;
+        const int hs = (kLmUsable - prm.WS * kQ4WStage) / hst;
+        prm.HS = hs > kQ4MaxHStages ? kQ4MaxHStages : hs;
+        if (prm.WS < 2 || prm.HS < 2 || prm.NA < 1)  // the rings index stages modulo their counts
+            return fail(TSV_EUNSUPPORTED, "lm_head_argmax: shared memory too small for the 4-bit pipeline");
+        if (logits) {
+            cudaFuncSetAttribute(lm_q4s_kernel<true, NI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+            launch_pdl(lm_q4s_kernel<true, NI>, groups * nchunks, Q4s<NI>::kThreads, kLmSmem, stream, prm);
+        } else {
+            cudaFuncSetAttribute(lm_q4s_kernel<false, NI>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
+            launch_pdl(lm_q4s_kernel<false, NI>, groups * nchunks, Q4s<NI>::kThreads, kLmSmem, stream, prm);
+        }
+        return check_launch("lm_head_argmax(tcgen05, 4-bit, few rows)");
+    }
     if (logits) {
         cudaFuncSetAttribute(lm_q4_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kLmSmem);
         launch_pdl(lm_q4_kernel<true>, groups * nchunks, kQ4Threads, kLmSmem, stream, prm);

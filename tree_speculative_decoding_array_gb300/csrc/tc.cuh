@@ -26,6 +26,14 @@ __device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// One lane of the converged warp arrives: elect.sync plus a predicated arrive, so no divergent branch (whose
+// reconvergence costs the warp issue slots) is taken.
+__device__ __forceinline__ void mbar_arrive_one(uint64_t* bar) {
+    asm volatile(
+        "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n @p mbarrier.arrive.shared::cta.b64 _, [%0];\n}" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
 }
