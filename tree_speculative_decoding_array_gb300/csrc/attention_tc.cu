@@ -343,7 +343,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             const bool bf = p.mma_bf16 != 0;
             const uint32_t id_qk = tc::idesc_f16(bf, false, false, kTcRows, kTcBK);
             const uint32_t id_pv = tc::idesc_f16(bf, false, true, kTcRows, kTcD);
-            const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV);
+            const uint64_t dK0 = tc::sdesc_sw128(tc::smem_u32(sK), 16, 1024);
+            const uint64_t dV0 = tc::sdesc_sw128(tc::smem_u32(sV), 8192, 1024);
             bool ok = tc::mbar_wait_spin(q_full, 0, abort_flag);
             if (ok) tc::tc_fence_after();
             int sj = 0, pj = 0;
@@ -359,10 +360,10 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
                     if (ready) ready = I8 ? tc::mbar_test(&vc_full[cb], (pj >> 1) & 1) : tc::mbar_test(&vfull[st], (pj / NS) & 1);
                     if (ready) {
                         tc::tc_fence_after();
-                        const uint32_t vbase = aV + (I8 ? cb : st) * kTileBytes;
+                        const uint64_t vdesc = tc::sdesc_add(dV0, (uint32_t)(I8 ? cb : st) * kTileBytes);
 #pragma unroll
                         for (int kk = 0; kk < kTcBK / 16; ++kk) {  // A = P, 16-bit pairs over S buffer cb
-                            const uint64_t db = tc::sdesc_sw128(vbase + kk * 2048, 8192, 1024);
+                            const uint64_t db = tc::sdesc_add(vdesc, kk * 2048);
                             tc::mma_f16_ts(tmem + kColO, tmem + kColS + cb * kTcBK + kk * 8, db, id_pv,
                                            (pj > 0 || kk > 0) ? 1u : 0u);
                         }
@@ -378,10 +379,10 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
                     if (ready && sj >= 2) ready = tc::mbar_test(&sp_free[sb], ((sj >> 1) - 1) & 1);
                     if (ready) {
                         tc::tc_fence_after();
-                        const uint32_t kbase = aK + (I8 ? sb : st) * kTileBytes;
+                        const uint64_t kdesc = tc::sdesc_add(dK0, (uint32_t)(I8 ? sb : st) * kTileBytes);
 #pragma unroll
                         for (int kk = 0; kk < kTcD / 16; ++kk) {
-                            const uint64_t db = tc::sdesc_sw128(kbase + (kk >> 2) * 8192 + (kk & 3) * 32, 16, 1024);
+                            const uint64_t db = tc::sdesc_add(kdesc, (kk >> 2) * 8192 + (kk & 3) * 32);
                             tc::mma_f16_ts(tmem + kColS + sb * kTcBK, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
                         }
                         tc::mma_commit(&s_full[sb]);
@@ -419,10 +420,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             convert_i8_tile(sRawV + st * 16384, sV + cb * kTileBytes, nk, ct);
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(&vempty[st]);
-                tc::mbar_arrive(&vc_full[cb]);
-            }
+            tc::mbar_arrive_one(&vempty[st]);
+            tc::mbar_arrive_one(&vc_full[cb]);
         }
     } else if (I8 && warp >= 6 && warp < 10) {
         // ------------------------------------------------------------ Int8 K converters (and every tile's scales)
@@ -452,15 +451,13 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
                 if (ct < 64) v *= 1.4426950408889634f * 0.0625f;  // K scales carry log2(e) / sqrt(256)
                 sScale[slot * 128 + ct] = v;
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&sc_full[slot]);
+                tc::mbar_arrive_one(&sc_full[slot]);
             }
             convert_i8_tile(sRawK + st * 16384, sK + cb * kTileBytes, nk, ct);
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(&kempty[st]);
-                tc::mbar_arrive(&kc_full[cb]);
-            }
+            tc::mbar_arrive_one(&kempty[st]);
+            tc::mbar_arrive_one(&kc_full[cb]);
         }
     } else if (warp < 4 || warp >= kSoftB) {
         // ------------------------------------------------------------ softmax, in two halves
@@ -506,7 +503,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             tc::tmem_wait_st();
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(q_full);
+            tc::mbar_arrive_one(q_full);
         }
         // exchange number jj (one per tile, then one for the row sums): xv[(jj & 1) * 2 + half][row]
         auto exchange = [&](int jj, float mine, float& other) -> bool {
@@ -514,7 +511,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             xv[(slot * 2 + h) * kTcRows + r] = mine;
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&xch[qd * 2 + slot]);
+            tc::mbar_arrive_one(&xch[qd * 2 + slot]);
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&xch[qd * 2 + slot], (jj >> 1) & 1, abort_flag))) return false;
             tc::tc_fence_after();
             other = xv[(slot * 2 + (h ^ 1)) * kTcRows + r];
@@ -623,7 +620,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             if (zero_v) tc::fence_proxy_async_smem();  // the zeroed V rows
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&p_full[sb]);
+            tc::mbar_arrive_one(&p_full[sb]);
         }
         if (ok) {  // the row sum of both halves
             float lo;
@@ -808,7 +805,10 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
             const bool bf = p.mma_bf16 != 0;
             const uint32_t id_qk = tc::idesc_f16(bf, false, false, kTcRows, kWK);
             const uint32_t id_pv = tc::idesc_f16(bf, false, true, kTcRows, kTcD);
-            const uint32_t aK = tc::smem_u32(sK), aV = tc::smem_u32(sV), aP = tc::smem_u32(sP);
+            // descriptors built once; each MMA adds its byte offset to the address field
+            const uint64_t dK0 = tc::sdesc_sw128(tc::smem_u32(sK), 16, 1024);
+            const uint64_t dV0 = tc::sdesc_sw128(tc::smem_u32(sV), 8192, 1024);
+            const uint64_t dP0 = tc::sdesc_sw128(tc::smem_u32(sP), 16, 1024);
             bool ok = tc::mbar_wait_spin(q_full, 0, abort_flag);
             if (ok) tc::tc_fence_after();
             int sj = 0, pq = 0;  // next Q K^T tile, next P V half
@@ -822,11 +822,11 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
                     if (ready) ready = tc::mbar_test(&vfull[st], (pq >> 1) & 1);
                     if (ready) {
                         tc::tc_fence_after();
-                        const uint32_t vbase = aV + st * kTileBytes, pbase = aP + h * 16384;
+                        const uint64_t dv = tc::sdesc_add(dV0, st * kTileBytes), dp = tc::sdesc_add(dP0, h * 16384);
 #pragma unroll
                         for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                            const uint64_t da = tc::sdesc_sw128(pbase + kk * 32, 16, 1024);
-                            const uint64_t db = tc::sdesc_sw128(vbase + kk * 2048, 8192, 1024);
+                            const uint64_t da = tc::sdesc_add(dp, kk * 32);
+                            const uint64_t db = tc::sdesc_add(dv, kk * 2048);
                             tc::mma_f16(tmem + kColO, da, db, id_pv, (pq > 0 || kk > 0) ? 1u : 0u);
                         }
                         tc::mma_commit(&p_free[h]);
@@ -841,10 +841,10 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
                     if (ready && sj >= 1) ready = tc::mbar_test(s_free, (sj - 1) & 1);
                     if (ready) {
                         tc::tc_fence_after();
-                        const uint32_t kbase = aK + st * kWKTile;
+                        const uint64_t dk = tc::sdesc_add(dK0, st * kWKTile);
 #pragma unroll
                         for (int kk = 0; kk < kTcD / 16; ++kk) {
-                            const uint64_t db = tc::sdesc_sw128(kbase + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024);
+                            const uint64_t db = tc::sdesc_add(dk, (kk >> 2) * 16384 + (kk & 3) * 32);
                             tc::mma_f16_ts(tmem + kColS, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
                         }
                         tc::mma_commit(s_full);
@@ -907,7 +907,7 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
             tc::tmem_wait_st();
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(q_full);
+            tc::mbar_arrive_one(q_full);
         }
         const float qk_scale = 1.4426950408889634f * 0.0625f;  // log2(e) / sqrt(256)
         float m_ref = -INFINITY, l = 0.f;
@@ -926,7 +926,7 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
             }
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(s_free);
+            tc::mbar_arrive_one(s_free);
 
             const int c0 = k_begin + j * kWK;
             if (c0 + kWK <= k_end && c0 + kWK <= S && c0 >= lo_last) {
@@ -1000,7 +1000,7 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
                 tc::fence_proxy_async_smem();
                 tc::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&p_full[h]);
+                tc::mbar_arrive_one(&p_full[h]);
             }
             if (!ok) break;
             l = l * alpha + ps;
@@ -1334,10 +1334,8 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
             }
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(&kr_empty[rs]);
-                tc::mbar_arrive(&kq_full[q]);
-            }
+            tc::mbar_arrive_one(&kr_empty[rs]);
+            tc::mbar_arrive_one(&kq_full[q]);
             if (q == 3) sc_cur = sc_nxt;
         }
     } else if (warp >= 15) {
@@ -1361,10 +1359,8 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
             convert_i8_tile_scaled(sVr + st * 16384, sVh + st * 32768, nk, ct, s2);
             tc::fence_proxy_async_smem();
             __syncwarp();
-            if (lane == 0) {
-                tc::mbar_arrive(&vr_empty[st]);
-                tc::mbar_arrive(&vh_full[st]);
-            }
+            tc::mbar_arrive_one(&vr_empty[st]);
+            tc::mbar_arrive_one(&vh_full[st]);
             sc_cur = sc_nxt;
         }
     } else {
@@ -1400,13 +1396,13 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
             tc::tmem_wait_st();
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(q_full);
+            tc::mbar_arrive_one(q_full);
         }
         auto exchange = [&](int jj, float mine, float& other) -> bool {
             const int slot = jj & 1;
             xv[(slot * 2 + h) * kTcRows + r] = mine;
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&xch[qd * 2 + slot]);
+            tc::mbar_arrive_one(&xch[qd * 2 + slot]);
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&xch[qd * 2 + slot], (jj >> 1) & 1, abort_flag))) return false;
             other = xv[(slot * 2 + (h ^ 1)) * kTcRows + r];
             return true;
@@ -1427,7 +1423,7 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
             }
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(s_free);
+            tc::mbar_arrive_one(s_free);
             const int ct = k_begin + j * kWK;  // first key of the tile
             const int c0 = ct + h * 64;        // first key of this half
             if (!(ct + kWK <= k_end && ct + kWK <= S && ct >= lo_last)) {  // some key of the tile is masked
@@ -1484,7 +1480,7 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
             tc::fence_proxy_async_smem();
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&p_full[h]);
+            tc::mbar_arrive_one(&p_full[h]);
             l = l * alpha + ps;
         }
         if (ok) {  // the row sum of both halves
