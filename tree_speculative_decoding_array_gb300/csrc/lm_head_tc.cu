@@ -16,9 +16,11 @@
 // holding it, and merges the packed (logit, ~index) key with a shared atomic
 // maximum; the CTA's bests go to global memory once at the end.
 //
-// 16-bit heads (lm_tc_kernel): warp 4 streams W block [128 x 64] and hidden
-// block [NP x 64] (both 128-byte swizzled) through one ring of as many stages
-// (up to 16) as shared memory holds; warp 5 issues the MMAs from shared memory.
+// 16-bit heads (lm_tc_kernel): warp 4 streams W blocks [128 x 64] from HBM
+// through a ring of up to 16 stages, warp 6 the hidden blocks [NP x 64] (L2
+// hits after the first vocabulary tile) through a ring of 3-4 (both 128-byte
+// swizzled): the W ring carries the DRAM latency, so it gets the shared
+// memory; warp 5 issues the MMAs from shared memory.
 //
 // 4-bit heads (lm_q4_kernel): the dequantised weights never touch shared
 // memory.  Warp 4 streams the raw codes of 8 k-blocks plus their scales and
@@ -84,34 +86,41 @@ __device__ __forceinline__ void lm_drain_wait(uint64_t* bar, uint32_t parity) {
 
 // ------------------------------------------------------------------ 16-bit heads
 constexpr int kLmMaxStages = 16;
-constexpr int kLmThreads16 = kLmEpi + 64;
+constexpr int kLmMaxHStages = 8;
+constexpr int kLmHStages256 = 4;  // hidden stages at 256 rows (32 KB each)
+constexpr uint32_t kLmProdSleep = 256;  // producers' longest sleep between polls (ns)
+constexpr int kLmThreads16 = kLmEpi + 96;
 
 struct LmTcParams {
     CUtensorMap wmap;
     CUtensorMap hmap;
     unsigned long long* best;
     float* logits;  // NULL, or [rows][V] fp32 written by the epilogue
-    int rows, H, V, NP, nchunks, vtiles, mma_bf16, stages, stage_bytes;
+    int rows, H, V, NP, nchunks, vtiles, mma_bf16;
+    int stages, hstages;  // W ring stages (16 KB each), hidden ring stages (NP x 128 B each)
 };
 
-// Shared memory: [TMA ring: stages x (W block 16 KB | hidden block NP x 128 B)] ... [bests | barriers]
+// Shared memory: [W ring: stages x 16 KB] [hidden ring: hstages x NP*128 B] ... [bests | barriers]
 template <bool LOGITS>
 __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_constant__ LmTcParams p) {
     griddep_begin();
-    const int S = p.stages;
+    const int S = p.stages, HS = p.hstages;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
-    uint8_t* ring = sm;  // [S][stage_bytes]
+    uint8_t* ring = sm;                  // [S][16 KB]
+    uint8_t* hring = sm + S * 16384;     // [HS][NP * 128]
     uint8_t* tail = sm + kLmUsable;
     unsigned long long* s_best = reinterpret_cast<unsigned long long*>(tail);  // [256]
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail + 2048);
-    uint64_t* full = bars;            // [16]
-    uint64_t* empty = bars + 16;      // [16]
-    uint64_t* acc_full = bars + 32;   // [2]
-    uint64_t* acc_empty = bars + 34;  // [2]
-    uint64_t* drain = bars + 36;
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 37);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 38);
+    uint64_t* full = bars;            // [16] W block landed
+    uint64_t* empty = bars + 16;      // [16] MMAs done with it
+    uint64_t* hfull = bars + 32;      // [8] hidden block landed
+    uint64_t* hempty = bars + 40;     // [8]
+    uint64_t* acc_full = bars + 48;   // [2]
+    uint64_t* acc_empty = bars + 50;  // [2]
+    uint64_t* drain = bars + 52;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 53);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 54);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int chunk = blockIdx.x % p.nchunks;
@@ -125,6 +134,10 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
         for (int s = 0; s < S; ++s) {
             tc::mbar_init(&full[s], 1);
             tc::mbar_init(&empty[s], 1);
+        }
+        for (int s = 0; s < HS; ++s) {
+            tc::mbar_init(&hfull[s], 1);
+            tc::mbar_init(&hempty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&acc_full[s], 1);
@@ -144,56 +157,69 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
     const uint32_t b_bytes = (uint32_t)p.NP * 128;
 
-    if (warp == 4) {
-        // ------------------------------------------------------------ TMA producer
+    if (warp == 4 || warp == 6) {
+        // ------------------------------------------------------------ TMA producers: warp 4 W blocks, warp 6 hidden
+        // (a warp each: a lane that sleeps in its wait would hold up the other producer)
         if (lane == 0) {
-            tc::tma_prefetch_desc(&p.wmap);
-            tc::tma_prefetch_desc(&p.hmap);
-            int g = 0, issued = 0;
+            const bool isW = warp == 4;
+            const CUtensorMap* m = isW ? &p.wmap : &p.hmap;
+            const int R = isW ? S : HS;
+            uint64_t* fullb = isW ? full : hfull;
+            uint64_t* emptyb = isW ? empty : hempty;
+            uint8_t* base = isW ? ring : hring;
+            const uint32_t bytes = isW ? 16384u : b_bytes;
+            tc::tma_prefetch_desc(m);
+            int g = 0, issued = 0, st = 0;
+            uint32_t fill = 0;  // parity of stage st's current fill
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups) {
                 for (int kb = 0; kb < KB; ++kb, ++g) {
-                    const int st = g % S;
-                    if (g >= S && !tc::mbar_wait(&empty[st], ((g / S) - 1) & 1, abort_flag, 256)) { ok = false; break; }
-                    uint8_t* stage = ring + st * p.stage_bytes;
-                    tc::mbar_expect_tx(&full[st], 16384 + b_bytes);
-                    tc::tma_load_2d(stage, &p.wmap, &full[st], kb * kLmKB, vt * kLmM);
-                    tc::tma_load_2d(stage + 16384, &p.hmap, &full[st], kb * kLmKB, chunk * p.NP);
+                    if (g >= R && !tc::mbar_wait(&emptyb[st], fill ^ 1u, abort_flag, kLmProdSleep)) { ok = false; break; }
+                    tc::mbar_expect_tx(&fullb[st], bytes);
+                    tc::tma_load_2d(base + st * bytes, m, &fullb[st], kb * kLmKB, isW ? vt * kLmM : chunk * p.NP);
                     issued = g + 1;
+                    if (++st == R) { st = 0; fill ^= 1u; }
                 }
             }
             if (*abort_flag)
-                for (int q = max(0, issued - S); q < issued; ++q) lm_drain_wait(&full[q % S], (q / S) & 1);
+                for (int q = max(0, issued - R); q < issued; ++q) lm_drain_wait(&fullb[q % R], (q / R) & 1);
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_f16(p.mma_bf16 != 0, false, false, kLmM, p.NP);
-            const uint32_t rbase = tc::smem_u32(ring);
-            int it = 0, st = 0;
-            uint32_t ph = 0;  // phase parity of the ring
+            const uint64_t dW0 = tc::sdesc_sw128(tc::smem_u32(ring), 16, 1024);
+            const uint64_t dH0 = tc::sdesc_sw128(tc::smem_u32(hring), 16, 1024);
+            int it = 0, st = 0, hs = 0;
+            uint32_t ph = 0, hph = 0;  // phase parities of the two rings
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups, ++it) {
                 const int buf = it & 1;
                 if (it >= 2 && !tc::mbar_wait_spin(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!tc::mbar_wait_spin(&full[st], ph, abort_flag)) { ok = false; break; }
+                    if (!tc::mbar_wait_spin(&full[st], ph, abort_flag) || !tc::mbar_wait_spin(&hfull[hs], hph, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
                     tc::tc_fence_after();
-                    const uint32_t sa = rbase + st * p.stage_bytes;
+                    const uint64_t da = tc::sdesc_add(dW0, (uint32_t)st * 16384u);
+                    const uint64_t db = tc::sdesc_add(dH0, (uint32_t)hs * b_bytes);
 #pragma unroll
                     for (int kk = 0; kk < kLmKB / 16; ++kk)
-                        tc::mma_f16(tmem + buf * 256, tc::sdesc_sw128(sa + kk * 32, 16, 1024),
-                                    tc::sdesc_sw128(sa + 16384 + kk * 32, 16, 1024), idesc, (kb > 0 || kk > 0) ? 1u : 0u);
+                        tc::mma_f16(tmem + buf * 256, tc::sdesc_add(da, kk * 32), tc::sdesc_add(db, kk * 32), idesc,
+                                    (kb > 0 || kk > 0) ? 1u : 0u);
                     tc::mma_commit(&empty[st]);
+                    tc::mma_commit(&hempty[hs]);
                     if (++st == S) { st = 0; ph ^= 1u; }
+                    if (++hs == HS) { hs = 0; hph ^= 1u; }
                 }
                 if (ok) tc::mma_commit(&acc_full[buf]);
             }
             tc::mma_commit(drain);
             lm_drain_wait(drain, 0);
         }
-    } else {
+    } else if (warp < 4) {
         // ------------------------------------------------------------ argmax epilogue
         const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
         int it = 0;
@@ -205,7 +231,7 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
                              p.logits, chunk * p.NP);
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
+            tc::mbar_arrive_one(&acc_empty[buf]);
         }
     }
 
@@ -987,8 +1013,10 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
     prm.nchunks = nchunks;
     prm.vtiles = (V + kLmM - 1) / kLmM;
     prm.mma_bf16 = w_dtype == TSV_BF16;
-    prm.stage_bytes = 16384 + NP * 128;  // multiples of 1024: every block stays 1024-aligned
-    const int stages = kLmUsable / prm.stage_bytes;
+    // hidden blocks (NP x 128 B, multiples of 1024: every block stays 1024-aligned) come from L2 after the first
+    // tile: 3 stages at 256 rows, 4 below; the W ring takes the rest
+    prm.hstages = NP >= 256 ? kLmHStages256 : NP >= 128 ? 5 : 4;
+    const int stages = (kLmUsable - prm.hstages * NP * 128) / 16384;
     prm.stages = stages > kLmMaxStages ? kLmMaxStages : stages;
     if (prm.stages < 2) return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the pipeline");
     const int sms = sm_count();
