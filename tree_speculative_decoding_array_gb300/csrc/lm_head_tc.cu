@@ -407,12 +407,12 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
             tc::tma_prefetch_desc(&p.wmap);
             tc::tma_prefetch_desc(&p.smap);
             tc::tma_prefetch_desc(&p.bmap);
-            int c = 0, issued = 0;
+            int c = 0, issued = 0, s = 0;
+            uint32_t fill = 0;  // parity of stage s's current fill
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups) {
                 for (int i = 0; i < NSt; ++i, ++c) {
-                    const int s = c % kQ4WStages;
-                    if (c >= kQ4WStages && !tc::mbar_wait(&wempty[s], ((c / kQ4WStages) - 1) & 1, abort_flag, 512)) {
+                    if (c >= kQ4WStages && !tc::mbar_wait(&wempty[s], fill ^ 1u, abort_flag, 512)) {
                         ok = false;
                         break;
                     }
@@ -423,6 +423,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                     tc::tma_load_2d(st + 32768, &p.smap, &wfull[s], i * kQ4KBPerStage, vt * kLmM);
                     tc::tma_load_2d(st + 34816, &p.bmap, &wfull[s], i * kQ4KBPerStage, vt * kLmM);
                     issued = c + 1;
+                    if (++s == kQ4WStages) { s = 0; fill ^= 1u; }
                 }
             }
             if (*abort_flag)
@@ -433,16 +434,17 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
         if (lane == 0) {
             // -------------------------------------------------------- hidden blocks, GK k-blocks per stage
             tc::tma_prefetch_desc(&p.hmap);
-            int g = 0, issued = 0;
+            int g = 0, issued = 0, s = 0;
+            uint32_t fill = 0;
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups) {
                 for (int kb = 0; kb < KB; kb += GK, ++g) {
-                    const int s = g % HS;
-                    if (g >= HS && !tc::mbar_wait(&hempty[s], ((g / HS) - 1) & 1, abort_flag, 512)) { ok = false; break; }
+                    if (g >= HS && !tc::mbar_wait(&hempty[s], fill ^ 1u, abort_flag, 512)) { ok = false; break; }
                     tc::mbar_expect_tx(&hfull[s], h_bytes * GK);
                     for (int u = 0; u < GK; ++u)
                         tc::tma_load_2d(hring + (s * GK + u) * h_bytes, &p.hmap, &hfull[s], (kb + u) * kLmKB, chunk * p.NP);
                     issued = g + 1;
+                    if (++s == HS) { s = 0; fill ^= 1u; }
                 }
             }
             if (*abort_flag)
@@ -452,7 +454,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
         // ------------------------------------------------------------ MMA issuer: A from TMEM, hidden from smem
         if (lane == 0) {
             const uint32_t idesc = tc::idesc_f16(false, false, false, kLmM, p.NP);
-            const uint32_t hbase = tc::smem_u32(hring);
+            const uint64_t hdesc0 = tc::sdesc_sw128(tc::smem_u32(hring), 16, 1024);
             int it = 0, as = 0, hs = 0;
             uint32_t aph = 0, hph = 0;  // phase parities of the A-slot and hidden rings
             bool ok = true;
@@ -467,10 +469,10 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                     tc::tc_fence_after();
                     for (int u = 0; u < GK; ++u) {
                         const uint32_t a = tmem + a_col + (uint32_t)(as * GK + u) * 32;
-                        const uint32_t b = hbase + (uint32_t)(hs * GK + u) * h_bytes;
+                        const uint64_t b = tc::sdesc_add(hdesc0, (uint32_t)(hs * GK + u) * h_bytes);
 #pragma unroll
                         for (int kk = 0; kk < kLmKB / 16; ++kk)
-                            tc::mma_f16_ts(tmem + buf * p.DC, a + kk * 8, tc::sdesc_sw128(b + kk * 32, 16, 1024), idesc,
+                            tc::mma_f16_ts(tmem + buf * p.DC, a + kk * 8, tc::sdesc_add(b, kk * 32), idesc,
                                            (kb + u > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc::mma_commit(&aempty[as]);
@@ -485,41 +487,50 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
         }
     } else if (warp >= 6) {
         // ------------------------------------------------------------ converters: codes -> fp16 A slots in TMEM
-        // Set `par` converts the k-blocks g with g % kQ4Sets == par; its four warps cover the four lane quarters.
+        // Set `par` converts the k-blocks g with g % kQ4Sets == par (k-blocks par and par + 4 of every W stage);
+        // its four warps cover the four lane quarters.  k-block g goes to A-slot group g / GK, slot g % GK of it;
+        // a set's consecutive k-blocks are kQ4Sets / GK groups apart, and NA is a multiple of that step, so a
+        // set's group index advances by the step and wraps at NA, flipping the parity of its slots' reuse.
         const int par = (warp - 6) >> 2, quad = warp & 3;
         const int r = quad * 32 + lane;  // vocabulary row within the tile = TMEM lane
-        const uint32_t lane_base = (uint32_t)(quad * 32) << 16;
+        const uint32_t a_lane = tmem + ((uint32_t)(quad * 32) << 16) + a_col + (uint32_t)(par % GK) * 32;
         const __half2 k1024 = __floats2half2_rn(1024.f, 1024.f);
-        int c = 0, g = 0;
+        const int step = kQ4Sets / GK;
+        int as = par / GK, n = 0, ws = 0;  // A-slot group, k-blocks converted, W stage
+        uint32_t use = 0, wph = 0;         // parity of the group's current use; of stage ws's fill
         bool ok = true;
         for (int vt = group; ok && vt < p.vtiles; vt += groups) {
-            for (int i = 0; ok && i < NSt; ++i, ++c) {
-                const int s = c % kQ4WStages;
-                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&wfull[s], (c / kQ4WStages) & 1, abort_flag, 256))) {
+            for (int i = 0; ok && i < NSt; ++i) {
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&wfull[ws], wph, abort_flag, 256))) {
                     ok = false;
                     break;
                 }
-                const uint8_t* st = wring + s * kQ4WStage;
-                const uint4 sc8 = *reinterpret_cast<const uint4*>(st + 32768 + r * 16);
-                const uint4 bi8 = *reinterpret_cast<const uint4*>(st + 34816 + r * 16);
-                for (int kk = 0; kk < kQ4KBPerStage; ++kk, ++g) {
-                    if ((g % kQ4Sets) != par) continue;
-                    // A-slot group of k-block g; a set converts at most one k-block of any group (GK <= kQ4Sets)
-                    const int gg = g / GK, as = gg % NA, gi = g % GK;
-                    if (gg >= NA &&
-                        !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&aempty[as], ((gg / NA) - 1) & 1, abort_flag, 256))) {
+                const uint8_t* st = wring + ws * kQ4WStage;
+                const uint16_t* scr = reinterpret_cast<const uint16_t*>(st + 32768 + r * 16);
+                const uint16_t* bir = reinterpret_cast<const uint16_t*>(st + 34816 + r * 16);
+#pragma unroll
+                for (int h = 0; h < kQ4KBPerStage / kQ4Sets; ++h) {
+                    const int kk = par + kQ4Sets * h;
+                    // the group's previous use (n * step >= NA) must have been read by its MMAs
+                    if (n * step >= NA &&
+                        !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&aempty[as], use ^ 1u, abort_flag, 256))) {
                         ok = false;
                         break;
                     }
                     tc::tc_fence_after();
-                    q4_convert_kblock(st, r, kk, sc8, bi8, k1024, tmem + lane_base + a_col + (uint32_t)(as * GK + gi) * 32);
+                    q4_convert_row(st, r, kk, __uint_as_float((uint32_t)scr[kk] << 16),
+                                   __uint_as_float((uint32_t)bir[kk] << 16), k1024, a_lane + (uint32_t)(as * GK) * 32);
                     tc::tmem_wait_st();
                     tc::tc_fence_before();
                     __syncwarp();
-                    if (lane == 0) tc::mbar_arrive(&afull[as]);
+                    tc::mbar_arrive_one(&afull[as]);
+                    ++n;
+                    as += step;
+                    if (as >= NA) { as -= NA; use ^= 1u; }
                 }
                 __syncwarp();
-                if (lane == 0) tc::mbar_arrive(&wempty[s]);
+                tc::mbar_arrive_one(&wempty[ws]);
+                if (++ws == kQ4WStages) { ws = 0; wph ^= 1u; }
             }
         }
     } else {
@@ -534,7 +545,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                              p.logits, chunk * p.NP);
             tc::tc_fence_before();
             __syncwarp();
-            if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
+            tc::mbar_arrive_one(&acc_empty[buf]);
         }
     }
 
