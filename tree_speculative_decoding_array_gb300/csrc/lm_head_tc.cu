@@ -86,7 +86,6 @@ __device__ __forceinline__ void lm_drain_wait(uint64_t* bar, uint32_t parity) {
 
 // ------------------------------------------------------------------ 16-bit heads
 constexpr int kLmMaxStages = 16;
-constexpr int kLmMaxHStages = 8;
 constexpr int kLmHStages256 = 4;  // hidden stages at 256 rows (32 KB each)
 constexpr uint32_t kLmProdSleep = 256;  // producers' longest sleep between polls (ns)
 constexpr int kLmThreads16 = kLmEpi + 96;
@@ -112,10 +111,13 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
     uint8_t* tail = sm + kLmUsable;
     unsigned long long* s_best = reinterpret_cast<unsigned long long*>(tail);  // [256]
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail + 2048);
-    uint64_t* full = bars;            // [16] W block landed
-    uint64_t* empty = bars + 16;      // [16] MMAs done with it
-    uint64_t* hfull = bars + 32;      // [8] hidden block landed
-    uint64_t* hempty = bars + 40;     // [8]
+    // One barrier pair per k-block serves both rings: full[g % S] completes when both producers have armed it
+    // for k-block g (two arrivals, each with its own byte count) and its W and hidden blocks have landed,
+    // empty[g % S] when its MMAs are done.  The hidden producer refills slot g % HS after the MMAs of k-block
+    // g - HS (HS <= S, so it arms full[g % S] only after the phase of k-block g - S has completed).  The MMA
+    // thread waits once and commits once per k-block.
+    uint64_t* full = bars;            // [16] W and hidden blocks landed
+    uint64_t* empty = bars + 16;      // [16] MMAs done with both
     uint64_t* acc_full = bars + 48;   // [2]
     uint64_t* acc_empty = bars + 50;  // [2]
     uint64_t* drain = bars + 52;
@@ -132,12 +134,8 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
-            tc::mbar_init(&full[s], 1);
+            tc::mbar_init(&full[s], 2);
             tc::mbar_init(&empty[s], 1);
-        }
-        for (int s = 0; s < HS; ++s) {
-            tc::mbar_init(&hfull[s], 1);
-            tc::mbar_init(&hempty[s], 1);
         }
         for (int s = 0; s < 2; ++s) {
             tc::mbar_init(&acc_full[s], 1);
@@ -157,32 +155,48 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
     const uint32_t tmem = *tmem_slot;
     const uint32_t b_bytes = (uint32_t)p.NP * 128;
 
-    if (warp == 4 || warp == 6) {
-        // ------------------------------------------------------------ TMA producers: warp 4 W blocks, warp 6 hidden
-        // (a warp each: a lane that sleeps in its wait would hold up the other producer)
+    if (warp == 4) {
+        // ------------------------------------------------------------ W producer
         if (lane == 0) {
-            const bool isW = warp == 4;
-            const CUtensorMap* m = isW ? &p.wmap : &p.hmap;
-            const int R = isW ? S : HS;
-            uint64_t* fullb = isW ? full : hfull;
-            uint64_t* emptyb = isW ? empty : hempty;
-            uint8_t* base = isW ? ring : hring;
-            const uint32_t bytes = isW ? 16384u : b_bytes;
-            tc::tma_prefetch_desc(m);
+            tc::tma_prefetch_desc(&p.wmap);
             int g = 0, issued = 0, st = 0;
-            uint32_t fill = 0;  // parity of stage st's current fill
+            uint32_t fill = 0;  // parity of stage st's current use
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups) {
                 for (int kb = 0; kb < KB; ++kb, ++g) {
-                    if (g >= R && !tc::mbar_wait(&emptyb[st], fill ^ 1u, abort_flag, kLmProdSleep)) { ok = false; break; }
-                    tc::mbar_expect_tx(&fullb[st], bytes);
-                    tc::tma_load_2d(base + st * bytes, m, &fullb[st], kb * kLmKB, isW ? vt * kLmM : chunk * p.NP);
+                    if (g >= S && !tc::mbar_wait(&empty[st], fill ^ 1u, abort_flag, kLmProdSleep)) { ok = false; break; }
+                    tc::mbar_expect_tx(&full[st], 16384u);
+                    tc::tma_load_2d(ring + st * 16384, &p.wmap, &full[st], kb * kLmKB, vt * kLmM);
                     issued = g + 1;
-                    if (++st == R) { st = 0; fill ^= 1u; }
+                    if (++st == S) { st = 0; fill ^= 1u; }
                 }
             }
             if (*abort_flag)
-                for (int q = max(0, issued - R); q < issued; ++q) lm_drain_wait(&fullb[q % R], (q / R) & 1);
+                for (int q = max(0, issued - S); q < issued; ++q) lm_drain_wait(&full[q % S], (q / S) & 1);
+        }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ hidden producer (a warp of its own: a lane
+        // that sleeps in its wait would hold up the W producer)
+        if (lane == 0) {
+            tc::tma_prefetch_desc(&p.hmap);
+            int g = 0, hs = 0, fs = 0, es = 0;  // k-block, hidden slot, its full[] index, empty[] index of g - HS
+            uint32_t eph = 0;                    // parity of that empty[] phase
+            bool ok = true;
+            for (int vt = group; ok && vt < p.vtiles; vt += groups) {
+                for (int kb = 0; kb < KB; ++kb, ++g) {
+                    if (g >= HS) {
+                        if (!tc::mbar_wait(&empty[es], eph, abort_flag, kLmProdSleep)) { ok = false; break; }
+                        if (++es == S) { es = 0; eph ^= 1u; }
+                    }
+                    tc::mbar_expect_tx(&full[fs], b_bytes);
+                    tc::tma_load_2d(hring + hs * b_bytes, &p.hmap, &full[fs], kb * kLmKB, chunk * p.NP);
+                    if (++hs == HS) hs = 0;
+                    if (++fs == S) fs = 0;
+                }
+            }
+            // at most HS copies are in flight: let them land (bounded waits) before the CTA goes away
+            if (*abort_flag)
+                for (int q = max(0, g - HS); q < g; ++q) lm_drain_wait(&full[q % S], (q / S) & 1);
         }
     } else if (warp == 5) {
         // ------------------------------------------------------------ MMA issuer
@@ -191,17 +205,14 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
             const uint64_t dW0 = tc::sdesc_sw128(tc::smem_u32(ring), 16, 1024);
             const uint64_t dH0 = tc::sdesc_sw128(tc::smem_u32(hring), 16, 1024);
             int it = 0, st = 0, hs = 0;
-            uint32_t ph = 0, hph = 0;  // phase parities of the two rings
+            uint32_t ph = 0;  // phase parity of the W ring
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups, ++it) {
                 const int buf = it & 1;
                 if (it >= 2 && !tc::mbar_wait_spin(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
                 tc::tc_fence_after();
                 for (int kb = 0; kb < KB; ++kb) {
-                    if (!tc::mbar_wait_spin(&full[st], ph, abort_flag) || !tc::mbar_wait_spin(&hfull[hs], hph, abort_flag)) {
-                        ok = false;
-                        break;
-                    }
+                    if (!tc::mbar_wait_spin(&full[st], ph, abort_flag)) { ok = false; break; }
                     tc::tc_fence_after();
                     const uint64_t da = tc::sdesc_add(dW0, (uint32_t)st * 16384u);
                     const uint64_t db = tc::sdesc_add(dH0, (uint32_t)hs * b_bytes);
@@ -210,9 +221,8 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
                         tc::mma_f16(tmem + buf * 256, tc::sdesc_add(da, kk * 32), tc::sdesc_add(db, kk * 32), idesc,
                                     (kb > 0 || kk > 0) ? 1u : 0u);
                     tc::mma_commit(&empty[st]);
-                    tc::mma_commit(&hempty[hs]);
                     if (++st == S) { st = 0; ph ^= 1u; }
-                    if (++hs == HS) { hs = 0; hph ^= 1u; }
+                    if (++hs == HS) hs = 0;
                 }
                 if (ok) tc::mma_commit(&acc_full[buf]);
             }
@@ -1029,7 +1039,8 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
     prm.hstages = NP >= 256 ? kLmHStages256 : NP >= 128 ? 5 : 4;
     const int stages = (kLmUsable - prm.hstages * NP * 128) / 16384;
     prm.stages = stages > kLmMaxStages ? kLmMaxStages : stages;
-    if (prm.stages < 2) return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the pipeline");
+    if (prm.stages < 2 || prm.stages < prm.hstages)  // the two rings share one barrier pair per W stage
+        return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the pipeline");
     const int sms = sm_count();
     const int groups = sms / nchunks > 0 ? sms / nchunks : 1;
     if (logits) {
