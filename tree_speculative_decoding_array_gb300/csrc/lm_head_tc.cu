@@ -281,12 +281,19 @@ struct LmQ4Params {
 };
 
 // One 32-bit word of codes (features 8j..8j+7, feature 8j+i in bits 4i..4i+3) -> four fp16 pairs
-// (8j+m, 8j+m+4), m = 0..3, each w = scale * q + bias with a single rounding.
+// (8j+m, 8j+m+4), m = 0..3, each w = scale * q + bias with a single rounding.  A code in the low nibble of its
+// byte becomes the fp16 1024 + q under the mask (1024 + q - 1024 = q exactly); one in the high nibble becomes
+// 1024 + 16 q without a shift, and (1024 + 16 q) / 16 - 64 = q exactly in one fma; one shift of the word by 8
+// serves codes m = 2, 3.
 __device__ __forceinline__ void q4_word(uint32_t x, __half2 s2, __half2 b2, __half2 k1024, uint32_t* out) {
+    const __half2 k16th = __floats2half2_rn(0.0625f, 0.0625f), km64 = __floats2half2_rn(-64.f, -64.f);
+    const uint32_t x8 = x >> 8;
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
-        uint32_t h = ((x >> (4 * m)) & 0x000F000Fu) | 0x64006400u;  // (1024 + q_m, 1024 + q_{m+4}), exact
-        const __half2 q = __hsub2(*reinterpret_cast<__half2*>(&h), k1024);
+        const uint32_t src = m < 2 ? x : x8;
+        uint32_t h = (src & ((m & 1) ? 0x00F000F0u : 0x000F000Fu)) | 0x64006400u;
+        const __half2 hv = *reinterpret_cast<__half2*>(&h);
+        const __half2 q = (m & 1) ? __hfma2(hv, k16th, km64) : __hsub2(hv, k1024);  // (q_m, q_{m+4}), exact
         const __half2 w = __hfma2(q, s2, b2);
         out[m] = *reinterpret_cast<const uint32_t*>(&w);
     }
