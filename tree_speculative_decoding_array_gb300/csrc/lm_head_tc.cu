@@ -753,42 +753,47 @@ __global__ void __launch_bounds__(Q4s<NI>::kThreads, 1) lm_q4s_kernel(const __gr
         }
     } else if (warp >= 6 && warp < Q4s<NI>::kConv0) {
         // ------------------------------------------------------------ issuer iss: k-blocks of sets iss, iss + NI, ...
+        // The whole warp runs the loop (warp-uniform operands); lane 0 issues the MMAs and commits.
         const int iss = warp - 6;
-        if (lane == 0) {
-            const uint32_t idesc = tc::idesc_f16(false, false, false, kLmM, p.NP);
-            const uint64_t hdesc0 = tc::sdesc_sw128(tc::smem_u32(hring), 16, 1024);
-            int it = 0, hs = 0, slot = 0;  // hidden stage; A slot (the same in every set: one k-block per stage each)
-            uint32_t hph = 0, aph = 0;
-            bool ok = true;
-            for (int vt = group; ok && vt < p.vtiles; vt += groups, ++it) {
-                const int buf = it & 1;
-                if (it >= 2 && !tc::mbar_wait_spin(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag)) { ok = false; break; }
-                tc::tc_fence_after();
-                const uint32_t d = tmem + (uint32_t)((buf * NI + iss) * DC);
-                for (int kb0 = 0; ok && kb0 < KB; kb0 += kQ4sKBPerHStage) {
-                    if (!tc::mbar_wait(&hfull[hs], hph, abort_flag, 64, kQ4sIssSpins)) { ok = false; break; }
-                    for (int u = iss; u < kQ4sKBPerHStage; u += NI) {  // set u converts k-block kb0 + u
-                        const int sl = u * NAS + slot;
-                        if (!tc::mbar_wait(&afull[sl], aph, abort_flag, 64, kQ4sIssSpins)) { ok = false; break; }
-                        tc::tc_fence_after();
-                        const uint32_t a = tmem + a_col + (uint32_t)sl * 32;
-                        const uint64_t b = tc::sdesc_add(hdesc0, (uint32_t)(hs * kQ4sKBPerHStage + u) * h_bytes);
-                        const uint32_t first = (kb0 == 0 && u == iss) ? 0u : 1u;
-                        tc::mma_f16_ts(d, a, b, idesc, first);
-                        tc::mma_f16_ts(d, a + 8, tc::sdesc_add(b, 32), idesc, 1u);
-                        tc::mma_f16_ts(d, a + 16, tc::sdesc_add(b, 64), idesc, 1u);
-                        tc::mma_f16_ts(d, a + 24, tc::sdesc_add(b, 96), idesc, 1u);
-                        tc::mma_commit(&aempty[sl]);
-                        tc::mma_commit(&hempty[hs]);
-                    }
-                    if (++slot == NAS) { slot = 0; aph ^= 1u; }
-                    if (++hs == HS) { hs = 0; hph ^= 1u; }
-                }
-                if (ok) tc::mma_commit(&acc_full[buf]);
+        const uint32_t idesc = tc::idesc_f16(false, false, false, kLmM, p.NP);
+        const uint64_t hdesc0 = tc::sdesc_sw128(tc::smem_u32(hring), 16, 1024);
+        int it = 0, hs = 0, slot = 0;  // hidden stage; A slot (the same in every set: one k-block per stage each)
+        uint32_t hph = 0, aph = 0;
+        bool ok = true;
+        for (int vt = group; ok && vt < p.vtiles; vt += groups, ++it) {
+            const int buf = it & 1;
+            if (it >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait_spin(&acc_empty[buf], ((it >> 1) - 1) & 1, abort_flag))) {
+                ok = false;
+                break;
             }
-            tc::mma_commit(&drain[iss]);
-            lm_drain_wait(&drain[iss], 0);
+            tc::tc_fence_after();
+            const uint32_t d = tmem + (uint32_t)((buf * NI + iss) * DC);
+            for (int kb0 = 0; ok && kb0 < KB; kb0 += kQ4sKBPerHStage) {
+                if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&hfull[hs], hph, abort_flag, 64, kQ4sIssSpins))) { ok = false; break; }
+                for (int u = iss; u < kQ4sKBPerHStage; u += NI) {  // set u converts k-block kb0 + u
+                    const int sl = u * NAS + slot;
+                    if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&afull[sl], aph, abort_flag, 64, kQ4sIssSpins))) {
+                        ok = false;
+                        break;
+                    }
+                    tc::tc_fence_after();
+                    const uint32_t a = tmem + a_col + (uint32_t)sl * 32;
+                    const uint64_t b = tc::sdesc_add(hdesc0, (uint32_t)(hs * kQ4sKBPerHStage + u) * h_bytes);
+                    const uint32_t first = (kb0 == 0 && u == iss) ? 0u : 1u;
+                    tc::mma_f16_ts_lane0(d, a, b, idesc, first);
+                    tc::mma_f16_ts_lane0(d, a + 8, tc::sdesc_add(b, 32), idesc, 1u);
+                    tc::mma_f16_ts_lane0(d, a + 16, tc::sdesc_add(b, 64), idesc, 1u);
+                    tc::mma_f16_ts_lane0(d, a + 24, tc::sdesc_add(b, 96), idesc, 1u);
+                    tc::mma_commit_lane0(&aempty[sl]);
+                    tc::mma_commit_lane0(&hempty[hs]);
+                }
+                if (++slot == NAS) { slot = 0; aph ^= 1u; }
+                if (++hs == HS) { hs = 0; hph ^= 1u; }
+            }
+            if (ok) tc::mma_commit_lane0(&acc_full[buf]);
         }
+        tc::mma_commit_lane0(&drain[iss]);
+        lm_drain_wait(&drain[iss], 0);
     } else if (warp >= Q4s<NI>::kConv0) {
         // ------------------------------------------------------------ converters: codes -> fp16 A slots in TMEM
         // Set par converts k-blocks par and par + 4 of every W stage into its own ring of NAS slots; every

@@ -189,6 +189,22 @@ __device__ __forceinline__ void mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uin
         "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// As mma_f16_ts and mma_commit, issued by lane 0 of a converged warp: the whole warp runs the issuing loop, so its
+// operands are warp-uniform values, and no divergent lane-0 branch is taken (the commit tracks lane 0's MMAs).
+__device__ __forceinline__ void mma_f16_ts_lane0(uint32_t d_tmem, uint32_t a_tmem, uint64_t b, uint32_t idesc,
+                                                 uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p, e;\n .reg .u32 l;\n mov.u32 l, %%laneid;\n setp.eq.u32 e, l, 0;\n"
+        " setp.ne.b32 p, %4, 0;\n @e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void mma_commit_lane0(uint64_t* bar) {
+    asm volatile(
+        "{\n .reg .pred e;\n .reg .u32 l;\n mov.u32 l, %%laneid;\n setp.eq.u32 e, l, 0;\n"
+        " @e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}" ::"r"(smem_u32(bar))
+        : "memory");
+}
 // Arrive on `bar` once all previously issued tcgen05 async operations of this thread complete.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(smem_u32(bar))
