@@ -77,6 +77,40 @@ __device__ __forceinline__ void lm_epilogue_tile(uint32_t taddr, int nrows, int 
     }
 }
 
+// The same argmax with a best per hidden row kept by each warp in its own row of wbest (no atomics, no divergent
+// branch): per 32 columns, the 32 warp maxima and ballots first (independent of each other), then lane k takes
+// column k's result and updates wbest[c0 + k] with a plain compare and store; the CTA merges its warps' rows at the
+// end.  A shared 64-bit atomic per column behind a lane-0 branch, contended by four warps, had made this epilogue
+// slower than a 256-column tile's MMAs.
+template <bool LOGITS>
+__device__ __forceinline__ void lm_epilogue_warp(uint32_t taddr, int nrows, int v, int V, unsigned long long* wbest,
+                                                 int lane, float* logits, int row0) {
+    const uint32_t v0 = (uint32_t)(v - lane);
+    for (int c0 = 0; c0 < nrows; c0 += 32) {
+        uint32_t d[32];
+        tc::tmem_ld32(taddr + c0, d);
+        tc::tmem_wait_ld();
+        uint32_t my_mx = 0u, my_who = 0u;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+            if (LOGITS && v < V && c0 + k < nrows) logits[(size_t)(row0 + c0 + k) * V + v] = __uint_as_float(d[k]);
+            const uint32_t o = v < V ? orderable(__uint_as_float(d[k])) : 0u;
+            const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, o);
+            const uint32_t who = __ballot_sync(0xFFFFFFFFu, o == mx);
+            if (k == lane) {  // a predicated move: k is a constant of the unrolled loop
+                my_mx = mx;
+                my_who = who;
+            }
+        }
+        const int c = c0 + lane;
+        if (c < nrows && my_mx != 0u) {
+            const uint32_t idx = v0 + (uint32_t)(__ffs(my_who) - 1);
+            const unsigned long long key = ((unsigned long long)my_mx << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+            if (key > wbest[c]) wbest[c] = key;
+        }
+    }
+}
+
 // Bounded wait used only while draining after an abort.
 __device__ __forceinline__ void lm_drain_wait(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = tc::globaltimer();
@@ -86,6 +120,7 @@ __device__ __forceinline__ void lm_drain_wait(uint64_t* bar, uint32_t parity) {
 
 // ------------------------------------------------------------------ 16-bit heads
 constexpr int kLmMaxStages = 16;
+constexpr int kLmUsable16 = kLmUsable - 6144;  // the 16-bit kernel's rings end here: per-warp bests [4][256] follow
 constexpr int kLmHStages256 = 4;  // hidden stages at 256 rows (32 KB each)
 constexpr uint32_t kLmProdSleep = 256;  // producers' longest sleep between polls (ns)
 constexpr int kLmThreads16 = kLmEpi + 96;
@@ -109,7 +144,8 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
     uint8_t* ring = sm;                  // [S][16 KB]
     uint8_t* hring = sm + S * 16384;     // [HS][NP * 128]
     uint8_t* tail = sm + kLmUsable;
-    unsigned long long* s_best = reinterpret_cast<unsigned long long*>(tail);  // [256]
+    // each epilogue warp's best per hidden row: [4][256], the last 2 KB in the tail's best slot
+    unsigned long long* wbest = reinterpret_cast<unsigned long long*>(sm + kLmUsable16);
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail + 2048);
     // One barrier pair per k-block serves both rings: full[g % S] completes when both producers have armed it
     // for k-block g (two arrivals, each with its own byte count) and its W and hidden blocks have landed,
@@ -145,7 +181,7 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
-    for (int c = threadIdx.x; c < 256; c += blockDim.x) s_best[c] = 0ull;
+    for (int c = threadIdx.x; c < 4 * 256; c += blockDim.x) wbest[c] = 0ull;
     if (warp == 5) {
         tc::tmem_alloc(tmem_slot, 512);
         tc::tmem_relinquish();
@@ -237,8 +273,8 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
             const int buf = it & 1;
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, 1024))) break;
             tc::tc_fence_after();
-            lm_epilogue_tile<LOGITS>(tmem + lane_base + buf * 256, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane,
-                             p.logits, chunk * p.NP);
+            lm_epilogue_warp<LOGITS>(tmem + lane_base + buf * 256, nrows, vt * kLmM + warp * 32 + lane, p.V,
+                                     wbest + warp * 256, lane, p.logits, chunk * p.NP);
             tc::tc_fence_before();
             __syncwarp();
             tc::mbar_arrive_one(&acc_empty[buf]);
@@ -247,8 +283,12 @@ __global__ void __launch_bounds__(kLmThreads16, 1) lm_tc_kernel(const __grid_con
 
     __syncthreads();
     if (!*abort_flag)
-        for (int c = threadIdx.x; c < nrows; c += blockDim.x)
-            if (s_best[c]) atomicMax(&p.best[chunk * p.NP + c], s_best[c]);
+        for (int c = threadIdx.x; c < nrows; c += blockDim.x) {
+            unsigned long long b = wbest[c];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) b = wbest[w * 256 + c] > b ? wbest[w * 256 + c] : b;
+            if (b) atomicMax(&p.best[chunk * p.NP + c], b);
+        }
     if (warp == 5) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, 512);
@@ -1049,7 +1089,7 @@ tsv_status launch_lm_tc(const void* hidden, int rows, int H, int V, int w_dtype,
     // hidden blocks (NP x 128 B, multiples of 1024: every block stays 1024-aligned) come from L2 after the first
     // tile: 3 stages at 256 rows, 4 below; the W ring takes the rest
     prm.hstages = NP >= 256 ? kLmHStages256 : NP >= 128 ? 5 : 4;
-    const int stages = (kLmUsable - prm.hstages * NP * 128) / 16384;
+    const int stages = (kLmUsable16 - prm.hstages * NP * 128) / 16384;
     prm.stages = stages > kLmMaxStages ? kLmMaxStages : stages;
     if (prm.stages < 2 || prm.stages < prm.hstages)  // the two rings share one barrier pair per W stage
         return fail(TSV_EUNSUPPORTED, "lm_head_argmax: hidden chunk too wide for the pipeline");
