@@ -50,38 +50,14 @@ __device__ __forceinline__ uint8_t* align1024(uint8_t* p) {
     return reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(p) + 1023) & ~uintptr_t(1023));
 }
 
-// Argmax of one accumulator tile over this warp's 32 vocabulary rows, for each of the nrows hidden rows
-// (TMEM columns starting at taddr).  v = this lane's vocabulary row; rows >= V never win.  With logits != NULL
-// every logit is also written to logits[row0 + column][v] (sampled verification).
-template <bool LOGITS>
-__device__ __forceinline__ void lm_epilogue_tile(uint32_t taddr, int nrows, int v, int V,
-                                                 unsigned long long* s_best, int lane, float* logits, int row0) {
-    const uint32_t v0 = (uint32_t)(v - lane);
-    for (int c0 = 0; c0 < nrows; c0 += 32) {
-        uint32_t d[32];
-        tc::tmem_ld32(taddr + c0, d);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-            if (c0 + k < nrows) {  // uniform across the warp
-                if (LOGITS && v < V) logits[(size_t)(row0 + c0 + k) * V + v] = __uint_as_float(d[k]);
-                const uint32_t o = v < V ? orderable(__uint_as_float(d[k])) : 0u;
-                const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, o);
-                const uint32_t who = __ballot_sync(0xFFFFFFFFu, o == mx);
-                if (lane == 0 && mx != 0u) {
-                    const uint32_t idx = v0 + (uint32_t)(__ffs(who) - 1);
-                    atomicMax(&s_best[c0 + k], ((unsigned long long)mx << 32) | (unsigned long long)(0xFFFFFFFFu - idx));
-                }
-            }
-        }
-    }
-}
-
-// The same argmax with a best per hidden row kept by each warp in its own row of wbest (no atomics, no divergent
-// branch): per 32 columns, the 32 warp maxima and ballots first (independent of each other), then lane k takes
-// column k's result and updates wbest[c0 + k] with a plain compare and store; the CTA merges its warps' rows at the
-// end.  A shared 64-bit atomic per column behind a lane-0 branch, contended by four warps, had made this epilogue
-// slower than a 256-column tile's MMAs.
+// Argmax of one accumulator tile over this warp's 32 vocabulary rows, for each of the nrows hidden rows (TMEM
+// columns starting at taddr).  v = this lane's vocabulary row; rows >= V never win; ties go to the lowest row.
+// With logits != NULL every logit is also written to logits[row0 + column][v] (sampled verification).  Each warp
+// keeps a best per hidden row in its own row of wbest (no atomics, no divergent branch): per 32 columns the 32
+// warp maxima and ballots first (independent of each other), then lane k takes column k's result and updates
+// wbest[c0 + k] with a plain compare and store; the CTA merges its warps' rows at the end.  A shared 64-bit atomic
+// per column behind a lane-0 branch, four warps contending, had made this epilogue slower than a 256-column
+// tile's MMAs.
 template <bool LOGITS>
 __device__ __forceinline__ void lm_epilogue_warp(uint32_t taddr, int nrows, int v, int V, unsigned long long* wbest,
                                                  int lane, float* logits, int row0) {
@@ -104,6 +80,44 @@ __device__ __forceinline__ void lm_epilogue_warp(uint32_t taddr, int nrows, int 
         }
         const int c = c0 + lane;
         if (c < nrows && my_mx != 0u) {
+            const uint32_t idx = v0 + (uint32_t)(__ffs(my_who) - 1);
+            const unsigned long long key = ((unsigned long long)my_mx << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
+            if (key > wbest[c]) wbest[c] = key;
+        }
+    }
+}
+
+// lm_epilogue_warp over the sum (fp32) of NI accumulators (columns taddr + i * DC), CW columns at a time (lanes
+// 0 .. CW - 1 take the columns; CW = 8 or 16, which the 4-bit few-row kernel's register budget allows).
+template <bool LOGITS, int NI, int CW>
+__device__ __forceinline__ void lm_epilogue_sum_warp(uint32_t taddr, int DC, int nrows, int v, int V,
+                                                     unsigned long long* wbest, int lane, float* logits, int row0) {
+    const uint32_t v0 = (uint32_t)(v - lane);
+    for (int c0 = 0; c0 < nrows; c0 += CW) {
+        float acc[CW];
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            uint32_t d[CW];
+            if constexpr (CW == 8) tc::tmem_ld8(taddr + (uint32_t)(i * DC) + c0, d);
+            else tc::tmem_ld16(taddr + (uint32_t)(i * DC) + c0, d);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int k = 0; k < CW; ++k) acc[k] = i == 0 ? __uint_as_float(d[k]) : acc[k] + __uint_as_float(d[k]);
+        }
+        uint32_t my_mx = 0u, my_who = 0u;
+#pragma unroll
+        for (int k = 0; k < CW; ++k) {
+            if (LOGITS && v < V && c0 + k < nrows) logits[(size_t)(row0 + c0 + k) * V + v] = acc[k];
+            const uint32_t o = v < V ? orderable(acc[k]) : 0u;
+            const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, o);
+            const uint32_t who = __ballot_sync(0xFFFFFFFFu, o == mx);
+            if (k == lane) {
+                my_mx = mx;
+                my_who = who;
+            }
+        }
+        const int c = c0 + lane;
+        if (lane < CW && c < nrows && my_mx != 0u) {
             const uint32_t idx = v0 + (uint32_t)(__ffs(my_who) - 1);
             const unsigned long long key = ((unsigned long long)my_mx << 32) | (unsigned long long)(0xFFFFFFFFu - idx);
             if (key > wbest[c]) wbest[c] = key;
@@ -401,7 +415,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
     uint8_t* wring = sm;
     uint8_t* hring = sm + kQ4HOff;
     uint8_t* tail = sm + kLmUsable;
-    unsigned long long* s_best = reinterpret_cast<unsigned long long*>(tail);  // [256]
+    // each epilogue warp's best per hidden row: [4][128], ending in the tail's best slot
+    unsigned long long* wbest = reinterpret_cast<unsigned long long*>(tail - 2048);
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail + 2048);
     uint64_t* wfull = bars;           // [3] codes, scales and biases of a stage landed
     uint64_t* wempty = bars + 3;      // [3] every converter warp is done with the stage
@@ -446,7 +461,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
-    for (int c = threadIdx.x; c < 256; c += blockDim.x) s_best[c] = 0ull;
+    for (int c = threadIdx.x; c < 4 * kQ4MaxNP; c += blockDim.x) wbest[c] = 0ull;
     if (warp == 5) {
         tc::tmem_alloc(tmem_slot, 512);
         tc::tmem_relinquish();
@@ -598,8 +613,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
             const int buf = it & 1;
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, 1024))) break;
             tc::tc_fence_after();
-            lm_epilogue_tile<LOGITS>(tmem + lane_base + buf * p.DC, nrows, vt * kLmM + warp * 32 + lane, p.V, s_best, lane,
-                             p.logits, chunk * p.NP);
+            lm_epilogue_warp<LOGITS>(tmem + lane_base + buf * p.DC, nrows, vt * kLmM + warp * 32 + lane, p.V,
+                                     wbest + warp * kQ4MaxNP, lane, p.logits, chunk * p.NP);
             tc::tc_fence_before();
             __syncwarp();
             tc::mbar_arrive_one(&acc_empty[buf]);
@@ -608,8 +623,12 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
 
     __syncthreads();
     if (!*abort_flag)
-        for (int c = threadIdx.x; c < nrows; c += blockDim.x)
-            if (s_best[c]) atomicMax(&p.best[chunk * p.NP + c], s_best[c]);
+        for (int c = threadIdx.x; c < nrows; c += blockDim.x) {
+            unsigned long long b = wbest[c];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) b = wbest[w * kQ4MaxNP + c] > b ? wbest[w * kQ4MaxNP + c] : b;
+            if (b) atomicMax(&p.best[chunk * p.NP + c], b);
+        }
     if (warp == 5) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, 512);
@@ -637,42 +656,6 @@ struct Q4s {
     static constexpr int kThreads = kLmEpi + 64 + NI * 32 + kQ4Conv;
 };
 
-// Sum of the NI accumulators (columns taddr + i * DC) of one tile, then the argmax over this warp's 32
-// vocabulary rows for each of the nrows hidden rows, as lm_epilogue_tile.
-template <bool LOGITS, int NI>
-__device__ __forceinline__ void lm_epilogue_sum(uint32_t taddr, int DC, int nrows, int v, int V,
-                                                unsigned long long* s_best, int lane, float* logits, int row0) {
-    const uint32_t v0 = (uint32_t)(v - lane);
-    for (int c0 = 0; c0 < nrows; c0 += 16) {
-        float acc[16];
-        uint32_t d[16];
-        tc::tmem_ld16(taddr + c0, d);
-        tc::tmem_wait_ld();
-#pragma unroll
-        for (int k = 0; k < 16; ++k) acc[k] = __uint_as_float(d[k]);
-#pragma unroll
-        for (int i = 1; i < NI; ++i) {
-            tc::tmem_ld16(taddr + (uint32_t)(i * DC) + c0, d);
-            tc::tmem_wait_ld();
-#pragma unroll
-            for (int k = 0; k < 16; ++k) acc[k] += __uint_as_float(d[k]);
-        }
-#pragma unroll
-        for (int k = 0; k < 16; ++k) {
-            if (c0 + k < nrows) {  // uniform across the warp
-                if (LOGITS && v < V) logits[(size_t)(row0 + c0 + k) * V + v] = acc[k];
-                const uint32_t o = v < V ? orderable(acc[k]) : 0u;
-                const uint32_t mx = __reduce_max_sync(0xFFFFFFFFu, o);
-                const uint32_t who = __ballot_sync(0xFFFFFFFFu, o == mx);
-                if (lane == 0 && mx != 0u) {
-                    const uint32_t idx = v0 + (uint32_t)(__ffs(who) - 1);
-                    atomicMax(&s_best[c0 + k], ((unsigned long long)mx << 32) | (unsigned long long)(0xFFFFFFFFu - idx));
-                }
-            }
-        }
-    }
-}
-
 // Shared memory: [W ring: WS x 36 KB] [hidden ring: HS stages of 4 k-blocks] ... [bests | barriers]; the W ring
 // takes all but kQ4sMinHStages hidden stages, since its stages carry the DRAM latency (~5 us from TMA issue to
 // landing under full load) while the hidden blocks come from L2.  TMEM: accumulators [buf][issuer] of DC
@@ -685,7 +668,7 @@ __global__ void __launch_bounds__(Q4s<NI>::kThreads, 1) lm_q4s_kernel(const __gr
     uint8_t* wring = sm;
     uint8_t* hring = sm + p.WS * kQ4WStage;
     uint8_t* tail = sm + kLmUsable;
-    unsigned long long* s_best = reinterpret_cast<unsigned long long*>(tail);  // [256]
+    unsigned long long* wbest = reinterpret_cast<unsigned long long*>(tail);  // [4 warps][kQ4sMaxNP] bests
     uint64_t* bars = reinterpret_cast<uint64_t*>(tail + 2048);
     uint64_t* wfull = bars;           // [8]
     uint64_t* wempty = bars + 8;      // [8] every converter warp is done with the stage
@@ -730,7 +713,7 @@ __global__ void __launch_bounds__(Q4s<NI>::kThreads, 1) lm_q4s_kernel(const __gr
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
-    for (int c = threadIdx.x; c < 256; c += blockDim.x) s_best[c] = 0ull;
+    for (int c = threadIdx.x; c < 4 * kQ4sMaxNP; c += blockDim.x) wbest[c] = 0ull;
     if (warp == 5) {
         tc::tmem_alloc(tmem_slot, 512);
         tc::tmem_relinquish();
@@ -889,8 +872,9 @@ __global__ void __launch_bounds__(Q4s<NI>::kThreads, 1) lm_q4s_kernel(const __gr
             const int buf = it & 1;
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&acc_full[buf], (it >> 1) & 1, abort_flag, 1024))) break;
             tc::tc_fence_after();
-            lm_epilogue_sum<LOGITS, NI>(tmem + lane_base + (uint32_t)(buf * NI * DC), DC, nrows, vt * kLmM + warp * 32 + lane,
-                                        p.V, s_best, lane, p.logits, chunk * p.NP);
+            lm_epilogue_sum_warp<LOGITS, NI, LOGITS ? 8 : 16>(tmem + lane_base + (uint32_t)(buf * NI * DC), DC, nrows,
+                                             vt * kLmM + warp * 32 + lane, p.V, wbest + warp * kQ4sMaxNP, lane, p.logits,
+                                             chunk * p.NP);
             tc::tc_fence_before();
             __syncwarp();
             if (lane == 0) tc::mbar_arrive(&acc_empty[buf]);
@@ -899,8 +883,12 @@ __global__ void __launch_bounds__(Q4s<NI>::kThreads, 1) lm_q4s_kernel(const __gr
 
     __syncthreads();
     if (!*abort_flag)
-        for (int c = threadIdx.x; c < nrows; c += blockDim.x)
-            if (s_best[c]) atomicMax(&p.best[chunk * p.NP + c], s_best[c]);
+        for (int c = threadIdx.x; c < nrows; c += blockDim.x) {
+            unsigned long long b = wbest[c];
+#pragma unroll
+            for (int w = 1; w < 4; ++w) b = wbest[w * kQ4sMaxNP + c] > b ? wbest[w * kQ4sMaxNP + c] : b;
+            if (b) atomicMax(&p.best[chunk * p.NP + c], b);
+        }
     if (warp == 5) {
         tc::tc_fence_after();
         tc::tmem_dealloc(tmem, 512);
@@ -991,7 +979,7 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
         // a slot group must always be refilled by the same converter sets (its previous use then completed
         // before they wait again): NA a multiple of kQ4Sets / GK
         NA -= NA % (kQ4Sets / GK);
-        HS = (kLmUsable - kQ4HOff) / (NP * 128 * GK);
+        HS = (kLmUsable - 2048 - kQ4HOff) / (NP * 128 * GK);  // per-warp bests take the last 2 KB
         HS = HS > kQ4MaxHStages ? kQ4MaxHStages : HS;
         if (NA >= 2 && HS >= 2) break;
     }
