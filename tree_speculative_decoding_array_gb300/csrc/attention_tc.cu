@@ -30,13 +30,12 @@
 //              written over it is done, so the softmax of tile j + 1 never
 //              waits for the P V of tile j (except to rescale O).
 // Int8 caches (Int8 codes with fp16 per-token scales) use 608 threads: warps
-// 6-9 convert K tiles (and stage each tile's scales, fetched a tile ahead),
-// warps 10-13 convert V tiles, warp 14 is the V producer, warps 15-18 the
-// softmax's second half.  TMA brings the raw
-// int8 tiles (128-byte swizzled halves) into 2-stage staging rings; the
-// converters write the codes as fp16 (exact) into 2-stage operand rings; the
-// softmax warpgroup multiplies S column c by k_scale[c] and folds v_scale[c]
-// into P.
+// 6-9 convert K tiles, warps 10-13 convert V tiles, warp 14 is the V
+// producer, warps 15-18 the softmax's second half.  TMA brings the raw int8
+// tiles (128-byte swizzled halves) into 2-stage staging rings; each converter
+// thread owns one key of every tile and writes its codes times its scale
+// (fp16, one rounding; the scale fetched a tile ahead) into 2-stage operand
+// rings, so the softmax does no scale work.
 // Warp-collective roles take every wait decision warp-uniformly (__all_sync),
 // so that tcgen05.ld / __syncwarp never see a partial warp.
 // Every mbarrier wait is bounded in time: on expiry the CTA raises a shared
@@ -204,7 +203,6 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
     uint8_t* sV = sm + (I8 ? 65536 : 98304);
     uint8_t* sRawK = sm + 131072;
     uint8_t* sRawV = sm + 163840;
-    float* sScale = reinterpret_cast<float*>(sm + 212992);  // Int8: [4 slots][64 K scales x log2(e)/16 | 64 V scales]
     float* xv = reinterpret_cast<float*>(sm + 196608);
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + 215040);
     uint64_t* kfull = bars + 0;      // [3] K tile (16-bit) / raw K tile (Int8) landed
@@ -221,7 +219,6 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
     uint64_t* kc_empty = bars + 23;  // Int8: [2] Q K^T done with the fp16 K tile
     uint64_t* vc_full = bars + 25;   // Int8: [2] fp16 V tile written
     uint64_t* vc_empty = bars + 27;  // Int8: [2] P V done with the fp16 V tile
-    uint64_t* sc_full = bars + 29;   // Int8: [4] scale slot written
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 34);
     uint64_t* xch = bars + 36;       // [4 lane quarters][2 parities] both softmax halves posted their value
@@ -286,7 +283,6 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             tc::mbar_init(&vc_full[s], 4);
             tc::mbar_init(&vc_empty[s], 1);
         }
-        for (int s = 0; s < 4; ++s) tc::mbar_init(&sc_full[s], 4);
         for (int s = 0; s < 8; ++s) tc::mbar_init(&xch[s], 2);
         tc::mbar_init(o_done, 1);
         tc::mbar_init(q_full, 4);
@@ -411,49 +407,44 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
         }
     } else if (I8 && warp >= 10 && warp < 14) {
         // ------------------------------------------------------------ Int8 V converters
+        // each thread converts key ct & 63 of every tile and multiplies its codes by that key's scale; the scale
+        // is fetched one tile ahead so that the global load's latency overlaps the previous tile's work
         const int ct = threadIdx.x - 320;
+        const uint16_t* vsrc = p.vs[layer] + ((size_t)b * p.HKV + kvh) * (size_t)p.s_cap + k_begin + (ct & 63);
+        auto vscale = [&](int jj) -> uint16_t {
+            return (jj < ntiles && k_begin + jj * kTcBK + (ct & 63) < k_end) ? vsrc[jj * kTcBK] : (uint16_t)0;
+        };
+        uint16_t sc_next = vscale(0);
         for (int j = 0; j < ntiles; ++j) {
             const int st = j % NS, cb = j & 1;
+            const __half sh = __ushort_as_half(sc_next);
+            sc_next = vscale(j + 1);
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / NS) & 1, abort_flag))) break;
             const int nk = min(kTcBK, k_end - (k_begin + j * kTcBK));
             if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vc_empty[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
-            convert_i8_tile(sRawV + st * 16384, sV + cb * kTileBytes, nk, ct);
+            convert_i8_tile_scaled(sRawV + st * 16384, sV + cb * kTileBytes, nk, ct, __halves2half2(sh, sh));
             tc::fence_proxy_async_smem();
             __syncwarp();
             tc::mbar_arrive_one(&vempty[st]);
             tc::mbar_arrive_one(&vc_full[cb]);
         }
     } else if (I8 && warp >= 6 && warp < 10) {
-        // ------------------------------------------------------------ Int8 K converters (and every tile's scales)
+        // ------------------------------------------------------------ Int8 K converters
+        // as the V converters: key ct & 63 of every tile, times its scale, fetched one tile ahead
         const int ct = threadIdx.x - 192;
-        const size_t seq_row = ((size_t)b * p.HKV + kvh) * (size_t)p.s_cap;
-        const uint16_t* ksg = p.ks[layer] + seq_row;
-        const uint16_t* vsg = p.vs[layer] + seq_row;
-        // threads 0-63 fetch the K scales of a tile, 64-127 its V scales, one tile ahead of the conversion so
-        // that the global load's latency overlaps the previous tile's work
-        const uint16_t* scale_src = (ct < 64 ? ksg : vsg) + (ct & 63);
-        auto fetch_scale = [&](int jj) -> uint16_t {
-            const int k = k_begin + jj * kTcBK + (ct & 63);
-            return (jj < ntiles && k < k_end) ? scale_src[k_begin + jj * kTcBK] : (uint16_t)0;
+        const uint16_t* ksrc = p.ks[layer] + ((size_t)b * p.HKV + kvh) * (size_t)p.s_cap + k_begin + (ct & 63);
+        auto kscale = [&](int jj) -> uint16_t {
+            return (jj < ntiles && k_begin + jj * kTcBK + (ct & 63) < k_end) ? ksrc[jj * kTcBK] : (uint16_t)0;
         };
-        uint16_t sc_next = fetch_scale(0);
+        uint16_t sc_next = kscale(0);
         for (int j = 0; j < ntiles; ++j) {
-            const int st = j % NS, cb = j & 1, slot = j & 3;
-            const uint16_t sc_bits = sc_next;
-            sc_next = fetch_scale(j + 1);
+            const int st = j % NS, cb = j & 1;
+            const __half sh = __ushort_as_half(sc_next);
+            sc_next = kscale(j + 1);
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kfull[st], (j / NS) & 1, abort_flag))) break;
-            const int key0 = k_begin + j * kTcBK;
-            const int nk = min(kTcBK, k_end - key0);
+            const int nk = min(kTcBK, k_end - (k_begin + j * kTcBK));
             if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kc_empty[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
-            {  // this tile's scales into slot j & 3.  The slot was last read by the softmax of tile j - 4: Q K^T of
-               // tile j - 2, done (waited for above), had waited for P V of tile j - 4, which needed that softmax.
-                float v = f16_bits_to_f32(sc_bits);  // keys past the range fetched 0
-                if (ct < 64) v *= 1.4426950408889634f * 0.0625f;  // K scales carry log2(e) / sqrt(256)
-                sScale[slot * 128 + ct] = v;
-                __syncwarp();
-                tc::mbar_arrive_one(&sc_full[slot]);
-            }
-            convert_i8_tile(sRawK + st * 16384, sK + cb * kTileBytes, nk, ct);
+            convert_i8_tile_scaled(sRawK + st * 16384, sK + cb * kTileBytes, nk, ct, __halves2half2(sh, sh));
             tc::fence_proxy_async_smem();
             __syncwarp();
             tc::mbar_arrive_one(&kempty[st]);
@@ -527,25 +518,23 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             uint32_t sc[32];
             tc::tmem_ld32(tmem + lane_base + kColS + sb * kTcBK + h * 32, sc);
             tc::tmem_wait_ld();
-            // Int8: this half's 32 K scales (x log2(e)/16); its V scales 64 further
-            const float* ksc = sScale + (j & 3) * 128 + h * 32;
-            if (I8 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&sc_full[j & 3], (j >> 2) & 1, abort_flag))) { ok = false; break; }
 
             const int ct = k_begin + j * kTcBK;  // first key of the tile
             const int c0 = ct + h * 32;          // first key of this half
-            // Scores in the log2 domain.  Tiles whose 64 keys are all history keys inside the range need no mask.
-            // (padding rows past the unit's G*T rows take it too: their Q is zero and their results are dropped)
+            // Raw scores (Int8: the K scales are in the fp16 copy of K); masked keys become -inf.  Tiles whose 64
+            // keys are all history keys inside the range need no mask (padding rows past the unit's G*T rows take
+            // it too: their Q is zero and their results are dropped).  The maximum is taken on the raw scores (the
+            // scale is positive) and every p is ex2(s * scale - m) in one fused multiply-add, in the log2 domain.
             float x[32];
-            if (ct + kTcBK <= k_end && ct + kTcBK <= S && ct >= lo_last) {
 #pragma unroll
-                for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(sc[c]) * (I8 ? ksc[c] : qk_scale);
-            } else {
+            for (int c = 0; c < 32; ++c) x[c] = __uint_as_float(sc[c]);
+            if (!(ct + kTcBK <= k_end && ct + kTcBK <= S && ct >= lo_last)) {
 #pragma unroll
                 for (int c = 0; c < 32; ++c) {
                     const int key = c0 + c;
                     bool v = row_ok && key < k_end && key >= lo_row;
                     if (key >= S) v = v && ((anc >> ((key - S) & 63)) & 1ull);
-                    x[c] = v ? __uint_as_float(sc[c]) * (I8 ? ksc[c] : qk_scale) : -INFINITY;
+                    if (!v) x[c] = -INFINITY;
                 }
             }
             float mx[16];
@@ -557,7 +546,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
                 for (int c = 0; c < w; ++c) mx[c] = fmaxf(mx[c], mx[c + w]);
             float mo;
             if (!exchange(j, mx[0], mo)) { ok = false; break; }
-            const float mt_ = fmaxf(mx[0], mo);  // the row's tile maximum, the same in both halves
+            const float mt_ = fmaxf(mx[0], mo) * qk_scale;  // the row's tile maximum, the same in both halves
             float alpha = 1.f;
             bool resc = false;
             if (mt_ > m_ref + 8.f) {  // also when m_ref is still -inf
@@ -571,11 +560,10 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             float sm2[16];
 #pragma unroll
             for (int c = 0; c < 32; c += 2) {
-                const float p0 = tc::ex2_approx(x[c] - msub);
-                const float p1 = tc::ex2_approx(x[c + 1] - msub);
+                const float p0 = tc::ex2_approx(fmaf(x[c], qk_scale, -msub));
+                const float p1 = tc::ex2_approx(fmaf(x[c + 1], qk_scale, -msub));
                 sm2[c >> 1] = p0 + p1;
-                if (I8) pk[c >> 1] = pack2(p0 * ksc[64 + c], p1 * ksc[65 + c], false);
-                else pk[c >> 1] = pack2(p0, p1, bf);
+                pk[c >> 1] = pack2(p0, p1, I8 ? false : bf);
             }
 #pragma unroll
             for (int w = 8; w >= 1; w >>= 1)
