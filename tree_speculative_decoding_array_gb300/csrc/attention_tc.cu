@@ -29,9 +29,12 @@
 //              MN-major).  An S buffer is reused once the P V of the P
 //              written over it is done, so the softmax of tile j + 1 never
 //              waits for the P V of tile j (except to rescale O).
-// Int8 caches (Int8 codes with fp16 per-token scales) use 608 threads: warps
+// Int8 caches (Int8 codes with fp16 per-token scales) use 640 threads: warps
 // 6-9 convert K tiles, warps 10-13 convert V tiles, warp 14 is the V
-// producer, warps 15-18 the softmax's second half.  TMA brings the raw int8
+// producer, warps 15-18 the softmax's second half; warp 5 issues only the
+// Q K^T MMAs and warp 19 the P V MMAs (one issuing thread holds the tensor
+// pipe's front end for every MMA it issues, two double the issue rate).
+// TMA brings the raw int8
 // tiles (128-byte swizzled halves) into 2-stage staging rings; each converter
 // thread owns one key of every tile and writes its codes times its scale
 // (fp16, one rounding; the scale fetched a tile ahead) into 2-stage operand
@@ -53,9 +56,9 @@ constexpr int kTcBK = 64;
 constexpr int kTcD = 256;
 constexpr int kTcThreads16 = 224;  // 128-key kernel: + warp 6: V producer
 // 64-key kernel: 16-bit: warp 6 V producer, warps 7-10 the softmax's second half; Int8: warps 6-9 K converters,
-// 10-13 V converters, warp 14 V producer, warps 15-18 the softmax's second half
+// 10-13 V converters, warp 14 V producer, warps 15-18 the softmax's second half, warp 19 issues the P V MMAs
 constexpr int kTc64Threads16 = 352;
-constexpr int kTcThreadsI8 = 608;
+constexpr int kTcThreadsI8 = 640;
 constexpr int kTcSmem = 1024 + 215040 + 512;
 constexpr uint32_t kTileBytes = kTcBK * kTcD * 2;  // one K (or V) tile: 32 KiB
 
@@ -219,6 +222,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
     uint64_t* kc_empty = bars + 23;  // Int8: [2] Q K^T done with the fp16 K tile
     uint64_t* vc_full = bars + 25;   // Int8: [2] fp16 V tile written
     uint64_t* vc_empty = bars + 27;  // Int8: [2] P V done with the fp16 V tile
+    uint64_t* drain_pv = bars + 29;  // Int8: every MMA of the P V issuer done (abort path)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 34);
     uint64_t* xch = bars + 36;       // [4 lane quarters][2 parities] both softmax halves posted their value
@@ -287,6 +291,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
         tc::mbar_init(o_done, 1);
         tc::mbar_init(q_full, 4);
         tc::mbar_init(drain, 1);
+        tc::mbar_init(drain_pv, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -329,6 +334,58 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             }
             if (*abort_flag) {  // let our own copies land before the CTA goes away
                 for (int j = max(0, issued - NS); j < issued; ++j) drain_wait(&fullb[j % NS], (j / NS) & 1);
+            }
+        }
+    } else if (I8 && (warp == 5 || warp == 19)) {
+        // ------------------------------------------------------------ Int8: two MMA issuers
+        // warp 5: S = Q K^T into S buffer j & 1 once the fp16 K tile is written and the P V of tile j - 2 (whose
+        // P sits in that buffer) is done; warp 19: O += P V once both softmax halves wrote P and the fp16 V tile
+        // is written.  O is only written by warp 19, in tile order.
+        if (lane == 0) {
+            const bool qk = warp == 5;
+            const uint32_t id_qk = tc::idesc_f16(false, false, false, kTcRows, kTcBK);
+            const uint32_t id_pv = tc::idesc_f16(false, false, true, kTcRows, kTcD);
+            const uint64_t dK0 = tc::sdesc_sw128(tc::smem_u32(sK), 16, 1024);
+            const uint64_t dV0 = tc::sdesc_sw128(tc::smem_u32(sV), 8192, 1024);
+            bool ok = !qk || tc::mbar_wait_spin(q_full, 0, abort_flag);
+            if (ok) tc::tc_fence_after();
+            for (int j = 0; ok && j < ntiles; ++j) {
+                const int b2 = j & 1;
+                if (qk) {
+                    ok = tc::mbar_wait(&kc_full[b2], (j >> 1) & 1, abort_flag, 32, 64);
+                    if (ok && j >= 2) ok = tc::mbar_wait(&sp_free[b2], ((j >> 1) - 1) & 1, abort_flag, 32, 64);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const uint64_t kdesc = tc::sdesc_add(dK0, (uint32_t)b2 * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kTcD / 16; ++kk) {
+                        const uint64_t db = tc::sdesc_add(kdesc, (kk >> 2) * 8192 + (kk & 3) * 32);
+                        tc::mma_f16_ts(tmem + kColS + b2 * kTcBK, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
+                    }
+                    tc::mma_commit(&s_full[b2]);
+                    tc::mma_commit(&kc_empty[b2]);
+                } else {
+                    ok = tc::mbar_wait(&p_full[b2], (j >> 1) & 1, abort_flag, 32, 64);
+                    if (ok) ok = tc::mbar_wait(&vc_full[b2], (j >> 1) & 1, abort_flag, 32, 64);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const uint64_t vdesc = tc::sdesc_add(dV0, (uint32_t)b2 * kTileBytes);
+#pragma unroll
+                    for (int kk = 0; kk < kTcBK / 16; ++kk) {  // A = P, 16-bit pairs over S buffer b2
+                        const uint64_t db = tc::sdesc_add(vdesc, kk * 2048);
+                        tc::mma_f16_ts(tmem + kColO, tmem + kColS + b2 * kTcBK + kk * 8, db, id_pv,
+                                       (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                    tc::mma_commit(&sp_free[b2]);
+                    tc::mma_commit(&vc_empty[b2]);
+                }
+            }
+            if (ok) {
+                if (!qk) tc::mma_commit(o_done);
+            } else {  // wait for every MMA this thread issued before TMEM is freed
+                uint64_t* dr = qk ? drain : drain_pv;
+                tc::mma_commit(dr);
+                drain_wait(dr, 0);
             }
         }
     } else if (warp == 5) {
