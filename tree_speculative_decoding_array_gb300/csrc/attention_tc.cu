@@ -223,12 +223,15 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
     uint64_t* vc_full = bars + 25;   // Int8: [2] fp16 V tile written
     uint64_t* vc_empty = bars + 27;  // Int8: [2] P V done with the fp16 V tile
     uint64_t* drain_pv = bars + 29;  // Int8: every MMA of the P V issuer done (abort path)
+    uint64_t* s_free = bars + 30;    // Int8: every softmax warp has read the S tile
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 34);
     uint64_t* xch = bars + 36;       // [4 lane quarters][2 parities] both softmax halves posted their value
-    // TMEM columns: Q [0, 128) as 16-bit pairs, S [128, 192) and [192, 256) (P, 16-bit pairs, over the first 32
-    // columns of its S tile once the softmax has read it), O [256, 512).
-    constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
+    // TMEM columns.  16-bit caches: Q [0, 128) as 16-bit pairs, S [128, 192) and [192, 256) (P, 16-bit pairs,
+    // over the first 32 columns of its S tile once the softmax has read it), O [256, 512).  Int8 caches: Q, one
+    // S tile [128, 192) (freed as soon as both softmax halves have read it, so Q K^T of the next tile never
+    // waits for a P V), P [192, 224) and [224, 256) for tiles j & 1, O [256, 512).
+    constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256, kColP8 = 192;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     int item = blockIdx.x;
@@ -292,6 +295,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
         tc::mbar_init(q_full, 4);
         tc::mbar_init(drain, 1);
         tc::mbar_init(drain_pv, 1);
+        tc::mbar_init(s_free, 8);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -338,9 +342,11 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
         }
     } else if (I8 && (warp == 5 || warp == 19)) {
         // ------------------------------------------------------------ Int8: two MMA issuers
-        // warp 5: S = Q K^T into S buffer j & 1 once the fp16 K tile is written and the P V of tile j - 2 (whose
-        // P sits in that buffer) is done; warp 19: O += P V once both softmax halves wrote P and the fp16 V tile
-        // is written.  O is only written by warp 19, in tile order.
+        // warp 5: S = Q K^T once the fp16 K tile is written and both softmax halves have read the previous S;
+        // warp 19: O += P V (A = P buffer j & 1) once both halves wrote P and the fp16 V tile is written.  O is
+        // only written by warp 19, in tile order.  Their commits free the operand slots too: s_full[j & 1]
+        // (Q K^T of tile j done) frees fp16 K slot j & 1, sp_free[j & 1] (P V of tile j done) fp16 V slot and P
+        // buffer j & 1.
         if (lane == 0) {
             const bool qk = warp == 5;
             const uint32_t id_qk = tc::idesc_f16(false, false, false, kTcRows, kTcBK);
@@ -353,17 +359,16 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
                 const int b2 = j & 1;
                 if (qk) {
                     ok = tc::mbar_wait(&kc_full[b2], (j >> 1) & 1, abort_flag, 32, 64);
-                    if (ok && j >= 2) ok = tc::mbar_wait(&sp_free[b2], ((j >> 1) - 1) & 1, abort_flag, 32, 64);
+                    if (ok && j >= 1) ok = tc::mbar_wait(s_free, (j - 1) & 1, abort_flag, 32, 64);
                     if (!ok) break;
                     tc::tc_fence_after();
                     const uint64_t kdesc = tc::sdesc_add(dK0, (uint32_t)b2 * kTileBytes);
 #pragma unroll
                     for (int kk = 0; kk < kTcD / 16; ++kk) {
                         const uint64_t db = tc::sdesc_add(kdesc, (kk >> 2) * 8192 + (kk & 3) * 32);
-                        tc::mma_f16_ts(tmem + kColS + b2 * kTcBK, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
+                        tc::mma_f16_ts(tmem + kColS, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
                     }
                     tc::mma_commit(&s_full[b2]);
-                    tc::mma_commit(&kc_empty[b2]);
                 } else {
                     ok = tc::mbar_wait(&p_full[b2], (j >> 1) & 1, abort_flag, 32, 64);
                     if (ok) ok = tc::mbar_wait(&vc_full[b2], (j >> 1) & 1, abort_flag, 32, 64);
@@ -371,13 +376,12 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
                     tc::tc_fence_after();
                     const uint64_t vdesc = tc::sdesc_add(dV0, (uint32_t)b2 * kTileBytes);
 #pragma unroll
-                    for (int kk = 0; kk < kTcBK / 16; ++kk) {  // A = P, 16-bit pairs over S buffer b2
+                    for (int kk = 0; kk < kTcBK / 16; ++kk) {  // A = P, 16-bit pairs in P buffer b2
                         const uint64_t db = tc::sdesc_add(vdesc, kk * 2048);
-                        tc::mma_f16_ts(tmem + kColO, tmem + kColS + b2 * kTcBK + kk * 8, db, id_pv,
+                        tc::mma_f16_ts(tmem + kColO, tmem + kColP8 + b2 * 32 + kk * 8, db, id_pv,
                                        (j > 0 || kk > 0) ? 1u : 0u);
                     }
                     tc::mma_commit(&sp_free[b2]);
-                    tc::mma_commit(&vc_empty[b2]);
                 }
             }
             if (ok) {
@@ -478,7 +482,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             sc_next = vscale(j + 1);
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vfull[st], (j / NS) & 1, abort_flag))) break;
             const int nk = min(kTcBK, k_end - (k_begin + j * kTcBK));
-            if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&vc_empty[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
+            // fp16 V slot cb free once P V of tile j - 2 is done
+            if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&sp_free[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
             convert_i8_tile_scaled(sRawV + st * 16384, sV + cb * kTileBytes, nk, ct, __halves2half2(sh, sh));
             tc::fence_proxy_async_smem();
             __syncwarp();
@@ -500,7 +505,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             sc_next = kscale(j + 1);
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kfull[st], (j / NS) & 1, abort_flag))) break;
             const int nk = min(kTcBK, k_end - (k_begin + j * kTcBK));
-            if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&kc_empty[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
+            // fp16 K slot cb free once Q K^T of tile j - 2 is done
+            if (j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&s_full[cb], ((j >> 1) - 1) & 1, abort_flag))) break;
             convert_i8_tile_scaled(sRawK + st * 16384, sK + cb * kTileBytes, nk, ct, __halves2half2(sh, sh));
             tc::fence_proxy_async_smem();
             __syncwarp();
@@ -513,8 +519,9 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
         // of the same rows.  The two warps owning one TMEM lane quarter exchange their row maxima (and at the
         // end their row sums) through shared memory, one mbarrier per warp pair and tile parity, so both take
         // the same lazy-rescale decisions; each rescales and reads out its 128 columns of O and writes its 16
-        // columns of P.  Half 1 writes P over S columns that half 0 reads, so only after the exchange, which
-        // half 0 enters once its scores are in registers.
+        // columns of P.  16-bit caches: half 1 writes P over S columns that half 0 reads, so only after the
+        // exchange, which half 0 enters once its scores are in registers.  Int8 caches: P goes to its own
+        // buffer, and the S tile is released right after it is read.
         const int h = warp < 4 ? 0 : 1;
         const int qd = warp & 3;
         const int r = qd * 32 + lane;  // row within the tile == TMEM lane
@@ -573,8 +580,13 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&s_full[sb], (j >> 1) & 1, abort_flag))) { ok = false; break; }
             tc::tc_fence_after();
             uint32_t sc[32];
-            tc::tmem_ld32(tmem + lane_base + kColS + sb * kTcBK + h * 32, sc);
+            tc::tmem_ld32(tmem + lane_base + kColS + (I8 ? 0 : sb * kTcBK) + h * 32, sc);
             tc::tmem_wait_ld();
+            if (I8) {  // the S tile is free for the next Q K^T
+                tc::tc_fence_before();
+                __syncwarp();
+                tc::mbar_arrive_one(s_free);
+            }
 
             const int ct = k_begin + j * kTcBK;  // first key of the tile
             const int c0 = ct + h * 32;          // first key of this half
@@ -659,8 +671,15 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
                     *reinterpret_cast<uint4*>(vb + (chunk >> 3) * 8192 + row * 128 + (chunk & 7) * 16) = make_uint4(0, 0, 0, 0);
                 }
             }
-            // this half's 32 keys of P, 16-bit pairs, over S columns [16 h, 16 h + 16) (the A operand of P V)
-            tc::tmem_st16(tmem + lane_base + kColS + sb * kTcBK + h * 16, pk);
+            // Int8: P buffer sb is free once P V of tile j - 2 is done (the phase before, P V of tile j - 4, was
+            // waited for at tile j - 2; the one after needs this P)
+            if (I8 && j >= 2 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&sp_free[sb], ((j >> 1) - 1) & 1, abort_flag))) {
+                ok = false;
+                break;
+            }
+            // this half's 32 keys of P, 16-bit pairs (the A operand of P V): 16-bit caches over S columns
+            // [16 h, 16 h + 16) of its S tile, Int8 columns [16 h, 16 h + 16) of P buffer sb
+            tc::tmem_st16(tmem + lane_base + (I8 ? kColP8 + sb * 32 : kColS + sb * kTcBK) + h * 16, pk);
             tc::tmem_wait_st();
             if (zero_v) tc::fence_proxy_async_smem();  // the zeroed V rows
             tc::tc_fence_before();
