@@ -219,9 +219,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
     uint64_t* q_full = bars + 19;
     uint64_t* drain = bars + 20;
     uint64_t* kc_full = bars + 21;   // Int8: [2] fp16 K tile written
-    uint64_t* kc_empty = bars + 23;  // Int8: [2] Q K^T done with the fp16 K tile
     uint64_t* vc_full = bars + 25;   // Int8: [2] fp16 V tile written
-    uint64_t* vc_empty = bars + 27;  // Int8: [2] P V done with the fp16 V tile
     uint64_t* drain_pv = bars + 29;  // Int8: every MMA of the P V issuer done (abort path)
     uint64_t* s_free = bars + 30;    // Int8: every softmax warp has read the S tile
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 33);
@@ -286,9 +284,7 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
             tc::mbar_init(&sp_free[s], 1);
             tc::mbar_init(&p_full[s], 8);  // both softmax halves
             tc::mbar_init(&kc_full[s], 4);
-            tc::mbar_init(&kc_empty[s], 1);
             tc::mbar_init(&vc_full[s], 4);
-            tc::mbar_init(&vc_empty[s], 1);
         }
         for (int s = 0; s < 8; ++s) tc::mbar_init(&xch[s], 2);
         tc::mbar_init(o_done, 1);
@@ -414,10 +410,10 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
                 if (pj < sj) {
                     const int st = pj % NS, cb = pj & 1;
                     bool ready = tc::mbar_test(&p_full[cb], (pj >> 1) & 1);
-                    if (ready) ready = I8 ? tc::mbar_test(&vc_full[cb], (pj >> 1) & 1) : tc::mbar_test(&vfull[st], (pj / NS) & 1);
+                    if (ready) ready = tc::mbar_test(&vfull[st], (pj / NS) & 1);
                     if (ready) {
                         tc::tc_fence_after();
-                        const uint64_t vdesc = tc::sdesc_add(dV0, (uint32_t)(I8 ? cb : st) * kTileBytes);
+                        const uint64_t vdesc = tc::sdesc_add(dV0, (uint32_t)st * kTileBytes);
 #pragma unroll
                         for (int kk = 0; kk < kTcBK / 16; ++kk) {  // A = P, 16-bit pairs over S buffer cb
                             const uint64_t db = tc::sdesc_add(vdesc, kk * 2048);
@@ -425,25 +421,25 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
                                            (pj > 0 || kk > 0) ? 1u : 0u);
                         }
                         tc::mma_commit(&sp_free[cb]);
-                        tc::mma_commit(I8 ? &vc_empty[cb] : &vempty[st]);
+                        tc::mma_commit(&vempty[st]);
                         ++pj;
                         prog = true;
                     }
                 }
                 if (sj < ntiles) {
                     const int sb = sj & 1, st = sj % NS;
-                    bool ready = I8 ? tc::mbar_test(&kc_full[sb], (sj >> 1) & 1) : tc::mbar_test(&kfull[st], (sj / NS) & 1);
+                    bool ready = tc::mbar_test(&kfull[st], (sj / NS) & 1);
                     if (ready && sj >= 2) ready = tc::mbar_test(&sp_free[sb], ((sj >> 1) - 1) & 1);
                     if (ready) {
                         tc::tc_fence_after();
-                        const uint64_t kdesc = tc::sdesc_add(dK0, (uint32_t)(I8 ? sb : st) * kTileBytes);
+                        const uint64_t kdesc = tc::sdesc_add(dK0, (uint32_t)st * kTileBytes);
 #pragma unroll
                         for (int kk = 0; kk < kTcD / 16; ++kk) {
                             const uint64_t db = tc::sdesc_add(kdesc, (kk >> 2) * 8192 + (kk & 3) * 32);
                             tc::mma_f16_ts(tmem + kColS + sb * kTcBK, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
                         }
                         tc::mma_commit(&s_full[sb]);
-                        tc::mma_commit(I8 ? &kc_empty[sb] : &kempty[st]);
+                        tc::mma_commit(&kempty[st]);
                         ++sj;
                         prog = true;
                     }
