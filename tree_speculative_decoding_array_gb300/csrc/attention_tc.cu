@@ -1120,17 +1120,18 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
 // The converters fold each token's scale into its fp16 row (code exact, then one rounding of code * scale), and
 // Q is stored pre-multiplied by log2(e) / sqrt(256), so S arrives in the log2 domain and the softmax multiplies
 // nothing but P.
-// The issuer takes whichever group of four MMAs is ready, P V first (the softmax waits for it): a quarter of
-// Q K^T or a half of P V.  Measured and rejected: alternating single MMAs of the two (barrier tests between them
-// cost 2.7x) and alternating the two groups' MMAs without tests (1.24x slower: the two shapes do not overlap).
-// 608 threads (104 registers each: a softmax thread holds its 64 scores):
+// Two issuing threads: warp 4 issues Q K^T a quarter (four MMAs) at a time as each fp16 K quarter is written,
+// warp 19 P V a half (four MMAs) at a time as each P half and fp16 V half are written; one issuing thread is held
+// for each MMA's whole pipe time, so one thread issuing both serialises them.
+// 640 threads (96 registers each: a softmax thread holds its 64 scores):
 //   warps 0-3, 7-10  softmax halves 0 and 1 (key columns 64 h .. 64 h + 63 of the tile; lane quarter = warp & 3);
 //                    half 0 also stores Q into TMEM
-//   warp 4           TMEM allocation and the MMA issuer
+//   warp 4           TMEM allocation and the Q K^T issuer
 //   warp 5, 6        TMA producers: raw K quarters, raw V halves
 //   warps 11-14      K converters (thread = key of the quarter)
 //   warps 15-18      V converters
-constexpr int kW8Threads = 608;
+//   warp 19          the P V issuer
+constexpr int kW8Threads = 640;
 
 // Keys c0 .. c0 + 63 as a bit mask (bit c = key c0 + c) of what one query row sees: keys below k_end and at or
 // above lo_row (the sliding band), history keys (< S) in full, block keys S + i where bit i of anc is set.
@@ -1186,6 +1187,7 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
     uint64_t* drain = bars + 38;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 39);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 40);
+    uint64_t* drain_pv = bars + 41;  // every MMA of the P V issuer done (abort path)
     constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1248,6 +1250,7 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
         tc::mbar_init(q_full, 4);
         tc::mbar_init(o_done, 1);
         tc::mbar_init(drain, 1);
+        tc::mbar_init(drain_pv, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -1289,9 +1292,10 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
             if (*abort_flag)
                 for (int g = max(0, issued - NS); g < issued; ++g) drain_wait(&fullb[g % NS], (g / NS) & 1);
         }
-    } else if (warp == 4) {
-        // ------------------------------------------------------------ MMA issuer
+    } else if (warp == 4 || warp == 19) {
+        // ------------------------------------------------------------ MMA issuers: warp 4 Q K^T, warp 19 P V
         if (lane == 0) {
+            const bool qk = warp == 4;
             const uint32_t id_qk = tc::idesc_f16(false, false, false, kTcRows, kWK);
             const uint32_t id_pv = tc::idesc_f16(false, false, true, kTcRows, kTcD);
             // one descriptor per operand ring; every MMA below is a constant offset from one of them
@@ -1299,64 +1303,46 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
             const uint64_t dV = tc::sdesc_sw128(tc::smem_u32(sVh), 8192, 1024);
             const uint64_t dP = tc::sdesc_sw128(tc::smem_u32(sP), 16, 1024);
             const uint32_t tS = tmem + kColS, tO = tmem + kColO;
-            bool ok = tc::mbar_wait_spin(q_full, 0, abort_flag);
+            bool ok = !qk || tc::mbar_wait_spin(q_full, 0, abort_flag);
             if (ok) tc::tc_fence_after();
-            int sj = 0, sq = 0, pq = 0;  // next Q K^T tile and quarter, next P V half
-            uint32_t idle = 0;
-            uint64_t t_idle = 0;
-            while (ok && pq < nhalves) {
-                bool prog = false;
-                if ((pq >> 1) < sj) {  // P V of half pq: P written, fp16 V half there
+            if (qk) {
+                for (int g = 0; ok && g < 4 * ntiles; ++g) {  // quarter g & 3 of tile g >> 2
+                    const int sj = g >> 2, sq = g & 3;
+                    if (sq == 0 && sj > 0) ok = tc::mbar_wait(s_free, (sj - 1) & 1, abort_flag, 32, 64);
+                    if (ok) ok = tc::mbar_wait(&kq_full[sq], sj & 1, abort_flag, 32, 64);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const uint64_t bk = tc::sdesc_add(dK, sq * 16384);
+                    const uint32_t aq = tmem + kColQ + sq * 32;  // Q columns of features 64 sq ..
+                    tc::mma_f16_ts(tS, aq, bk, id_qk, sq > 0 ? 1u : 0u);
+                    tc::mma_f16_ts(tS, aq + 8, tc::sdesc_add(bk, 32), id_qk, 1u);
+                    tc::mma_f16_ts(tS, aq + 16, tc::sdesc_add(bk, 64), id_qk, 1u);
+                    tc::mma_f16_ts(tS, aq + 24, tc::sdesc_add(bk, 96), id_qk, 1u);
+                    tc::mma_commit(&kq_empty[sq]);
+                    if (sq == 3) tc::mma_commit(s_full);
+                }
+            } else {
+                for (int pq = 0; ok && pq < nhalves; ++pq) {  // P V of half pq: P written, fp16 V half there
                     const int h = pq & 1, jt = pq >> 1;
-                    if (tc::mbar_test(&p_full[h], jt & 1) && tc::mbar_test(&vh_full[h], jt & 1)) {
-                        tc::tc_fence_after();
-                        const uint64_t a = tc::sdesc_add(dP, h * 16384), bv = tc::sdesc_add(dV, h * 32768);
-                        tc::mma_f16(tO, a, bv, id_pv, pq > 0 ? 1u : 0u);
-                        tc::mma_f16(tO, tc::sdesc_add(a, 32), tc::sdesc_add(bv, 2048), id_pv, 1u);
-                        tc::mma_f16(tO, tc::sdesc_add(a, 64), tc::sdesc_add(bv, 4096), id_pv, 1u);
-                        tc::mma_f16(tO, tc::sdesc_add(a, 96), tc::sdesc_add(bv, 6144), id_pv, 1u);
-                        tc::mma_commit(&p_free[h]);
-                        tc::mma_commit(&vh_empty[h]);
-                        ++pq;
-                        prog = true;
-                    }
-                }
-                if (sj < ntiles) {
-                    bool ready = sq > 0 || sj == 0 || tc::mbar_test(s_free, (sj - 1) & 1);
-                    if (ready) ready = tc::mbar_test(&kq_full[sq], sj & 1);
-                    if (ready) {
-                        tc::tc_fence_after();
-                        const uint64_t bk = tc::sdesc_add(dK, sq * 16384);
-                        const uint32_t aq = tmem + kColQ + sq * 32;  // Q columns of features 64 sq ..
-                        tc::mma_f16_ts(tS, aq, bk, id_qk, sq > 0 ? 1u : 0u);
-                        tc::mma_f16_ts(tS, aq + 8, tc::sdesc_add(bk, 32), id_qk, 1u);
-                        tc::mma_f16_ts(tS, aq + 16, tc::sdesc_add(bk, 64), id_qk, 1u);
-                        tc::mma_f16_ts(tS, aq + 24, tc::sdesc_add(bk, 96), id_qk, 1u);
-                        tc::mma_commit(&kq_empty[sq]);
-                        if (++sq == 4) {
-                            tc::mma_commit(s_full);
-                            sq = 0;
-                            ++sj;
-                        }
-                        prog = true;
-                    }
-                }
-                if (prog) {
-                    idle = 0;
-                } else if ((++idle & 63) == 1) {  // bounded: give up after kWaitNs without progress
-                    const uint64_t now = tc::globaltimer();
-                    if (idle == 1) t_idle = now;
-                    if (*abort_flag || now - t_idle > tc::kWaitNs) {
-                        *abort_flag = 1;
-                        ok = false;
-                    }
+                    ok = tc::mbar_wait(&p_full[h], jt & 1, abort_flag, 32, 64);
+                    if (ok) ok = tc::mbar_wait(&vh_full[h], jt & 1, abort_flag, 32, 64);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const uint64_t a = tc::sdesc_add(dP, h * 16384), bv = tc::sdesc_add(dV, h * 32768);
+                    tc::mma_f16(tO, a, bv, id_pv, pq > 0 ? 1u : 0u);
+                    tc::mma_f16(tO, tc::sdesc_add(a, 32), tc::sdesc_add(bv, 2048), id_pv, 1u);
+                    tc::mma_f16(tO, tc::sdesc_add(a, 64), tc::sdesc_add(bv, 4096), id_pv, 1u);
+                    tc::mma_f16(tO, tc::sdesc_add(a, 96), tc::sdesc_add(bv, 6144), id_pv, 1u);
+                    tc::mma_commit(&p_free[h]);
+                    tc::mma_commit(&vh_empty[h]);
                 }
             }
             if (ok) {
-                tc::mma_commit(o_done);
-            } else {
-                tc::mma_commit(drain);
-                drain_wait(drain, 0);
+                if (!qk) tc::mma_commit(o_done);
+            } else {  // wait for every MMA this thread issued before TMEM is freed
+                uint64_t* dr = qk ? drain : drain_pv;
+                tc::mma_commit(dr);
+                drain_wait(dr, 0);
             }
         }
     } else if (warp >= 11 && warp < 15) {
@@ -1398,7 +1384,7 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
             tc::mbar_arrive_one(&kq_full[q]);
             if (q == 3) sc_cur = sc_nxt;
         }
-    } else if (warp >= 15) {
+    } else if (warp >= 15 && warp < 19) {
         // ------------------------------------------------------------ V converters: 64-key halves
         const int ct = threadIdx.x - 480;
         const uint16_t* vsg = p.vs[layer] + seq_row;
