@@ -54,7 +54,7 @@ namespace tsv {
 constexpr int kTcRows = 128;
 constexpr int kTcBK = 64;
 constexpr int kTcD = 256;
-constexpr int kTcThreads16 = 224;  // 128-key kernel: + warp 6: V producer
+constexpr int kTcThreads16 = 256;  // 128-key kernel: + warp 6: V producer, warp 7: P V issuer
 // 64-key kernel: 16-bit: warp 6 V producer, warps 7-10 the softmax's second half; Int8: warps 6-9 K converters,
 // 10-13 V converters, warp 14 V producer, warps 15-18 the softmax's second half, warp 19 issues the P V MMAs
 constexpr int kTc64Threads16 = 352;
@@ -736,7 +736,8 @@ __global__ void __launch_bounds__(I8 ? kTcThreadsI8 : kTc64Threads16, 1) attn_tc
 // 64-key halves (V stages of 64 keys, P written half by half, so P V of the first half starts while the
 // second is being written).  TMEM: Q [0, 128), S [128, 256) (one buffer: the softmax frees it right after
 // reading it), O [256, 512).  Shared memory: K stages [2 x 64 KB] at 0 (layout [64-dim block][128 keys][128 B]),
-// V stages [2 x 32 KB] at 128 KB, P [2 halves x 16 KB] at 192 KB, barriers at 224 KB.
+// V stages [2 x 32 KB] at 128 KB, P [2 halves x 16 KB] at 192 KB, barriers at 224 KB.  Warp 5 issues Q K^T and
+// warp 7 P V, so a P V never waits behind the next tile's Q K^T.
 constexpr int kWK = 128;
 constexpr uint32_t kWKTile = kWK * kTcD * 2;  // 64 KiB
 constexpr int kWSmem = 1024 + 229376 + 512;
@@ -762,6 +763,7 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
     uint64_t* drain = bars + 16;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 17);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 18);
+    uint64_t* drain_pv = bars + 19;  // every MMA of the P V issuer done (abort path)
     constexpr uint32_t kColQ = 0, kColS = 128, kColO = 256;
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -815,6 +817,7 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
         tc::mbar_init(o_done, 1);
         tc::mbar_init(q_full, 4);
         tc::mbar_init(drain, 1);
+        tc::mbar_init(drain_pv, 1);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -859,9 +862,12 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
             if (*abort_flag)
                 for (int j = max(0, issued - 2); j < issued; ++j) drain_wait(&fullb[j & 1], (j >> 1) & 1);
         }
-    } else if (warp == 5) {
-        // ------------------------------------------------------------ MMA issuer (event loop, P V first)
+    } else if (warp == 5 || warp == 7) {
+        // ------------------------------------------------------------ MMA issuers: warp 5 Q K^T, warp 7 P V
+        // One issuing thread is held for each MMA's whole pipe time, so a P V whose P is ready would otherwise
+        // wait behind the 16 MMAs of the next tile's Q K^T.
         if (lane == 0) {
+            const bool qk = warp == 5;
             const bool bf = p.mma_bf16 != 0;
             const uint32_t id_qk = tc::idesc_f16(bf, false, false, kTcRows, kWK);
             const uint32_t id_pv = tc::idesc_f16(bf, false, true, kTcRows, kTcD);
@@ -869,66 +875,48 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
             const uint64_t dK0 = tc::sdesc_sw128(tc::smem_u32(sK), 16, 1024);
             const uint64_t dV0 = tc::sdesc_sw128(tc::smem_u32(sV), 8192, 1024);
             const uint64_t dP0 = tc::sdesc_sw128(tc::smem_u32(sP), 16, 1024);
-            bool ok = tc::mbar_wait_spin(q_full, 0, abort_flag);
+            bool ok = !qk || tc::mbar_wait_spin(q_full, 0, abort_flag);
             if (ok) tc::tc_fence_after();
-            int sj = 0, pq = 0;  // next Q K^T tile, next P V half
-            uint32_t idle = 0;
-            uint64_t t_idle = 0;
-            while (ok && pq < nhalves) {
-                bool prog = false;
-                if (pq < 2 * sj) {
-                    const int h = pq & 1, j = pq >> 1, st = pq & 1;
-                    bool ready = tc::mbar_test(&p_full[h], j & 1);
-                    if (ready) ready = tc::mbar_test(&vfull[st], (pq >> 1) & 1);
-                    if (ready) {
-                        tc::tc_fence_after();
-                        const uint64_t dv = tc::sdesc_add(dV0, st * kTileBytes), dp = tc::sdesc_add(dP0, h * 16384);
-#pragma unroll
-                        for (int kk = 0; kk < kTcBK / 16; ++kk) {
-                            const uint64_t da = tc::sdesc_add(dp, kk * 32);
-                            const uint64_t db = tc::sdesc_add(dv, kk * 2048);
-                            tc::mma_f16(tmem + kColO, da, db, id_pv, (pq > 0 || kk > 0) ? 1u : 0u);
-                        }
-                        tc::mma_commit(&p_free[h]);
-                        tc::mma_commit(&vempty[st]);
-                        ++pq;
-                        prog = true;
-                    }
-                }
-                if (sj < ntiles) {
+            if (qk) {
+                for (int sj = 0; ok && sj < ntiles; ++sj) {  // S = Q K^T once K is there and S was read
                     const int st = sj & 1;
-                    bool ready = tc::mbar_test(&kfull[st], (sj >> 1) & 1);
-                    if (ready && sj >= 1) ready = tc::mbar_test(s_free, (sj - 1) & 1);
-                    if (ready) {
-                        tc::tc_fence_after();
-                        const uint64_t dk = tc::sdesc_add(dK0, st * kWKTile);
+                    ok = tc::mbar_wait(&kfull[st], (sj >> 1) & 1, abort_flag, 32, 64);
+                    if (ok && sj >= 1) ok = tc::mbar_wait(s_free, (sj - 1) & 1, abort_flag, 32, 64);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const uint64_t dk = tc::sdesc_add(dK0, st * kWKTile);
 #pragma unroll
-                        for (int kk = 0; kk < kTcD / 16; ++kk) {
-                            const uint64_t db = tc::sdesc_add(dk, (kk >> 2) * 16384 + (kk & 3) * 32);
-                            tc::mma_f16_ts(tmem + kColS, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
-                        }
-                        tc::mma_commit(s_full);
-                        tc::mma_commit(&kempty[st]);
-                        ++sj;
-                        prog = true;
+                    for (int kk = 0; kk < kTcD / 16; ++kk) {
+                        const uint64_t db = tc::sdesc_add(dk, (kk >> 2) * 16384 + (kk & 3) * 32);
+                        tc::mma_f16_ts(tmem + kColS, tmem + kColQ + kk * 8, db, id_qk, kk > 0);
                     }
+                    tc::mma_commit(s_full);
+                    tc::mma_commit(&kempty[st]);
                 }
-                if (prog) {
-                    idle = 0;
-                } else if ((++idle & 63) == 1) {
-                    const uint64_t now = tc::globaltimer();
-                    if (idle == 1) t_idle = now;
-                    if (*abort_flag || now - t_idle > tc::kWaitNs) {
-                        *abort_flag = 1;
-                        ok = false;
+            } else {
+                for (int pq = 0; ok && pq < nhalves; ++pq) {  // O += P V over 64-key half pq
+                    const int h = pq & 1, j = pq >> 1, st = pq & 1;
+                    ok = tc::mbar_wait(&p_full[h], j & 1, abort_flag, 32, 64);
+                    if (ok) ok = tc::mbar_wait(&vfull[st], (pq >> 1) & 1, abort_flag, 32, 64);
+                    if (!ok) break;
+                    tc::tc_fence_after();
+                    const uint64_t dv = tc::sdesc_add(dV0, st * kTileBytes), dp = tc::sdesc_add(dP0, h * 16384);
+#pragma unroll
+                    for (int kk = 0; kk < kTcBK / 16; ++kk) {
+                        const uint64_t da = tc::sdesc_add(dp, kk * 32);
+                        const uint64_t db = tc::sdesc_add(dv, kk * 2048);
+                        tc::mma_f16(tmem + kColO, da, db, id_pv, (pq > 0 || kk > 0) ? 1u : 0u);
                     }
+                    tc::mma_commit(&p_free[h]);
+                    tc::mma_commit(&vempty[st]);
                 }
             }
             if (ok) {
-                tc::mma_commit(o_done);
-            } else {
-                tc::mma_commit(drain);
-                drain_wait(drain, 0);
+                if (!qk) tc::mma_commit(o_done);
+            } else {  // wait for every MMA this thread issued before TMEM is freed
+                uint64_t* dr = qk ? drain : drain_pv;
+                tc::mma_commit(dr);
+                drain_wait(dr, 0);
             }
         }
     } else if (warp < 4) {
