@@ -201,7 +201,7 @@ typedef struct {
     int64_t s_cap;      /* capacity of every cache buffer's sequence axis, in positions */
     int32_t max_kv_len; /* host-known upper bound of every kv_len[b] (<= s_cap); sizes the grid */
     int32_t kv_dtype;   /* TSV_F16, TSV_BF16 or TSV_I8_SCALED */
-    int32_t splits;     /* key-range splits per (layer, sequence, kv head); 0 = automatic */
+    int32_t splits;     /* key-range splits per (layer, sequence, kv head); 0 = automatic; at most 64 */
     int32_t path;       /* TSV_ATTN_AUTO, TSV_ATTN_SIMT or TSV_ATTN_TCGEN05 */
     const void* q[TSV_MAX_LAYERS];       /* per layer: bf16 [B, T, HQ, D] */
     const void* k[TSV_MAX_LAYERS];       /* per layer: [B, HKV, s_cap, D] in kv_dtype (int8 codes) */

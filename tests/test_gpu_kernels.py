@@ -238,6 +238,17 @@ def test_attention_splits_agree(gpu_lib, path):
                       path=path)
 
 
+def test_attention_refuses_too_many_splits(gpu_lib):
+    """More than 64 key-range splits per unit is refused before any launch (the merge keeps 64 weights a row)."""
+    B, T, HQ, HKV, D = 1, 2, 4, 2, 64
+    q = [torch.zeros(B, T, HQ, D, dtype=torch.bfloat16, device=DEV)]
+    k = [torch.zeros(B, HKV, 8192, D, dtype=torch.float16, device=DEV)]
+    desc = gpu_lib.attn_desc(q, k, [k[0].clone()], [q[0].clone()], i32([8000]), torch.ones(B, T, dtype=torch.int64,
+                             device=DEV), T=T, HQ=HQ, HKV=HKV, D=D, kv_dtype=0, max_kv_len=8000, splits=65)
+    with pytest.raises(gpu_lib.TsvError, match="TSV_ECAPACITY"):
+        gpu_lib.tree_verify_attention(desc, torch.empty(64 << 20, dtype=torch.uint8, device=DEV))
+
+
 def test_attention_bad_kv_len(gpu_lib):
     rng = np.random.default_rng(1)
     B, T, HQ, HKV, D = 2, 4, 4, 2, 64

@@ -328,37 +328,62 @@ __global__ void __launch_bounds__(kAttThreads) attn_simt_kernel(const __grid_con
     }
 }
 
-// Merge split partials: O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
-__global__ void attn_combine_kernel(const __grid_constant__ tsv_attn_desc d, int splits, const float* __restrict__ ws_o,
-                                    const float* __restrict__ ws_ml) {
+// Merge split partials: O = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.  One warp per query row: the lanes
+// take the splits' weights (each computed once per row, kept in shared memory), then 4 columns each per pass
+// with 16-byte loads of the partials.
+constexpr int kCombRows = 4;  // rows (warps) per block
+constexpr int kCombMaxSplits = 64;
+__global__ void __launch_bounds__(kCombRows * 32) attn_combine_kernel(const __grid_constant__ tsv_attn_desc d, int splits,
+                                                                      const float* __restrict__ ws_o,
+                                                                      const float* __restrict__ ws_ml) {
     griddep_begin();
+    __shared__ float sw[kCombRows][kCombMaxSplits];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int rows_unit = (d.HQ / d.HKV) * d.T;
     const int unit = blockIdx.y;
-    const int gr = blockIdx.x;
+    const int gr = blockIdx.x * kCombRows + warp;
     const int kvh = unit % d.HKV;
     const int b = (unit / d.HKV) % d.B;
     const int layer = unit / (d.HKV * d.B);
-    if (!kv_len_ok(d.kv_len[b], d.T, d.max_kv_len, d.s_cap)) return;
+    if (gr >= rows_unit || !kv_len_ok(d.kv_len[b], d.T, d.max_kv_len, d.s_cap)) return;  // whole warps
     const int G = d.HQ / d.HKV, D = d.D;
+    const size_t slot0 = (size_t)unit * splits * rows_unit + gr;  // split s: slot0 + s * rows_unit
     float M = -INFINITY;
-    for (int s = 0; s < splits; ++s) M = fmaxf(M, ws_ml[2 * (((size_t)unit * splits + s) * rows_unit + gr)]);
+    for (int s = lane; s < splits; s += 32) M = fmaxf(M, ws_ml[2 * (slot0 + (size_t)s * rows_unit)]);
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xFFFFFFFFu, M, o));
     float L = 0.f;
-    for (int s = 0; s < splits; ++s) {
-        const size_t slot = ((size_t)unit * splits + s) * rows_unit + gr;
-        const float m = ws_ml[2 * slot];
-        if (m != -INFINITY) L += exp2f(m - M) * ws_ml[2 * slot + 1];
+    for (int s = lane; s < splits; s += 32) {
+        const size_t sl = slot0 + (size_t)s * rows_unit;
+        const float m = ws_ml[2 * sl];
+        const float w = m != -INFINITY ? exp2f(m - M) : 0.f;
+        sw[warp][s] = w;
+        L += w * ws_ml[2 * sl + 1];
     }
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) L += __shfl_xor_sync(0xFFFFFFFFu, L, o);
+    __syncwarp();
     const float inv = L > 0.f ? 1.f / L : 0.f;
     const int i = gr / G, h = kvh * G + gr % G;
     __nv_bfloat16* O = reinterpret_cast<__nv_bfloat16*>(d.o[layer]) + ((size_t)(b * d.T + i) * d.HQ + h) * D;
-    for (int c = threadIdx.x; c < D; c += blockDim.x) {
-        float o = 0.f;
+    for (int c = lane * 4; c < D; c += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         for (int s = 0; s < splits; ++s) {
-            const size_t slot = ((size_t)unit * splits + s) * rows_unit + gr;
-            const float m = ws_ml[2 * slot];
-            if (m != -INFINITY) o += exp2f(m - M) * ws_o[slot * D + c];
+            const float w = sw[warp][s];
+            if (w != 0.f) {
+                const float4 v = *reinterpret_cast<const float4*>(ws_o + (slot0 + (size_t)s * rows_unit) * D + c);
+                acc.x += w * v.x;
+                acc.y += w * v.y;
+                acc.z += w * v.z;
+                acc.w += w * v.w;
+            }
         }
-        O[c] = __float2bfloat16_rn(o * inv);
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x * inv, acc.y * inv);
+        const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z * inv, acc.w * inv);
+        uint2 pk;
+        pk.x = *reinterpret_cast<const uint32_t*>(&lo);
+        pk.y = *reinterpret_cast<const uint32_t*>(&hi);
+        *reinterpret_cast<uint2*>(O + c) = pk;
     }
 }
 
@@ -400,6 +425,8 @@ static tsv_status check_desc(const tsv_attn_desc* d) {
         return fail(TSV_EINVAL, "tree_verify_attention: max_kv_len=%d must be in [T, s_cap=%lld]", d->max_kv_len,
                     (long long)d->s_cap);
     if (d->splits < 0) return fail(TSV_EINVAL, "tree_verify_attention: splits=%d < 0", d->splits);
+    if (d->splits > kCombMaxSplits)
+        return fail(TSV_ECAPACITY, "tree_verify_attention: splits=%d > %d", d->splits, kCombMaxSplits);
     for (int l = 0; l < d->n_layers; ++l)
         if (d->window[l] < 0) return fail(TSV_EINVAL, "tree_verify_attention: layer %d window=%d < 0", l, d->window[l]);
     if (d->path < TSV_ATTN_AUTO || d->path > TSV_ATTN_TCGEN05_128)
@@ -447,8 +474,8 @@ extern "C" tsv_status tsv_tree_verify_attention(const tsv_attn_desc* d, void* wo
     if (g.path == TSV_ATTN_TCGEN05) {
         st = launch_tc(d, g.splits, g.chunk, ws_o, ws_ml, dev_status, stream);
         if (st != TSV_OK || g.splits == 1) return st;
-        dim3 cg(g.rows_unit, g.units);
-        launch_pdl(attn_combine_kernel, cg, 128, 0, stream, *d, g.splits, ws_o, ws_ml);
+        dim3 cg((g.rows_unit + kCombRows - 1) / kCombRows, g.units);
+        launch_pdl(attn_combine_kernel, cg, kCombRows * 32, 0, stream, *d, g.splits, ws_o, ws_ml);
         return check_launch("tree_verify_attention(combine)");
     }
     switch (d->D) {
@@ -458,7 +485,7 @@ extern "C" tsv_status tsv_tree_verify_attention(const tsv_attn_desc* d, void* wo
     }
     st = check_launch("tree_verify_attention");
     if (st != TSV_OK || g.splits == 1) return st;
-    dim3 cg(g.rows_unit, g.units);
-    launch_pdl(attn_combine_kernel, cg, 128, 0, stream, *d, g.splits, ws_o, ws_ml);
+    dim3 cg((g.rows_unit + kCombRows - 1) / kCombRows, g.units);
+    launch_pdl(attn_combine_kernel, cg, kCombRows * 32, 0, stream, *d, g.splits, ws_o, ws_ml);
     return check_launch("tree_verify_attention(combine)");
 }
