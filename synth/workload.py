@@ -39,8 +39,6 @@ class Workload:
 
     def __init__(self, cfg: Config, device="cuda", round_id: int = 0, n_layers: int | None = None,
                  s_cap: int | None = None, splits: int = 0, attn_path: int = 0):
-        from tree_speculative_decoding_array_gb300 import VerifyRound
-
         self.cfg = cfg
         self.device = device
         L = n_layers or cfg.n_layers
@@ -58,6 +56,8 @@ class Workload:
             specs += [(f"{w}{l}", (B, T, cfg.HKV, cfg.D), torch.bfloat16) for l in range(L) for w in ("k_new", "v_new")]
         if cfg.sample:
             specs.append(("uniforms", (cfg.rows,), torch.float32))
+        self._specs = specs
+        self._splits, self._attn_path = splits, attn_path
         self.inputs, views = _arena(specs, device)
         q_fed = [sd.alloc_q(cfg, l, device, out=views[f"q{l}"]) for l in range(L)]
         self.q_in = self.new_kv = None
@@ -81,20 +81,45 @@ class Workload:
             from . import tensors as st
             self.uniforms = views["uniforms"]
             self.uniforms.copy_(torch.from_numpy(st.node_uniforms(cfg, round_id)))
+        self.vr = self._verify_round(self.parents, self.tokens, self.q, self.hidden, self.q_in, self.new_kv,
+                                     self.uniforms)
+        self._tail = None
+
+    def _verify_round(self, parents, tokens, q, hidden, q_in, new_kv, uniforms):
+        """A VerifyRound over these per-round inputs and this workload's caches, head and kv_len."""
+        from tree_speculative_decoding_array_gb300 import VerifyRound
+
+        cfg = self.cfg
         i8 = cfg.kv_dtype == I8
-        self.vr = VerifyRound(
+        return VerifyRound(
             T=cfg.T, HQ=cfg.HQ, HKV=cfg.HKV, D=cfg.D, V=cfg.V, kv_dtype=cfg.kv_dtype, w_dtype=cfg.w_dtype,
-            max_kv_len=self.s_cap, parents=self.parents, tokens=self.tokens, q=self.q,
-            k=[c["k"] for c in self.caches], v=[c["v"] for c in self.caches], hidden=self.hidden,
+            max_kv_len=self.s_cap, parents=parents, tokens=tokens, q=q,
+            k=[c["k"] for c in self.caches], v=[c["v"] for c in self.caches], hidden=hidden,
             W=self.head["W"], kv_len=self.kv_len,
             k_scale=[c["ks"] for c in self.caches] if i8 else None,
             v_scale=[c["vs"] for c in self.caches] if i8 else None,
-            w_scales=self.head["scales"], w_biases=self.head["biases"], splits=splits, attn_path=attn_path,
-            window=tuple(cfg.layer_window(l) for l in range(L)) if cfg.window else None,
-            q_in=self.q_in, k_new=[x["k_new"] for x in self.new_kv] if self.append else None,
-            v_new=[x["v_new"] for x in self.new_kv] if self.append else None, rot_dim=cfg.rot_dim,
-            rope_base=cfg.rope_base, sample=tuple(cfg.sample) if cfg.sample else None, uniforms=self.uniforms)
-        self._tail = None
+            w_scales=self.head["scales"], w_biases=self.head["biases"], splits=self._splits,
+            attn_path=self._attn_path,
+            window=tuple(cfg.layer_window(l) for l in range(len(self.caches))) if cfg.window else None,
+            q_in=q_in, k_new=[x["k_new"] for x in new_kv] if self.append else None,
+            v_new=[x["v_new"] for x in new_kv] if self.append else None, rot_dim=cfg.rot_dim,
+            rope_base=cfg.rope_base, sample=tuple(cfg.sample) if cfg.sample else None, uniforms=uniforms)
+
+    def twin(self):
+        """A second input buffer of the same layout as ``inputs`` and a VerifyRound over it that shares this
+        workload's caches, head and kv_len: a caller copies one round's inputs into one buffer while the round
+        over the other buffer runs.  Returns (buffer, VerifyRound)."""
+        L = len(self.caches)
+        buf, views = _arena(self._specs, self.device)
+        q_fed = [views[f"q{l}"] for l in range(L)]
+        if self.append:
+            q_in, q = q_fed, [torch.empty_like(t) for t in q_fed]
+            new_kv = [{w: views[f"{w}{l}"] for w in ("k_new", "v_new")} for l in range(L)]
+        else:
+            q_in, q, new_kv = None, q_fed, None
+        uniforms = views["uniforms"] if self.cfg.sample else None
+        vr = self._verify_round(views["parents"], views["tokens"], q, views["hidden"], q_in, new_kv, uniforms)
+        return buf, vr
 
     def set_round(self, round_id: int):
         """Load another round's tree, tokens and hidden states (same caches and head)."""
