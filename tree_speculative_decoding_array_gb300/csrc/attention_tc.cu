@@ -977,21 +977,27 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
             tc::mbar_arrive_one(s_free);
 
             const int c0 = k_begin + j * kWK;
-            if (c0 + kWK <= k_end && c0 + kWK <= S && c0 >= lo_last) {
-#pragma unroll
-                for (int c = 0; c < 128; ++c) x[c] *= qk_scale;
-            } else {
+            // Raw scores; masked keys become -inf.  The tile maximum is taken on the raw scores (the scale is
+            // positive, eight independent chains) and every p is ex2(s * scale - m) in one fused multiply-add.
+            if (!(c0 + kWK <= k_end && c0 + kWK <= S && c0 >= lo_last)) {
 #pragma unroll
                 for (int c = 0; c < 128; ++c) {
                     const int key = c0 + c;
                     bool v = row_ok && key < k_end && key >= lo_row;
                     if (key >= S) v = v && ((anc >> ((key - S) & 63)) & 1ull);
-                    x[c] = v ? x[c] * qk_scale : -INFINITY;
+                    if (!v) x[c] = -INFINITY;
                 }
             }
-            float mt_ = x[0];
+            float mx[8];
 #pragma unroll
-            for (int c = 1; c < 128; ++c) mt_ = fmaxf(mt_, x[c]);
+            for (int k = 0; k < 8; ++k) mx[k] = x[k];
+#pragma unroll
+            for (int c = 8; c < 128; ++c) mx[c & 7] = fmaxf(mx[c & 7], x[c]);
+#pragma unroll
+            for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+                for (int k = 0; k < w; ++k) mx[k] = fmaxf(mx[k], mx[k + w]);
+            const float mt_ = mx[0] * qk_scale;
             float alpha = 1.f;
             bool resc = false;
             if (mt_ > m_ref + 8.f) {
@@ -1000,25 +1006,25 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
                 resc = true;
             }
             const float msub = m_ref == -INFINITY ? 0.f : m_ref;
-            if (j >= 1) {  // P V of the previous tile (both halves) done: P reusable, O stable for the rescale
+            if (j >= 1 && __any_sync(0xFFFFFFFFu, resc)) {  // P V of the previous tile done with O: rescale it
                 if (!__all_sync(0xFFFFFFFFu, tc::mbar_wait(&p_free[1], (j - 1) & 1, abort_flag))) { ok = false; break; }
                 tc::tc_fence_after();
-                if (__any_sync(0xFFFFFFFFu, resc)) {
 #pragma unroll 1
-                    for (int ch = 0; ch < 8; ++ch) {
-                        uint32_t o[32];
-                        tc::tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
-                        tc::tmem_wait_ld();
+                for (int ch = 0; ch < 8; ++ch) {
+                    uint32_t o[32];
+                    tc::tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
+                    tc::tmem_wait_ld();
 #pragma unroll
-                        for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                        tc::tmem_st32(tmem + lane_base + kColO + ch * 32, o);
-                    }
-                    tc::tmem_wait_st();
+                    for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
+                    tc::tmem_st32(tmem + lane_base + kColO + ch * 32, o);
                 }
+                tc::tmem_wait_st();
             }
             float ps = 0.f;
 #pragma unroll
             for (int h = 0; h < 2; ++h) {
+                // P half h of the previous tile no longer read (P V of that half done)
+                if (j >= 1 && !__all_sync(0xFFFFFFFFu, tc::mbar_wait(&p_free[h], (j - 1) & 1, abort_flag))) { ok = false; break; }
                 const int ch0 = c0 + h * kTcBK;
                 if (ch0 + kTcBK > k_end) {  // zero V rows past the key range in this half's stage (not our bytes)
                     const int q = 2 * j + h, st = q & 1;
@@ -1031,15 +1037,15 @@ __global__ void __launch_bounds__(kTcThreads16, 1) attn_tcw_kernel(const __grid_
                     }
                 }
                 uint32_t pk[32];
-                float sm2 = 0.f;
+                float sm4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int c = 0; c < 64; c += 2) {
-                    const float p0 = tc::ex2_approx(x[h * 64 + c] - msub);
-                    const float p1 = tc::ex2_approx(x[h * 64 + c + 1] - msub);
-                    sm2 += p0 + p1;
+                    const float p0 = tc::ex2_approx(fmaf(x[h * 64 + c], qk_scale, -msub));
+                    const float p1 = tc::ex2_approx(fmaf(x[h * 64 + c + 1], qk_scale, -msub));
+                    sm4[(c >> 1) & 3] += p0 + p1;
                     pk[c >> 1] = pack2(p0, p1, bf);
                 }
-                ps += sm2;
+                ps += (sm4[0] + sm4[1]) + (sm4[2] + sm4[3]);
                 uint8_t* ph = sP + h * 16384;
 #pragma unroll
                 for (int ch = 0; ch < 8; ++ch)
