@@ -1504,16 +1504,17 @@ __global__ void __launch_bounds__(kW8Threads, 1) attn_tcw8_kernel(const __grid_c
                 }
                 *reinterpret_cast<uint4*>(prow + ((ch ^ (r & 7)) << 4)) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
             }
-            // O *= alpha for this half's 128 columns (the scores are dead by now); P V of this tile waits for p_full
-            if (j >= 1 && __any_sync(0xFFFFFFFFu, resc)) {
+            // O *= alpha, all 256 columns, by half 0 alone: the P V over the first 64 keys, which writes every
+            // column of O, waits only for half 0's P (both halves take the same rescale decision)
+            if (h == 0 && j >= 1 && __any_sync(0xFFFFFFFFu, resc)) {
 #pragma unroll 1
-                for (int ch = 0; ch < 4; ++ch) {
+                for (int ch = 0; ch < 8; ++ch) {
                     uint32_t o[32];
-                    tc::tmem_ld32(tmem + lane_base + kColO + h * 128 + ch * 32, o);
+                    tc::tmem_ld32(tmem + lane_base + kColO + ch * 32, o);
                     tc::tmem_wait_ld();
 #pragma unroll
                     for (int k = 0; k < 32; ++k) o[k] = __float_as_uint(__uint_as_float(o[k]) * alpha);
-                    tc::tmem_st32(tmem + lane_base + kColO + h * 128 + ch * 32, o);
+                    tc::tmem_st32(tmem + lane_base + kColO + ch * 32, o);
                 }
                 tc::tmem_wait_st();
             }
