@@ -45,7 +45,7 @@ DEFAULT_ROUND = {"chain3_27b_bf16": 2}  # the round that accepts the whole chain
 TRAFFIC = {
     ("chain3_27b_bf16", ("lm_head.cu", "common.cuh")): {"hash": "2530ef189b03e4bc", "bytes": 2543127040 + 2785024},
     ("eagle64x32_27b_i8", ("attention.cu", "attention_tc.cu", "common.cuh", "tc.cuh")):
-        {"hash": "4a306aad7683e8a7", "bytes": (1086705920 + 2978048) * 128},
+        {"hash": "af0faa37c76ef2ad", "bytes": (1086705920 + 2978048) * 128},
 }
 SRC = {"lm": ("lm_head.cu", "lm_head_tc.cu", "common.cuh", "tc.cuh"),
        "attn": ("attention.cu", "attention_tc.cu", "common.cuh", "tc.cuh")}

@@ -32,9 +32,11 @@
 // Int8 caches (Int8 codes with fp16 per-token scales) use 640 threads: warps
 // 6-9 convert K tiles, warps 10-13 convert V tiles, warp 14 is the V
 // producer, warps 15-18 the softmax's second half; warp 5 issues only the
-// Q K^T MMAs and warp 19 the P V MMAs (one issuing thread holds the tensor
-// pipe's front end for every MMA it issues, two double the issue rate).
-// TMA brings the raw int8
+// Q K^T MMAs and warp 19 the P V MMAs (an issuing thread is held for each
+// MMA's whole pipe time, so one thread issuing both would make a ready P V
+// wait behind the next Q K^T).  TMEM then holds Q, one S tile (released as
+// soon as both softmax halves have read it, so the next Q K^T never waits
+// for a P V), two P buffers of 32 columns and O.  TMA brings the raw int8
 // tiles (128-byte swizzled halves) into 2-stage staging rings; each converter
 // thread owns one key of every tile and writes its codes times its scale
 // (fp16, one rounding; the scale fetched a tile ahead) into 2-stage operand
