@@ -331,7 +331,7 @@ def run_ours(args, cfg, rank, world, local_rank, steps, warmup, e2e=True):
         assert got_len == want_len, (got_len, want_len)
     assert vr.outs["status"].cpu().tolist()[0] == 0, vr.outs["status"].cpu().tolist()
 
-    e2e_res = run_e2e(args, wl, stream, steps) if (rank == 0 and e2e) else None
+    e2e_res = run_e2e(args, wl, stream, steps, pre=build) if (rank == 0 and e2e) else None
     launches = count_launches(cfg, tsv, vr, args)
     return dict(cfg=cfg, ms=ms, per_round=per_round, per_kernel=per_kernel, clocks=clk.summary(), e2e=e2e_res,
                 launches=launches, round_id=round_id, setup_s=t_setup, stage_rounds=n_stage)
@@ -424,11 +424,12 @@ def make_build_stage(cfg, k, dev):
     return build
 
 
-def run_e2e(args, wl, stream, steps):
+def run_e2e(args, wl, stream, steps, pre=None):
     """Rounds through the public API with host buffers: every round copies its inputs from pinned host memory into
     device memory (one H2D copy) and reads its int32 results back (one D2H copy).  With graphs, two VerifyRounds
     over two input buffers alternate, and round k + 1's inputs are copied on a second stream while round k runs
-    (the copy into a buffer waits for the round that last read it)."""
+    (the copy into a buffer waits for the round that last read it).  ``pre`` (the tree-construction stage, when the
+    timed round has one) runs at the start of every round, as in the device-timed round."""
     import torch
 
     vr, cfg = wl.vr, wl.cfg
@@ -471,6 +472,8 @@ def run_e2e(args, wl, stream, steps):
                         ev_in[b].record(copy_stream)
                 stream.wait_event(ev_in[a])
                 wl.restore_tail()
+                if pre is not None:
+                    pre()
                 vrs[a].replay()
                 ev_done[a].record(stream)
                 h_res[a].copy_(vrs[a].outs["result"], non_blocking=True)
@@ -492,6 +495,8 @@ def run_e2e(args, wl, stream, steps):
         def e2e_step():
             wl.restore_tail()
             wl.inputs.copy_(h_in, non_blocking=True)
+            if pre is not None:
+                pre()
             vr.run()
             h_res.copy_(res, non_blocking=True)
 
