@@ -38,17 +38,28 @@ DEFAULT_CONFIG = "eagle64x32_27b_i8"
 EXTRA_CONFIGS = ("specinfer16_27b_i8", "eagle32x8_27b_f16")  # carried on the default line at N = 1
 DEFAULT_ROUND = {"chain3_27b_bf16": 2}  # the round that accepts the whole chain (3 tokens emitted)
 
-# ncu dram bytes (read + write) per launch of a workload's dominant kernel, with the hash of the sources it was
-# measured on (a changed kernel source makes the number stale and it is reported as null).
+# ncu dram bytes (read + write) per launch of a workload's dominant kernel, with the sources that kernel is built
+# from and their hash when it was measured (a changed source makes the number stale and it is reported as null).
 # The 64-node workload's attention was captured on 1 layer x 4 sequences (1.0867 GB read + 2.978 MB written); a
 # launch over 16 layers x 32 sequences reads and writes 128 times that (every unit streams its own keys).
 TRAFFIC = {
-    ("chain3_27b_bf16", ("lm_head.cu", "common.cuh")): {"hash": "2530ef189b03e4bc", "bytes": 2543127040 + 2785024},
-    ("eagle64x32_27b_i8", ("attention.cu", "attention_tc.cu", "common.cuh", "tc.cuh")):
-        {"hash": "af0faa37c76ef2ad", "bytes": (1086705920 + 2978048) * 128},
+    # the chain's bf16 LM head (the CUDA-core GEMV), one launch at full size
+    "chain3_27b_bf16": {"kernel": "lm", "src": ("lm_head.cu", "common.cuh"), "hash": "2530ef189b03e4bc",
+                        "bytes": 2543127040 + 2785024},
+    # the 16-node workload's 4-bit LM head (lm_q4s_kernel, 16 rows), one launch at full size
+    "specinfer16_27b_i8": {"kernel": "lm", "src": ("lm_head.cu", "lm_head_tc.cu", "common.cuh", "tc.cuh"),
+                           "hash": "0218d4bcb34f837a", "bytes": 715418368 + 3241984},
+    "eagle64x32_27b_i8": {"kernel": "attn", "src": ("attention.cu", "attention_tc.cu", "common.cuh", "tc.cuh"),
+                          "hash": "af0faa37c76ef2ad", "bytes": (1086705920 + 2978048) * 128},
 }
-SRC = {"lm": ("lm_head.cu", "lm_head_tc.cu", "common.cuh", "tc.cuh"),
-       "attn": ("attention.cu", "attention_tc.cu", "common.cuh", "tc.cuh")}
+
+
+def traffic_for(cfg_name, kernel):
+    """The recorded traffic of this workload's dominant kernel, or None when none is recorded or it is stale."""
+    tr = TRAFFIC.get(cfg_name)
+    if tr is None or tr["kernel"] != kernel or tr["hash"] != src_hash(tr["src"]):
+        return None
+    return tr["bytes"]
 
 
 def peaks():
@@ -531,11 +542,8 @@ def gpu_line_parts(cfg, r, world, steps):
     if tensor_bound(cfg):
         fl = cfg.attention_flops()
         ach = fl / (attn_ms * 1e-3) / 1e12
-        src = SRC["attn"]
-        tr = TRAFFIC.get((cfg.name, src))
         out["roofline"] = {"kernel": "tree_verify_attention", "bound": "tensor", "achieved": ach, "peak": tf_sus,
-                           "unit": "TFLOP/s", "frac": ach / tf_sus,
-                           "traffic": tr["bytes"] if tr and tr["hash"] == src_hash(src) else None,
+                           "unit": "TFLOP/s", "frac": ach / tf_sus, "traffic": traffic_for(cfg.name, "attn"),
                            "algorithmic_flops_per_launch": fl, "algorithmic_bytes_per_launch": kvb,
                            "avg_launch_ms": attn_ms, "peak_kind": f"{kind} bf16 sustained",
                            "hbm_gbs": kvb / (attn_ms * 1e-3) / 1e9,
@@ -545,10 +553,9 @@ def gpu_line_parts(cfg, r, world, steps):
         dom_bytes = cfg.lm_bytes() if dom == "lm" else kvb
         dom_ms = lm_ms if dom == "lm" else attn_ms
         ach = dom_bytes / (dom_ms * 1e-3) / 1e9
-        tr = TRAFFIC.get((cfg.name, SRC[dom]))
         out["roofline"] = {"kernel": {"lm": "lm_head_argmax", "attn": "tree_verify_attention"}[dom], "bound": "hbm",
                            "achieved": ach, "peak": hbm_peak, "unit": "GB/s", "frac": ach / hbm_peak,
-                           "traffic": tr["bytes"] if tr and tr["hash"] == src_hash(SRC[dom]) else None,
+                           "traffic": traffic_for(cfg.name, dom),
                            "algorithmic_bytes_per_launch": dom_bytes, "avg_launch_ms": dom_ms,
                            "peak_kind": kind}
     return out
