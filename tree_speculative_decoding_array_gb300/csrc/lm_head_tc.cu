@@ -315,9 +315,8 @@ constexpr int kQ4Conv = kQ4Sets * 128;                // converter warps 6 .. 6 
 constexpr int kQ4HWarp = 6 + kQ4Conv / 32;            // the hidden-block producer's warp
 constexpr int kQ4Threads = kLmEpi + 64 + kQ4Conv + 32;
 constexpr int kQ4KBPerStage = 8;                      // k-blocks of 64 features per W stage
-constexpr int kQ4WStages = 3;
+constexpr int kQ4WStages = 3;                         // lm_q4_kernel: at most 3 W stages (p.WS)
 constexpr int kQ4WStage = 2 * 16384 + 2 * 2048;       // codes [128 rows x 256 B] as two swizzled boxes, scales, biases
-constexpr int kQ4HOff = kQ4WStages * kQ4WStage;       // hidden ring after the W ring
 constexpr int kQ4MaxHStages = 16;
 constexpr int kQ4MaxAGroups = 8;
 constexpr int kQ4MaxNP = 128;
@@ -331,7 +330,7 @@ struct LmQ4Params {
     float* logits;     // NULL, or [rows][V] fp32 written by the epilogue
     int rows, H, V, NP, DC, NA, HS, nchunks, vtiles;
     int GK;            // k-blocks per A-slot group and per hidden stage (1, 2 or 4): one wait and one commit each
-    int WS;            // W stages (lm_q4s_kernel; lm_q4_kernel has kQ4WStages)
+    int WS;            // W stages
 };
 
 // One 32-bit word of codes (features 8j..8j+7, feature 8j+i in bits 4i..4i+3) -> four fp16 pairs
@@ -413,7 +412,8 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = align1024(smem_raw);
     uint8_t* wring = sm;
-    uint8_t* hring = sm + kQ4HOff;
+    const int WSt = p.WS;  // W stages: 2 or 3
+    uint8_t* hring = sm + WSt * kQ4WStage;
     uint8_t* tail = sm + kLmUsable;
     // each epilogue warp's best per hidden row: [4][128], ending in the tail's best slot
     unsigned long long* wbest = reinterpret_cast<unsigned long long*>(tail - 2048);
@@ -441,7 +441,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
     if (group >= p.vtiles || nrows <= 0) return;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kQ4WStages; ++s) {
+        for (int s = 0; s < WSt; ++s) {
             tc::mbar_init(&wfull[s], 1);
             tc::mbar_init(&wempty[s], kQ4Conv / 32);
         }
@@ -484,7 +484,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
             bool ok = true;
             for (int vt = group; ok && vt < p.vtiles; vt += groups) {
                 for (int i = 0; i < NSt; ++i, ++c) {
-                    if (c >= kQ4WStages && !tc::mbar_wait(&wempty[s], fill ^ 1u, abort_flag, 512)) {
+                    if (c >= WSt && !tc::mbar_wait(&wempty[s], fill ^ 1u, abort_flag, 512)) {
                         ok = false;
                         break;
                     }
@@ -495,12 +495,12 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                     tc::tma_load_2d(st + 32768, &p.smap, &wfull[s], i * kQ4KBPerStage, vt * kLmM);
                     tc::tma_load_2d(st + 34816, &p.bmap, &wfull[s], i * kQ4KBPerStage, vt * kLmM);
                     issued = c + 1;
-                    if (++s == kQ4WStages) { s = 0; fill ^= 1u; }
+                    if (++s == WSt) { s = 0; fill ^= 1u; }
                 }
             }
             if (*abort_flag)
-                for (int q = max(0, issued - kQ4WStages); q < issued; ++q)
-                    lm_drain_wait(&wfull[q % kQ4WStages], (q / kQ4WStages) & 1);
+                for (int q = max(0, issued - WSt); q < issued; ++q)
+                    lm_drain_wait(&wfull[q % WSt], (q / WSt) & 1);
         }
     } else if (warp == kQ4HWarp) {
         if (lane == 0) {
@@ -602,7 +602,7 @@ __global__ void __launch_bounds__(kQ4Threads, 1) lm_q4_kernel(const __grid_const
                 }
                 __syncwarp();
                 tc::mbar_arrive_one(&wempty[ws]);
-                if (++ws == kQ4WStages) { ws = 0; wph ^= 1u; }
+                if (++ws == WSt) { ws = 0; wph ^= 1u; }
             }
         }
     } else {
@@ -971,6 +971,11 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
     int NP = (rows + nchunks - 1) / nchunks;
     NP = ((NP + 15) / 16) * 16;
     const int DC = ((NP + 31) / 32) * 32;
+    // W stages: 3 when each CTA streams its W tiles from DRAM alone, 2 when several row chunks walk the same
+    // vocabulary tiles together (the later ones read them from L2): that leaves room for hidden stages of 4
+    // k-blocks, so the MMA thread issues 16 MMAs per wait (2,048 rows: 6.22 -> 5.03 ms; an issuer that waits
+    // between short bursts lets the tensor pipe drain every burst).
+    const int WS = nchunks >= 2 ? 2 : kQ4WStages;
     // k-blocks per group: the largest of 4, 2, 1 that leaves at least 2 hidden stages and 2 A-slot groups
     int GK = 4, NA = 0, HS = 0;
     for (; GK >= 1; GK >>= 1) {
@@ -979,7 +984,7 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
         // a slot group must always be refilled by the same converter sets (its previous use then completed
         // before they wait again): NA a multiple of kQ4Sets / GK
         NA -= NA % (kQ4Sets / GK);
-        HS = (kLmUsable - 2048 - kQ4HOff) / (NP * 128 * GK);  // per-warp bests take the last 2 KB
+        HS = (kLmUsable - 2048 - WS * kQ4WStage) / (NP * 128 * GK);  // per-warp bests take the last 2 KB
         HS = HS > kQ4MaxHStages ? kQ4MaxHStages : HS;
         if (NA >= 2 && HS >= 2) break;
     }
@@ -1009,6 +1014,7 @@ static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const
     prm.NA = NA;
     prm.HS = HS;
     prm.GK = GK;
+    prm.WS = WS;
     prm.nchunks = nchunks;
     prm.vtiles = (V + kLmM - 1) / kLmM;
     const int sms = sm_count();
