@@ -83,3 +83,27 @@ def test_zero_token_and_error_bound():
         s = float(np.uint16(sbits).view(np.float16))
         assert codes.min() >= -127 and codes.max() <= 127 and np.abs(codes).max() >= 126
         assert np.max(np.abs(codes * s - x)) <= 0.5 * s + np.max(np.abs(x)) * 2.0 ** -10
+
+
+def test_append_block_rotates_every_head_to_its_node_position():
+    # Each node's Q and new K rows turn by the complex rotation of position S + (edges to the root, counted here by
+    # walking the parent links); features past rot_dim and the V rows pass through unchanged.
+    rng = np.random.default_rng(11)
+    par = [-1, 0, 0, 1, 2, 2, 5, 6]
+    T, HQ, HKV, D, rd, S, base = len(par), 4, 2, 20, 12, 1000, 1e4
+    q = rng.standard_normal((T, HQ, D))
+    k = rng.standard_normal((T, HKV, D))
+    v = rng.standard_normal((T, HKV, D))
+    q_rot, k_rot, v_out = oap.append_block(q, k, v, par, S, base, rd)
+    h = rd // 2
+    for i in range(T):
+        d, j = 0, i
+        while par[j] >= 0:
+            j, d = par[j], d + 1
+        turn = np.exp(1j * (S + d) * base ** (-np.arange(h) * 2.0 / rd))
+        for x, y in ((q[i], q_rot[i]), (k[i], k_rot[i])):
+            z = (x[:, :h] + 1j * x[:, h:rd]) * turn
+            assert np.allclose(y[:, :h], z.real, rtol=0, atol=1e-12)
+            assert np.allclose(y[:, h:rd], z.imag, rtol=0, atol=1e-12)
+            assert np.array_equal(y[:, rd:], x[:, rd:])
+    assert np.array_equal(v_out, v)

@@ -27,6 +27,17 @@ def test_storage_known_values():
     assert v.tolist() == [[1.5, -63.5], [2.0, 0.0]]  # scales 0.5 and 2.0
 
 
+def test_kv_values_dispatches_each_format_to_its_decoder():
+    # Format 0 reads fp16 bit patterns, 1 bf16, 2 Int8 codes times their token's fp16 scale; anything else is refused.
+    bits = np.array([[0x3C00, 0xC000]], dtype=np.uint16)
+    assert osd.kv_values(0, bits).tolist() == [[1.0, -2.0]]
+    assert osd.kv_values(1, bits).tolist() == [[2.0 ** -7, -2.0 ** 1]]  # bf16 0x3C00 = 2^-7, 0xC000 = -2
+    codes = np.array([[4, -8]], dtype=np.int8)
+    assert osd.kv_values(2, codes, np.array([0x3400], dtype=np.uint16)).tolist() == [[1.0, -2.0]]  # scale 0.25
+    with pytest.raises(ValueError):
+        osd.kv_values(3, bits)
+
+
 def test_q4_hand_built_group():
     # byte 0x21 -> element 0 = 1 (low nibble), element 1 = 2 (high nibble)
     assert osd.unpack_q4(np.array([[0x21, 0xF0]], dtype=np.uint8)).tolist() == [[1, 2, 0, 15]]
@@ -199,6 +210,19 @@ def test_tail_form_equals_absolute_form_and_scales_move():
 
 
 # ----------------------------------------------------------------------------- sliding-window layers
+@pytest.mark.parametrize("n,offset,window", [(1, 0, 1), (4, 0, 2), (3, 10, 1), (5, 7, 4), (6, 2, 50)])
+def test_sliding_band_is_the_causal_band_of_numpy_triangles(n, offset, window):
+    # Row q sits at position offset + q and keeps the `window` positions ending at itself; a window wider than the
+    # history reduces to the plain causal mask with offset.
+    ones = np.ones((n, offset + n), dtype=bool)
+    inside = np.tril(ones, k=offset) & np.triu(ones, k=offset - window + 1)
+    band = ot.sliding_band(n, offset, window)
+    assert np.array_equal(band == 0.0, inside)
+    assert np.all(band[~inside] == ot.BLOCKED)
+    if window >= offset + n:
+        assert np.array_equal(inside, np.tril(ones, k=offset))
+
+
 @pytest.mark.parametrize("S,T,window", [(0, 3, 2), (10, 4, 3), (30, 5, 8), (40, 6, 1), (12, 3, 15)])
 def test_sliding_linear_tree_is_banded_causal_sdpa(S, T, window):
     # A linear tree on a sliding-window layer is textbook sliding-window causal attention: query at position
