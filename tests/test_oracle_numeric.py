@@ -156,6 +156,10 @@ def test_argmax_ties_go_to_lowest_index_and_streaming_agrees():
     W[7, 0] = 1.0
     a, t, g = ol.argmax_streamed(lambda r0, r1: W[r0:r1], h, W.shape[0])
     assert (a[0], t[0], g[0]) == (20000, 2.0, 0.0)
+    W[39999, 0] = 0.5  # the runner-up is now an earlier chunk's best (row 5, 1.5), not the winning chunk's second
+    a, t, g = ol.argmax_streamed(lambda r0, r1: W[r0:r1], h, W.shape[0])
+    assert (a[0], t[0], g[0]) == (20000, 2.0, 0.5)
+    assert (a[0], t[0], g[0]) == tuple(v[0] for v in ol.argmax_gap(ol.logits(W, h)))
     rng = np.random.default_rng(9)
     W2 = rng.standard_normal((50000, 8))
     h2 = rng.standard_normal((3, 8))
@@ -252,6 +256,19 @@ def test_sliding_window_of_one_returns_own_value_and_wide_window_changes_nothing
         assert np.allclose(own[i], V[0, S + i], rtol=0, atol=1e-15)  # only the node itself survives the band
     full = oa.tree_verify_attention(q, K, V, par, S)
     assert np.allclose(oa.tree_verify_attention(q, K, V, par, S, window=S + T), full, rtol=1e-13, atol=1e-13)
+
+
+def test_sliding_mask_from_caller_boundary_is_inclusive():
+    # PR #1212 leaves a block untouched while offset + n <= window.  At equality an all-attend mask (whose future
+    # columns the band would block) comes back whole; one position past it, the band (numpy triangles) applies.
+    T = 5
+    for S in (0, 4, 11):
+        allatt = np.zeros((T, S + T))
+        assert np.array_equal(ot.sliding_mask_from_caller(allatt, S, S + T), allatt)
+        window = S + T - 1
+        ones = np.ones((T, S + T), dtype=bool)
+        inside = np.tril(ones, k=S) & np.triu(ones, k=S - window + 1)
+        assert np.array_equal(ot.sliding_mask_from_caller(allatt, S, window) == 0.0, inside)
 
 
 def test_sliding_mask_from_caller_properties():
@@ -352,6 +369,8 @@ def test_round_f16_hand_decoded_values(fn):
     r = lambda x: float(f(np.array([x]))[0])
     assert r(1.0 + 2.0 ** -11) == 1.0                     # tie -> even 0x3C00
     assert r(1.0 + 3 * 2.0 ** -11) == 1.0 + 2.0 ** -9     # tie -> even 0x3C02
+    assert r(1.0 + 2.0 ** -11 + 2.0 ** -30) == 1.0 + 2.0 ** -10  # just past the tie: up (one rounding, not via fp32)
+    assert r(1.0 + 2.0 ** -11 - 2.0 ** -30) == 1.0                # just short of it: down
     assert r(2049.0) == 2048.0 and r(2051.0) == 2052.0    # ulp 2 above 2048: ties to even
     with np.errstate(over="ignore"):
         assert r(65519.0) == 65504.0 and r(65520.0) == math.inf  # largest finite, then overflow

@@ -24,6 +24,11 @@ def test_hand_worked_draw():
     assert osm.draw(logits, 1.0, 3, 0.9, 0.7310) == 0
     assert osm.draw(logits, 1.0, 3, 0.9, 0.7312) == 1
     assert osm.draw(logits, 1.0, 3, 0.9, 0.999) == 1
+    # two equal logits: renormalised masses exactly [0.5, 0.5]; a uniform on the boundary belongs to the next
+    # token (the first whose cumulative mass exceeds u), zero to the first
+    assert osm.draw([0.0, 0.0], 1.0, 2, 1.0, 0.5) == 1
+    assert osm.draw([0.0, 0.0], 1.0, 2, 1.0, 0.0) == 0
+    assert osm.draw([0.0, 0.0], 1.0, 2, 1.0, np.nextafter(0.5, 0.0)) == 0
 
 
 def test_top_k_one_is_greedy_with_lowest_index_ties():
