@@ -76,6 +76,11 @@ def test_zero_token_and_error_bound():
     # a scale below half the smallest fp16 subnormal rounds to 0: such a token stores zeros
     codes, scale = oap.quantize_token(np.full(8, 2.0 ** -20))
     assert codes.tolist() == [0] * 8 and int(scale) == 0
+    # absmax 177.8 * 2^-24: the scale absmax / 127 = 1.4 * 2^-24 rounds to the smallest fp16 subnormal 2^-24 (bits
+    # 0x0001), so the extreme features divide to -177.8 and 177.8 and clip symmetrically to -127 and 127
+    a = float(np.float32(177.8 * 2.0 ** -24))
+    codes, scale = oap.quantize_token(np.array([-a, float(np.float32(a / 2)), a]))
+    assert int(scale) == 0x0001 and codes.tolist() == [-127, 89, 127]
     rng = np.random.default_rng(9)
     for _ in range(50):
         x = (rng.standard_normal(256) * rng.uniform(1e-3, 10)).astype(np.float32).astype(np.float64)

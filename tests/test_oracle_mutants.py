@@ -68,6 +68,12 @@ MUTANTS = [
      "emitted = [int(tokens[p]) for p in path]"),
     ("oracle.tree", "validation accepts a self-parent", "if not (0 <= parents[i] < i):",
      "if not (0 <= parents[i] <= i):"),
+    ("oracle.tree", "ancestor bits shifted by one", "sum(1 << j for j in", "sum(1 << (j + 1) for j in"),
+    ("oracle.tree", "depth counts the node itself", "return len(ancestors(parents, i)) - 1", "return len(ancestors(parents, i))"),
+    ("oracle.tree", "root check skipped", "if parents[0] != -1:\n        return BAD_ROOT",
+     "if parents[0] < -1:\n        return BAD_ROOT"),
+    ("oracle.tree", "tree columns placed at the start of the history mask", "m[:, offset:] = tree_mask(parents)",
+     "m[:, :n] = tree_mask(parents)"),
     ("oracle.tree", "chain walk stops one early", "while k < len(drafts) and", "while k + 1 < len(drafts) and"),
     # append
     ("oracle.append", "inverse frequencies with exponent -j/rot_dim", "-2.0 * j / rot_dim", "-1.0 * j / rot_dim"),
@@ -79,6 +85,8 @@ MUTANTS = [
     ("oracle.append", "node position S + index instead of S + depth", "S + _tree.depth(parents, i)", "S + i"),
     ("oracle.append", "quantisation scale absmax / 128", "amax / np.float32(127.0)", "amax / np.float32(128.0)"),
     ("oracle.append", "quantisation truncates", "np.rint(x32 / s32)", "np.trunc(x32 / s32)"),
+    ("oracle.append", "codes clipped to -128", "np.clip(q, -127, 127)", "np.clip(q, -128, 127)"),
+    ("oracle.append", "scale from the first feature instead of the absmax", "np.max(np.abs(x32))", "np.abs(x32[0])"),
     ("oracle.append", "new K rows all at the first node's position", "rope(k_new[i], pos[i],", "rope(k_new[i], pos[0],"),
     ("oracle.append", "appended fp16 rows double-rounded through fp32",
      '"""Round to the nearest fp16 value (ties to even), returned as fp64."""\n'
@@ -107,11 +115,19 @@ MUTANTS = [
     ("oracle.gather", "new length one short", "return b, tail_start + len(kept_offsets)",
      "return b, tail_start + len(kept_offsets) - 1"),
     ("oracle.gather", "trim keeps one position too few", "np.arange(length)", "np.arange(length - 1)"),
+    ("oracle.gather", "absolute form drops the last kept position", "return np.take(np.asarray(buf), kept, axis=axis)",
+     "return np.take(np.asarray(buf), kept[:-1], axis=axis)"),
+    ("oracle.gather", "identity test accepts any kept list", "return all(int(k) == j for j, k in enumerate(kept_offsets))",
+     "return True"),
     ("oracle.gather", "tail sources read from the start of the cache",
      "[tail_start + int(k) for k in kept_offsets]", "[int(k) for k in kept_offsets]"),
     # LM head
     ("oracle.lm_head", "argmax ties to the highest index", "idx = np.argmax(lg, axis=1)",
      "idx = lg.shape[1] - 1 - np.argmax(lg[:, ::-1], axis=1)"),
+    ("oracle.lm_head", "runner-up taken with the top still in", "rest[np.arange(lg.shape[0]), idx] = -np.inf",
+     "rest[np.arange(lg.shape[0]), 0] = -np.inf"),
+    ("oracle.lm_head", "logits scaled by the hidden size", "return np.asarray(h, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T",
+     "return np.asarray(h, dtype=np.float64) @ np.asarray(W, dtype=np.float64).T / np.asarray(h).shape[-1]"),
     ("oracle.lm_head", "a later chunk takes ties", "if ctop[r] > best[r]:", "if ctop[r] >= best[r]:"),
     ("oracle.lm_head", "streamed argmax forgets the chunk offset", "arg[r] = r0 + ci[r]", "arg[r] = ci[r]"),
     ("oracle.lm_head", "streamed gap drops the old best", "second[r] = max(best[r], csec[r])", "second[r] = csec[r]"),
@@ -133,6 +149,8 @@ MUTANTS = [
     ("oracle.tree_build", "depth cap one short", "depth[i] <= depth_max", "depth[i] < depth_max"),
     ("oracle.tree_build", "equal scores take the later candidate", "key=lambda i: (-float(score[i]), i)",
      "key=lambda i: (-float(score[i]), -i)"),
+    ("oracle.tree_build", "selected parents indexed by candidate, not by position", "[where[int(parents[c])] for c in order]",
+     "[int(parents[c]) for c in order]"),
     ("oracle.tree_build", "one node too many", "[: max(0, T - 1)]", "[: max(0, T)]"),
     ("oracle.tree_build", "top-k children ties to the higher index", "np.lexsort((np.arange(V), -x))",
      "np.lexsort((-np.arange(V), -x))"),
