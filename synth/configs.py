@@ -91,10 +91,16 @@ class Config:
     def algorithmic_bytes(self) -> int:
         return self.kv_bytes() + self.kv_scale_bytes() + self.lm_bytes()
 
-    def attention_flops(self) -> int:
-        """2 contractions (QK^T and PV) per query row over its visible keys."""
-        rows = self.n_layers * self.B * self.HQ * self.T
-        return 2 * 2 * rows * self.D * (self.S + (self.T + 1) / 2)
+    def attention_flops(self) -> float:
+        """2 contractions (QK^T and PV) per query row over its visible keys: on a full layer the S history keys and
+        on average (T + 1) / 2 block keys (a chain's mean; a branching tree's nodes see fewer), on a sliding-window
+        layer no more than its window."""
+        keys = 0.0
+        for l in range(self.n_layers):
+            w = self.layer_window(l)
+            full = self.S + (self.T + 1) / 2
+            keys += full if w == 0 else min(full, w)
+        return 2 * 2 * self.B * self.HQ * self.T * self.D * keys
 
     def lm_flops(self) -> int:
         return 2 * self.rows * self.V * self.H

@@ -40,6 +40,23 @@ def test_default_workload_is_the_largest_single_gpu_config():
     assert not bench.tensor_bound(configs.workload("specinfer16_27b_i8"))
 
 
+def test_sliding_layers_keep_the_attention_intensity():
+    # A sliding-window layer reads window + T - 1 positions and each row multiplies at most window keys, so its flop
+    # per KV byte stays near a full layer's; the 32-node hybrid stays bound by HBM, as the full workload is.
+    sys.path.insert(0, ROOT)
+    import bench
+    from synth import configs
+
+    full = configs.workload("eagle32x8_27b_f16")
+    intensity = lambda c: c.attention_flops() / (c.kv_bytes() + c.kv_scale_bytes())
+    every_layer = configs.with_sliding_layers(full, 1024, full.n_layers + 1)
+    assert all(every_layer.layer_window(l) == 1024 for l in range(full.n_layers))
+    assert 0.95 < intensity(every_layer) / intensity(full) <= 1.0
+    assert every_layer.attention_flops() < full.attention_flops() * 1024 / full.S
+    assert not bench.tensor_bound(configs.with_sliding_layers(full, 1024, 6))
+    assert bench.tensor_bound(configs.with_sliding_layers(configs.workload("eagle64x32_27b_i8"), 4096, 4))
+
+
 def test_percentiles():
     sys.path.insert(0, ROOT)
     import bench
