@@ -247,14 +247,15 @@ tsv_status tsv_tree_verify_attention(const tsv_attn_desc* d, void* workspace, si
  *   argmax  int32 [rows], out: index of the largest logit, ties -> lowest index.
  *   maxlogit float [rows] or NULL, out: that logit (fp32 accumulation).
  *   H % 64 == 0 (H % 256 == 0 for TSV_F16/TSV_BF16), 1 <= V < 2^31, rows >= 1.
- *   Up to 8 rows stream the head once through CUDA cores; more rows use the
- *   tcgen05 kernel (fp16 or bf16 operands, fp32 accumulation; 4-bit weights
- *   are dequantised to fp16 with one rounding, and hidden is rounded to fp16
- *   for fp16 and 4-bit heads).
+ *   fp16 and bf16 heads with up to 4 rows stream the head once through CUDA
+ *   cores; more rows, and 4-bit heads at any row count (H % 512 == 0, scales
+ *   and biases 16-byte aligned), use the tcgen05 kernels (fp16 or bf16
+ *   operands, fp32 accumulation; 4-bit weights are dequantised to fp16 with
+ *   one rounding, and hidden is rounded to fp16 for fp16 and 4-bit heads).
  */
 /* Workspace bytes for tsv_lm_head_argmax: 8 per hidden row (running bests), plus, when the tensor-core
- * kernel applies (rows > 8) to an fp16 or 4-bit head, an fp16 copy of hidden (rows * H * 2).  A smaller
- * workspace (at least 8 bytes per row) is accepted and selects the CUDA-core kernel. */
+ * kernel applies to an fp16 or 4-bit head, an fp16 copy of hidden (rows * H * 2, rounded up to 256).  A
+ * smaller workspace (at least 8 bytes per row) is accepted and selects the CUDA-core kernel. */
 size_t tsv_lm_head_workspace_size(int32_t rows, int32_t H, int32_t V, int32_t w_dtype);
 
 tsv_status tsv_lm_head_argmax(const void* hidden, int32_t rows, int32_t H, int32_t V, int32_t w_dtype,
@@ -312,14 +313,17 @@ tsv_status tsv_sample_nucleus(const float* logits, int32_t rows, int32_t V, floa
  *   one array, so calls whose work overlaps on the GPU (on different streams,
  *   or from different host threads) race and give wrong results; serialise
  *   them on one stream.
- *   Speed: the array holds only the running bests, not the fp16 copy of hidden
- *   that the tensor-core kernel needs for fp16 and 4-bit heads.  For those two
- *   formats every call therefore takes the CUDA-core kernel, which streams the
- *   whole head once per 8 hidden rows: ceil(rows / 8) passes (a 4-bit head of
- *   248,320 x 5120 rows costs about 0.1 ms per pass, so 4096 rows take about
- *   50 ms instead of a few).  bf16 heads above 8 rows keep the tensor-core
- *   kernel.  Callers with many rows and an fp16 or 4-bit head should use
- *   tsv_lm_head_argmax with a workspace.
+ *   Speed: the array is also the call's workspace, and for fp16 and 4-bit
+ *   heads the tensor-core kernel needs an fp16 copy of hidden beside the
+ *   bests (rows * H * 2 bytes, rounded up to 256, after 8 bytes per row
+ *   rounded up to 256).  When that does not fit the 32 KiB (H = 5120: more
+ *   than 3 rows), the call takes the CUDA-core kernel instead, which streams
+ *   the whole head once per 8 hidden rows and, for a 4-bit head, dequantises
+ *   every weight again for each row (248,320 x 5120 4-bit head: about 2.1 ms
+ *   per 8-row pass, so 4096 rows take about a second instead of a few ms).
+ *   bf16 heads need no copy and keep the tensor-core kernel.  Callers with
+ *   many rows and an fp16 or 4-bit head should use tsv_lm_head_argmax with a
+ *   workspace.
  */
 #define TSV_NOALLOC_MAX_ROWS 4096
 

@@ -3,8 +3,9 @@
 Some callers cannot allocate device memory themselves (their host framework owns every device buffer through
 its own pool, or their latency budget cannot absorb cudaMalloc's implicit synchronisation).  For them the
 library keeps the LM head's scratch in a fixed device array.  This test compares that entry point with the
-workspace entry point on four calls in a row, with different row counts so that entries left over from one
-call would show up in the next, in every weight format, above and below the 8 rows of one CUDA-core pass.
+workspace entry point on five calls in a row, with different row counts so that entries left over from one
+call would show up in the next, in every weight format, on both sides of the point where the tensor-core
+kernel's fp16 copy of hidden no longer fits the fixed array.
 It runs last in the suite and also passes alone in a fresh process.
 """
 import ctypes as C
@@ -24,10 +25,11 @@ def test_noalloc_matches_workspace_entry_point(gpu_lib):
     lib = gpu_lib.load()
     stream = C.c_void_p(torch.cuda.current_stream().cuda_stream)
     V, H = 5003, 512
-    # bf16 above 8 rows (tensor-core kernel), 4-bit below 8, and 4-bit and fp16 above 8 rows: there the fixed
-    # array has no room for the tensor-core kernel's fp16 copy of hidden, so the call streams the head once per
-    # 8 rows through the CUDA-core kernel while the workspace call takes the tensor-core one
-    for call, (rows, w_dtype) in enumerate([(13, 1), (5, 3), (20, 3), (20, 0)]):
+    # 13 bf16 rows and 3 4-bit rows take the tensor-core kernels in both calls (bf16 needs no copy of hidden, and
+    # 3 x 512 x 2 bytes fit the 32 KiB array); 2 fp16 rows take the CUDA-core GEMV in both; 40 4-bit and 37 fp16
+    # rows overflow the array (40 KB, 37 KB), so the no-alloc call streams the head once per 8 rows through the
+    # CUDA-core kernel while the workspace call takes the tensor-core one
+    for call, (rows, w_dtype) in enumerate([(13, 1), (3, 3), (40, 3), (2, 0), (37, 0)]):
         rng = np.random.default_rng(100 + call)
         target = rng.integers(0, V, size=rows)
         if w_dtype == 3:

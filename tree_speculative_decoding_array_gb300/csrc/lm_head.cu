@@ -322,7 +322,8 @@ static tsv_status lm_head_run(const char* name, const void* hidden, int32_t rows
         return fail(TSV_ECAPACITY, "%s: workspace %zu < %zu bytes", name, ws_bytes, best_bytes(rows));
     unsigned long long* best = (unsigned long long*)workspace;
     launch_pdl(lm_zero_best_kernel, std::min((rows + 255) / 256, sm_count()), 256, 0, stream, best, rows);
-    // More than one 8-row pass: the tensor-core kernel, when the workspace also holds what it needs.
+    // The tensor-core kernels where they apply (every 4-bit head; a 16-bit head with more rows than one GEMV
+    // pass serves), when the workspace also holds what they need.
     const bool sb_aligned = w_dtype != TSV_Q4_G64 || ((((uintptr_t)scales | (uintptr_t)biases) & 15) == 0);
     if (lm_tc_applies(rows, H, V, w_dtype) && sb_aligned &&
         ws_bytes >= best_bytes(rows) + lm_tc_extra_bytes(rows, H, w_dtype)) {

@@ -2,8 +2,9 @@
 //
 // Same operation as the CUDA-core GEMV in lm_head.cu (mlxcel issue #1185,
 // "Phase 2" item 2a: projection fused with the argmax, logits never written;
-// "Phase 3": affine group-64 4-bit weights), for row counts where streaming
-// the head once per 8 rows would make the CUDA-core path compute-bound.
+// "Phase 3": affine group-64 4-bit weights), for every 4-bit head and for
+// 16-bit heads with more rows than one pass of the CUDA-core GEMV serves: there
+// the GEMV would be bound by its arithmetic or stream the head more than once.
 //
 // Swap-AB: one MMA tile is D[128 vocabulary rows x NP hidden rows] =
 // W_tile[128 x 64] . hidden_chunk[NP x 64]^T, accumulated over H / 64
@@ -957,10 +958,18 @@ size_t lm_tc_extra_bytes(int rows, int H, int w_dtype) {
 }
 
 // Shape conditions of the tensor-core paths.  The 4-bit path reads scales and biases 8 groups of a row at a
-// time, so H must be a multiple of 512 and (checked by the caller) both pointers 16-byte aligned.
+// time, so H must be a multiple of 512 and (checked by the caller) both pointers 16-byte aligned.  Row counts:
+// a 4-bit head takes the tensor-core kernels at every count, since the CUDA-core GEMV dequantises each weight
+// again for every row and is bound by that arithmetic (248,320 x 5120 head: 0.32 ms at 1 row, 0.82 at 3, 2.1 at
+// 8, against 0.19 ms for the few-row kernel at 1 to 16 rows, the rows padded to the MMA's 16); a 16-bit head
+// stays on the GEMV while one pass of it serves every row (up to kLmGemvRows16 rows, at the HBM rate: 0.35-0.37
+// ms for 2.54 GB), above that the GEMV streams the head twice (0.73 ms at 8 rows, against 0.39 ms for the
+// tensor-core kernel).
+constexpr int kLmGemvRows16 = 4;
 bool lm_tc_applies(int rows, int H, int V, int w_dtype) {
-    if (rows <= 8 || V < 1) return false;
-    return w_dtype == TSV_Q4_G64 ? H % (kLmKB * kQ4KBPerStage) == 0 : H % kLmKB == 0;
+    if (rows < 1 || V < 1) return false;
+    if (w_dtype == TSV_Q4_G64) return H % (kLmKB * kQ4KBPerStage) == 0;
+    return rows > kLmGemvRows16 && H % kLmKB == 0;
 }
 
 static tsv_status launch_lm_q4(const void* hidden, int rows, int H, int V, const void* W, const void* scales,
