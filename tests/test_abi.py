@@ -110,3 +110,11 @@ def test_host_validation_refuses_without_launching():
     assert lib.tsv_tree_append(C.byref(a), C.c_void_p(16), None, None) == _abi.EUNSUPPORTED
     assert lib.tsv_lm_head_workspace_size(3, 256, 1000, 1) >= 24
     assert lib.tsv_lm_head_workspace_size(16, 512, 1000, 3) >= 16 * 8 + 16 * 512 * 2  # fp16 copy of hidden
+    # which kernel a row count selects shows in the workspace it asks for: the tensor-core kernels take every
+    # 4-bit head whose H is a multiple of 512 (an fp16 copy of hidden beside the bests) and 16-bit heads above 4
+    # rows (fp16 heads need the copy, bf16 heads none); below, the CUDA-core GEMV needs only the bests
+    ws = lib.tsv_lm_head_workspace_size
+    assert ws(1, 512, 1000, 3) == 256 + 1024 and ws(3, 512, 1000, 3) == 256 + 3072
+    assert ws(3, 256, 1000, 3) == 256  # H not a multiple of 512: GEMV
+    assert ws(4, 256, 1000, 0) == 256 and ws(5, 256, 1000, 0) == 256 + 2560
+    assert ws(8, 256, 1000, 1) == 256
