@@ -959,9 +959,9 @@ size_t lm_tc_extra_bytes(int rows, int H, int w_dtype) {
 
 // Shape conditions of the tensor-core paths.  The 4-bit path reads scales and biases 8 groups of a row at a
 // time, so H must be a multiple of 512 and (checked by the caller) both pointers 16-byte aligned.  Row counts:
-// a 4-bit head takes the tensor-core kernels at every count, since the CUDA-core GEMV dequantises each weight
-// again for every row and is bound by that arithmetic (248,320 x 5120 head: 0.32 ms at 1 row, 0.82 at 3, 2.1 at
-// 8, against 0.19 ms for the few-row kernel at 1 to 16 rows, the rows padded to the MMA's 16); a 16-bit head
+// a 4-bit head takes the tensor-core kernels at every count: the CUDA-core GEMV runs below the HBM rate even at
+// one row and dequantises each weight again for every row (248,320 x 5120 head: 0.32 ms at 1 row, 0.82 at 3,
+// 2.1 at 8, against 0.19 ms for the few-row kernel at 1 to 16 rows, the rows padded to the MMA's 16); a 16-bit head
 // stays on the GEMV while one pass of it serves every row (up to kLmGemvRows16 rows, at the HBM rate: 0.35-0.37
 // ms for 2.54 GB), above that the GEMV streams the head twice (0.73 ms at 8 rows, against 0.39 ms for the
 // tensor-core kernel).
