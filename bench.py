@@ -44,11 +44,11 @@ DEFAULT_ROUND = {"chain3_27b_bf16": 2}  # the round that accepts the whole chain
 # launch over 16 layers x 32 sequences reads and writes 128 times that (every unit streams its own keys).
 TRAFFIC = {
     # the chain's bf16 LM head (the CUDA-core GEMV), one launch at full size
-    "chain3_27b_bf16": {"kernel": "lm", "src": ("lm_head.cu", "common.cuh"), "hash": "2530ef189b03e4bc",
+    "chain3_27b_bf16": {"kernel": "lm", "src": ("lm_head.cu", "common.cuh"), "hash": "46f6f865d5feba27",
                         "bytes": 2543127040 + 2785024},
     # the 16-node workload's 4-bit LM head (lm_q4s_kernel, 16 rows), one launch at full size
     "specinfer16_27b_i8": {"kernel": "lm", "src": ("lm_head.cu", "lm_head_tc.cu", "common.cuh", "tc.cuh"),
-                           "hash": "0218d4bcb34f837a", "bytes": 715418368 + 3241984},
+                           "hash": "07d6b485b4e260fc", "bytes": 715418368 + 3241984},
     "eagle64x32_27b_i8": {"kernel": "attn", "src": ("attention.cu", "attention_tc.cu", "common.cuh", "tc.cuh"),
                           "hash": "af0faa37c76ef2ad", "bytes": (1086705920 + 2978048) * 128},
 }
