@@ -49,6 +49,9 @@ TRAFFIC = {
     # the 16-node workload's 4-bit LM head (lm_q4s_kernel, 16 rows), one launch at full size
     "specinfer16_27b_i8": {"kernel": "lm", "src": ("lm_head.cu", "lm_head_tc.cu", "common.cuh", "tc.cuh"),
                            "hash": "07d6b485b4e260fc", "bytes": 715418368 + 3241984},
+    # the 32-node workload's attention (attn_tcw_kernel, 16 layers x 8 sequences), one launch at full size
+    "eagle32x8_27b_f16": {"kernel": "attn", "src": ("attention.cu", "attention_tc.cu", "common.cuh", "tc.cuh"),
+                          "hash": "af0faa37c76ef2ad", "bytes": 17298162176 + 49117952},
     "eagle64x32_27b_i8": {"kernel": "attn", "src": ("attention.cu", "attention_tc.cu", "common.cuh", "tc.cuh"),
                           "hash": "af0faa37c76ef2ad", "bytes": (1086705920 + 2978048) * 128},
 }
