@@ -279,7 +279,7 @@ def q4_pack(codes):
 
 
 @pytest.mark.parametrize("w_dtype", [0, 1, 3])
-@pytest.mark.parametrize("rows,V,H", [(1, 1000, 256), (3, 4099, 512), (5, 777, 256), (8, 2048, 1024), (13, 3001, 256),
+@pytest.mark.parametrize("rows,V,H", [(1, 1000, 256), (2, 1536, 5120), (3, 4099, 512), (5, 777, 256), (8, 2048, 1024), (13, 3001, 256),
                                       (16, 1280, 5120), (17, 257, 512), (29, 3001, 1024), (64, 5003, 512),
                                       (200, 2303, 256), (257, 1000, 1024),
                                       (600, 700, 256), (600, 700, 512)])
